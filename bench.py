@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated temporal scan layer: forward + backward on GB300.
+
+One step = m2scan_fwd + m2scan_bwd over one batch of the 8192-sample workload
+(K=8, SH2=256, D=16, fp32), inputs resident in HBM. L2 is flushed (a 512 MiB
+write) before every timed forward and every timed backward, outside the
+timed intervals, so both read their inputs from HBM. Each rank times K steps
+with CUDA events on its stream; the line reports the maximum over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
+(the only reference the layer has) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd samples/s (B=8192, K=8, SH2=256, D=16)"
+UNIT = "samples/s"
+FLUSH_BYTES = 512 << 20
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+               "clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="pages")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ multi-rank plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, values, device="cpu"):
+    """Elementwise maximum of a list of floats over all ranks."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_throughput(units_per_rank: int, world: int, seconds_max: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * world / seconds_max if seconds_max > 0 else 0.0
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + CLOCK_QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, gpus):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [s.strip() for s in line.split(",")]
+                if len(p) < 10:
+                    continue
+                try:
+                    rows.append(dict(idx=int(p[0]), sm=float(p[1]), smax=float(p[2]),
+                                     util=float(p[4]) if p[4] not in ("[N/A]", "") else 0.0,
+                                     hw=p[6], hwt=p[7], swt=p[8], swp=p[9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        rows = [r for r in rows if r["idx"] in gpus] or rows
+        load = [r for r in rows if r["util"] >= 50.0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median([r["sm"] for r in load]) if load else None,
+                "sm_max_mhz": max((r["smax"] for r in load), default=None),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_ssm_temporal_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[kernel]
+        if t.get("kernel_sha") == kernel_sources_sha():
+            return float(t["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+def cpu_baseline(x, seconds: float):
+    """The fp64 oracle on this host's cores, repeated on the workload batch for ~seconds."""
+    import oracle
+    threads = oracle.default_threads()
+    B = x["h_history"].shape[0]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"], x["W_O"],
+                       x["tw"], n_threads=threads)
+        oracle.backward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"], x["W_O"],
+                        x["tw"], x["d_h_enriched"], n_threads=threads)
+        done += B
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d passes of fwd+bwd over the full %d-sample batch (%.1f s)"
+                      % (done // B, B, el)}
+
+
+# -------------------------------------------------------------- native arm
+
+def run_native(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import gated_ssm_temporal_gb300 as g
+    from gated_ssm_temporal_gb300 import build as gbuild
+    from gated_ssm_temporal_gb300.workloads import WORKLOADS, algorithmic_bytes, make_inputs
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    gbuild.build()
+    g.load_library()
+    base = WORKLOADS[args.workload]
+    w = base.with_batch(base.B, seed=base.seed + rank)
+    B, K, SH2, D = w.B, w.K, w.SH2, w.D
+    x = make_inputs(w)
+    dev = torch.device("cuda", local)
+    d = {k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v) for k, v in x.items()}
+    y = torch.empty((B, SH2), device=dev)
+    outs = g.alloc_bwd_outputs(B, K, SH2, D, dev)
+    ws = g.alloc_workspace(B, K, SH2, D, dev)
+    flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        g.fwd(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"], out=y,
+              stream=stream)
+
+    def bwd():
+        g.bwd(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"],
+              d["d_h_enriched"], outs=outs, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        fwd()
+        flush.zero_()
+        bwd()
+    torch.cuda.synchronize()
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    sampler = ClockSampler()
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(dist, local)
+    torch.cuda.synchronize()
+    launches_before = 0
+    wall0 = time.perf_counter()
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd()
+        launches_before += g.m2scan_last_launch_count()
+        ev[i][1].record(stream)
+        flush.zero_()
+        ev[i][2].record(stream)
+        bwd()
+        launches_before += g.m2scan_last_launch_count()
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop(gpus=list(range(max(world, 1)))) if rank == 0 else None
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    bwd_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / n
+    fwd_ms, bwd_ms = max_over_ranks(dist, [fwd_ms, bwd_ms], device=dev)
+    step_ms = fwd_ms + bwd_ms
+    value = whole_job_throughput(B, world, step_ms / 1e3)
+
+    # end to end: pinned host inputs in, every output back to pinned host memory
+    host_in = {k: torch.from_numpy(x[k]).pin_memory() for k in ("h_history", "h_s2", "d_h_enriched")}
+    host_out = {"h_enriched": torch.empty((B, SH2)).pin_memory()}
+    host_out.update({k: torch.empty(tuple(v.shape)).pin_memory() for k, v in outs.items()})
+    h2d = sum(t.numel() * 4 for t in host_in.values())
+    d2h = sum(t.numel() * 4 for t in host_out.values())
+
+    def e2e_step():
+        for k, t in host_in.items():
+            d[k].copy_(t, non_blocking=True)
+        fwd()
+        bwd()
+        host_out["h_enriched"].copy_(y, non_blocking=True)
+        for k, t in outs.items():
+            host_out[k].copy_(t, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    (e2e_ms,) = max_over_ranks(dist, [e2e_ms], device=dev)
+
+    if rank != 0:
+        return
+    ab = algorithmic_bytes(B, K, SH2)
+    peak, peak_src = measured_peaks()
+    achieved = ab["bwd"] / (bwd_ms / 1e3) / 1e9
+    traffic = recorded_traffic("m2scan_bwd")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g per rank" % (w.name, B, K, SH2, D,
+                                                                             w.tw),
+                   "B": B, "K": K, "SH2": SH2, "D": D, "parallelism": "replicas x%d" % world,
+                   "l2": "flushed (512 MiB write) before every timed fwd and every timed bwd"},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "hbm_gbs": ab["total"] / (step_ms / 1e3) / 1e9,
+        "hbm_frac_of_measured": ab["total"] / (step_ms / 1e3) / 1e9 / peak,
+        "roofline": {"kernel": "m2scan_bwd (fused backward + slot reduction)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "peak_source": peak_src + " hbm_gbs burst",
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes": ab["bwd"]},
+        "e2e": {"value": whole_job_throughput(B, world, e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_before,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+        "pages_h100_context_ms": {"fwd": 22.0, "bwd": 1567.0},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from gated_ssm_temporal_gb300.workloads import WORKLOADS, make_inputs
+    base = WORKLOADS[args.workload]
+    threads = oracle.default_threads()
+    x = make_inputs(base)
+    # size each step so the whole run stays within about two minutes
+    cal = {k: (v[:64] if hasattr(v, "shape") and v.shape[0] == base.B else v) for k, v in x.items()}
+    t0 = time.perf_counter()
+    oracle.forward(cal["h_history"], cal["h_s2"], cal["W_A"], cal["W_B"], cal["W_C"], cal["W_O"],
+                   cal["tw"], n_threads=threads)
+    oracle.backward(cal["h_history"], cal["h_s2"], cal["W_A"], cal["W_B"], cal["W_C"],
+                    cal["W_O"], cal["tw"], cal["d_h_enriched"], n_threads=threads)
+    per_sample = max((time.perf_counter() - t0) / 64, 1e-7)
+    budget = min(5.0, 120.0 / max(1, args.steps + args.warmup))
+    ns = int(max(16, min(base.B, budget / per_sample)))
+    xs = {k: (v[:ns] if hasattr(v, "shape") and v.shape[0] == base.B else v) for k, v in x.items()}
+
+    def step():
+        oracle.forward(xs["h_history"], xs["h_s2"], xs["W_A"], xs["W_B"], xs["W_C"], xs["W_O"],
+                       xs["tw"], n_threads=threads)
+        oracle.backward(xs["h_history"], xs["h_s2"], xs["W_A"], xs["W_B"], xs["W_C"], xs["W_O"],
+                        xs["tw"], xs["d_h_enriched"], n_threads=threads)
+
+    for _ in range(max(0, args.warmup)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = ns * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g" % (base.name, base.B, base.K,
+                                                                    base.SH2, base.D, base.tw),
+                   "B": base.B, "K": base.K, "SH2": base.SH2, "D": base.D},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "first %d of the %d samples per step" % (ns, base.B)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_native(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+// Generic kernels of the gated temporal scan layer, for shapes outside the
+// fused fast path (e.g. D = 64 with SH2 = 512), and the slot reduction shared
+// by both backward paths.
+//
+// The generic kernels keep one sample at a time in shared memory: each CTA
+// owns the samples [c*B/P, (c+1)*B/P) and the weight-gradient slot c. Every
+// slot entry is owned by one fixed thread (entry e by thread e % 256), so the
+// partial sums are formed in a fixed order without atomics.
+#include "m2scan_device.cuh"
+#include "m2scan_internal.h"
+
+namespace m2scan {
+namespace {
+
+template <bool BWD>
+__global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) {
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  const int K = a.K, SH2 = a.SH2, D = a.D, TD = 2 * D;
+  float* sAB = sm;            // [K][2D]: A|B, then sigmoid|x, then dA|dB
+  float* sHs = sAB + K * TD;  // [SH2]
+  float* sG = sHs + SH2;      // [SH2]
+  float* sC = sG + SH2;       // [D]
+  float* sCtx = sC + D;
+  float* sDctx = sCtx + D;
+  float* sDC = sDctx + D;
+  const int tid = threadIdx.x;
+  const int P = gridDim.x, cta = blockIdx.x;
+  const long long b0 = a.B * cta / P, b1 = a.B * (cta + 1) / P;
+  const int n = SH2 * D;
+  float* slot = BWD ? a.ws + static_cast<size_t>(cta) * 4 * n : nullptr;
+  if (BWD)
+    for (int e = tid; e < 4 * n; e += kThreads) slot[e] = 0.f;
+
+  for (long long b = b0; b < b1; ++b) {
+    const float* h = a.h_history + b * K * SH2;
+    for (int j = tid; j < SH2; j += kThreads) {
+      sHs[j] = a.h_s2[b * SH2 + j];
+      if (BWD) sG[j] = a.g[b * SH2 + j];
+    }
+    __syncthreads();
+    // projections A|B (one output per thread and step), C and d_ctx
+    for (int e = tid; e < K * TD; e += kThreads) {
+      const int t = e / TD, k = e - (e / TD) * TD;
+      const float* W = k < D ? a.W_A : a.W_B;
+      const int col = k < D ? k : k - D;
+      const float* hr = h + static_cast<size_t>(t) * SH2;
+      float s = 0.f;
+      for (int j = 0; j < SH2; ++j) s = fmaf(hr[j], W[j * D + col], s);
+      sAB[e] = s;
+    }
+    for (int d = tid; d < D; d += kThreads) {
+      float c = 0.f;
+      for (int j = 0; j < SH2; ++j) c = fmaf(sHs[j], a.W_C[j * D + d], c);
+      sC[d] = c;
+      if (BWD) {
+        float o = 0.f;
+        for (int j = 0; j < SH2; ++j) o = fmaf(sG[j], a.W_O[static_cast<size_t>(d) * SH2 + j], o);
+        sDctx[d] = a.tw * o;
+      }
+    }
+    __syncthreads();
+    // scan (and reverse scan)
+    for (int d = tid; d < D; d += kThreads) {
+      float x = 0.f;
+      for (int t = 0; t < K; ++t) {
+        float* pr = sAB + t * TD;
+        const float sg = sigmoidf_(pr[d]);
+        x = fmaf(sg, x, pr[D + d]);
+        if (BWD) {
+          pr[d] = sg;
+          pr[D + d] = x;
+        }
+      }
+      sCtx[d] = sC[d] * x;
+      if (BWD) {
+        sDC[d] = sDctx[d] * x;
+        float dx = sDctx[d] * sC[d];
+        for (int t = K - 1; t >= 0; --t) {
+          float* pr = sAB + t * TD;
+          const float sg = pr[d];
+          const float xprev = t > 0 ? pr[D + d - TD] : 0.f;
+          pr[D + d] = dx;
+          pr[d] = dx * xprev * (sg * (1.f - sg));
+          dx *= sg;
+        }
+      }
+    }
+    __syncthreads();
+    if (!BWD) {
+      for (int j = tid; j < SH2; j += kThreads) {
+        float o = 0.f;
+        for (int d = 0; d < D; ++d) o = fmaf(sCtx[d], a.W_O[static_cast<size_t>(d) * SH2 + j], o);
+        a.out0[b * SH2 + j] = fmaf(a.tw, o, sHs[j]);
+      }
+    } else {
+      for (int e = tid; e < K * SH2; e += kThreads) {
+        const int t = e / SH2, j = e - (e / SH2) * SH2;
+        const float* pr = sAB + t * TD;
+        float s = 0.f;
+        for (int d = 0; d < D; ++d) {
+          s = fmaf(pr[d], a.W_A[j * D + d], s);
+          s = fmaf(pr[D + d], a.W_B[j * D + d], s);
+        }
+        a.out0[(b * K + t) * SH2 + j] = s;
+      }
+      for (int j = tid; j < SH2; j += kThreads) {
+        float s = sG[j];
+        for (int d = 0; d < D; ++d) s = fmaf(sDC[d], a.W_C[j * D + d], s);
+        a.out1[b * SH2 + j] = s;
+      }
+      for (int e = tid; e < n; e += kThreads) {
+        const int j = e / D, d = e - (e / D) * D;
+        float sa = 0.f, sb = 0.f;
+        for (int t = 0; t < K; ++t) {
+          const float hv = h[static_cast<size_t>(t) * SH2 + j];
+          sa = fmaf(hv, sAB[t * TD + d], sa);
+          sb = fmaf(hv, sAB[t * TD + D + d], sb);
+        }
+        slot[e] += sa;
+        slot[n + e] += sb;
+        slot[2 * n + e] += sHs[j] * sDC[d];
+      }
+      for (int e = tid; e < n; e += kThreads) {
+        const int d = e / SH2, j = e - (e / SH2) * SH2;
+        slot[3 * n + e] += a.tw * sCtx[d] * sG[j];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// dW[e] = sum over slots p = 0..P-1 of ws[p][e], added in a fixed order:
+// eight interleaved partial sums per element (slots g, g+8, ...), then the
+// eight partials in order. Each CTA covers 128 consecutive elements.
+__global__ void __launch_bounds__(kThreads) reduce_kernel(const float* __restrict__ ws, int P,
+                                                          int n, float* dW_A, float* dW_B,
+                                                          float* dW_C, float* dW_O) {
+  __shared__ float4 red[8][32];
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const long long total = 4ll * n;
+  const long long e0 = static_cast<long long>(blockIdx.x) * 128 + 4 * lane;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (e0 < total) {
+    for (int p = grp; p < P; p += 8) {
+      const float4 v = *reinterpret_cast<const float4*>(ws + static_cast<size_t>(p) * total + e0);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+  }
+  red[grp][lane] = s;
+  __syncthreads();
+  if (grp == 0 && e0 < total) {
+    float4 r = red[0][lane];
+    for (int g = 1; g < 8; ++g) {
+      const float4 v = red[g][lane];
+      r.x += v.x; r.y += v.y; r.z += v.z; r.w += v.w;
+    }
+    const int which = static_cast<int>(e0 / n);
+    const int i = static_cast<int>(e0 - static_cast<long long>(which) * n);
+    float* out = which == 0 ? dW_A : (which == 1 ? dW_B : (which == 2 ? dW_C : dW_O));
+    *reinterpret_cast<float4*>(out + i) = r;
+  }
+}
+
+}  // namespace
+
+size_t generic_smem_bytes(bool bwd, int K, int SH2, int D) {
+  (void)bwd;
+  return sizeof(float) * (static_cast<size_t>(K) * 2 * D + 2 * static_cast<size_t>(SH2) + 4 * D);
+}
+
+cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem,
+                           cudaStream_t stream) {
+  if (bwd)
+    generic_kernel<true><<<grid, kThreads, smem, stream>>>(a);
+  else
+    generic_kernel<false><<<grid, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float* dW_B,
+                          float* dW_C, float* dW_O, cudaStream_t stream) {
+  const long long total = 4ll * n;
+  const int grid = static_cast<int>((total + 127) / 128);
+  reduce_kernel<<<grid, kThreads, 0, stream>>>(ws, slots, n, dW_A, dW_B, dW_C, dW_O);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_generic_kernels(int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(generic_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(generic_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             max_smem);
+  return e;
+}
+
+}  // namespace m2scan

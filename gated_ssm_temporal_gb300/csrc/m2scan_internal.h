@@ -1,0 +1,87 @@
+// Internal declarations shared by the m2scan host API and its kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace m2scan {
+
+constexpr int kThreads = 256;     // threads per CTA, every kernel
+constexpr int kStages = 3;        // depth of the copy ring of the fast kernels
+constexpr int kMaxSlots = 152;    // CTAs (= weight-gradient slots) per call, at most
+constexpr int kTileRows = 128;    // rows (samples x K) per pass-1 tile, at most
+constexpr int kChunk = 32;        // SH2 columns per pass-1 chunk (128 bytes)
+constexpr int kRowsPerItem = 32;  // h_history rows per pass-2 row item
+constexpr int kMaxSampleItem = 16;
+
+// Arguments of the fused kernels. The three tensor maps describe h_history as
+// a 3-D tensor [SH2, K, B] (box [32, K, S_max]) and h_s2 / d_h_enriched as 2-D
+// tensors [SH2, B] (box [32, S_max]), all with 128-byte swizzle. Offsets are
+// bytes from the 1024-aligned start of dynamic shared memory.
+struct alignas(128) FastArgs {
+  CUtensorMap tm_h;
+  CUtensorMap tm_hs;
+  CUtensorMap tm_g;
+  const float* h_history;
+  const float* h_s2;
+  const float* g;
+  const float* W_A;
+  const float* W_B;
+  const float* W_C;
+  const float* W_O;
+  float* out0;  // forward: h_enriched; backward: d_h_history
+  float* out1;  // backward: d_h_s2
+  float* ws;    // backward: weight-gradient slots [P][4][SH2*D]
+  unsigned* err;
+  long long B;
+  int K;
+  int SH2;
+  int S_max;    // samples per tile, at most (also the TMA box depth)
+  int SG;       // samples per pass-2 sample item
+  int stage_bytes;
+  int hc_bytes;  // bytes of the h_history box (S_max*K rows of 128 bytes)
+  int sc_bytes;  // bytes of one h_s2 / d_h_enriched box (S_max rows)
+  int off_S;     // offset of the h_s2 box inside a chunk stage
+  int off_G;     // offset of the d_h_enriched box inside a chunk stage
+  int off_wab, off_wct, off_wo, off_p, off_cs, off_ctx, off_dctx, off_dc, off_bar;
+  int smem_bytes;
+  float tw;
+};
+
+struct GenericArgs {
+  const float* h_history;
+  const float* h_s2;
+  const float* g;
+  const float* W_A;
+  const float* W_B;
+  const float* W_C;
+  const float* W_O;
+  float* out0;
+  float* out1;
+  float* ws;
+  long long B;
+  int K;
+  int SH2;
+  int D;
+  float tw;
+};
+
+// Fast path shape limits (see m2scan.h).
+bool fast_path_ok(int K, int SH2, int D);
+// Fills the shared-memory plan of a fast kernel. Returns false if it does not fit.
+bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a);
+size_t generic_smem_bytes(bool bwd, int K, int SH2, int D);
+
+cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem,
+                           cudaStream_t stream);
+cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float* dW_B,
+                          float* dW_C, float* dW_O, cudaStream_t stream);
+cudaError_t prepare_kernels(int max_smem_optin);
+
+unsigned* device_error_word();  // device address of the error word (current device)
+
+}  // namespace m2scan

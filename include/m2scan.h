@@ -1,0 +1,143 @@
+/*
+ * m2scan — C ABI of the gated temporal scan layer (forward and backward) for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer, per sample b (t = 0 is the oldest history step and is scanned
+ * first; SH2 = trunk width, D = STATE_D, K = history length):
+ *
+ *   A[t,:]  = h_history[b,t,:] . W_A     B[t,:] = h_history[b,t,:] . W_B
+ *   C       = h_s2[b,:] . W_C
+ *       ("Custom Kernel Optimization -- cuBLAS Projections + Batch-Parallel
+ *        Scans", Design 1, Step 1: the three projections)
+ *   x_{-1} = 0,  x_t = sigmoid(A[t]) * x_{t-1} + B[t]        (elementwise)
+ *       (same section, Step 2; "Custom Kernel Optimization Implementation
+ *        Plan", Task 1 Step 3)
+ *   ctx = C * x_{K-1}                                         (elementwise)
+ *   h_enriched[b,:] = h_s2[b,:] + tw * (ctx . W_O)
+ *       (the pages leave this output step open, design spec Design 1 Step 3;
+ *        the layer fixes it as a residual plus a [D,SH2] output projection
+ *        scaled by the scalar tw)
+ *
+ * and the backward is the reverse scan of the implementation plan's Task 2
+ * (d_gate = dx * x_{t-1} * sigmoid', dx <- dx * gate), extended to every
+ * input: dW_A, dW_B, dW_C, dW_O, d_h_history and d_h_s2.
+ *
+ * Conventions for every call:
+ *   - All tensors are fp32, row-major and contiguous:
+ *       h_history, d_h_history  [B, K, SH2]
+ *       h_s2, h_enriched, d_h_enriched, d_h_s2  [B, SH2]
+ *       W_A, W_B, W_C, dW_A, dW_B, dW_C  [SH2, D]
+ *       W_O, dW_O  [D, SH2]
+ *   - Every pointer is a DEVICE pointer (cudaMalloc or equivalent) on the
+ *     current device, 16-byte aligned. The caller owns every buffer; the
+ *     library allocates nothing on the device and keeps no pointer after the
+ *     call returns.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
+ *     synchronise. Outputs are OVERWRITTEN, never accumulated into.
+ *   - Outputs must not overlap any input or each other (checked on the host).
+ *   - All argument checks run on the host before anything is launched; a
+ *     failing check launches nothing and returns the status.
+ *   - Results are bit-identical from run to run for the same inputs and
+ *     shapes on the same GPU model: the weight gradients are summed over a
+ *     fixed sample-to-slot assignment and the slots are added in slot order
+ *     (the deterministic two-phase reduction of "Phase 3 Kernel Optimization
+ *     Implementation Plan", Task 2), with no floating-point atomics.
+ *   - Supported shapes: B >= 0, K >= 1, SH2 >= 4 with SH2 % 4 == 0, D >= 1,
+ *     and per-sample scratch of 4*K*2*D bytes within shared memory (the
+ *     fallback path): K * D <= 16384. A fused fast path is used when D is 4,
+ *     8 or 16, SH2 % 32 == 0, SH2 * D <= 4096 and K <= 128.
+ */
+#ifndef M2SCAN_H
+#define M2SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* m2scan_stream_t;
+
+typedef enum {
+  M2SCAN_OK = 0,
+  M2SCAN_ERR_NULL = 1,        /* a required pointer is NULL */
+  M2SCAN_ERR_SHAPE = 2,       /* B < 0, K < 1, SH2 < 4, SH2 % 4 != 0 or D < 1 */
+  M2SCAN_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  M2SCAN_ERR_ALIAS = 4,       /* an output range overlaps an input or another output */
+  M2SCAN_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than the query says */
+  M2SCAN_ERR_UNSUPPORTED = 6, /* shape outside every kernel instance (K*D too large) */
+  M2SCAN_ERR_CUDA = 7,        /* a CUDA runtime call failed; see m2scan_last_cuda_error */
+  M2SCAN_ERR_DEVICE = 8       /* no usable sm_100-family device is current */
+} m2scan_status;
+
+/*
+ * Forward pass: writes h_enriched [B,SH2].
+ *   h_history [B,K,SH2], h_s2 [B,SH2]: inputs.
+ *   W_A, W_B, W_C [SH2,D], W_O [D,SH2]: weights; tw: scalar blend weight.
+ * One fused kernel launch (none when B == 0).
+ */
+m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float* W_A,
+                         const float* W_B, const float* W_C, const float* W_O, float tw,
+                         int64_t B, int32_t K, int32_t SH2, int32_t D, float* h_enriched,
+                         m2scan_stream_t stream);
+
+/*
+ * Bytes of device workspace m2scan_bwd needs for these shapes: the per-slot
+ * partial sums of the four weight gradients (min(B,152) slots of 4*SH2*D
+ * floats). Depends on the shapes only. Returns 0 for invalid shapes.
+ */
+size_t m2scan_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D);
+
+/*
+ * Backward pass. Inputs as for m2scan_fwd plus d_h_enriched [B,SH2] (the
+ * upstream gradient dL/dh_enriched). Writes d_h_history [B,K,SH2],
+ * d_h_s2 [B,SH2], dW_A, dW_B, dW_C [SH2,D] and dW_O [D,SH2].
+ * `workspace` is caller-owned device scratch of at least
+ * m2scan_bwd_workspace_bytes(B,K,SH2,D) bytes (16-byte aligned); its contents
+ * on entry do not matter and are garbage on exit. It must not overlap any
+ * input or output. The projections and the scan are recomputed from the
+ * inputs (nothing is saved by the forward). Two kernel launches: the fused
+ * backward and the fixed-order reduction of the weight-gradient slots. When
+ * B == 0 the weight gradients are zero-filled with cudaMemsetAsync.
+ */
+m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float* W_A,
+                         const float* W_B, const float* W_C, const float* W_O, float tw,
+                         const float* d_h_enriched, int64_t B, int32_t K, int32_t SH2,
+                         int32_t D, float* d_h_history, float* d_h_s2, float* dW_A,
+                         float* dW_B, float* dW_C, float* dW_O, void* workspace,
+                         size_t workspace_bytes, m2scan_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* m2scan_status_str(m2scan_status status);
+
+/* cudaError_t value of the last failing CUDA call made by the library on the
+ * calling thread (0 if none). */
+int m2scan_last_cuda_error(void);
+
+/* Kernel path selection for tests: 0 = automatic (default), 1 = always use the
+ * generic fallback kernels. Process-wide; returns the previous value. */
+int m2scan_set_force_generic(int force);
+
+/* Which kernel family m2scan_fwd/m2scan_bwd would launch for these shapes:
+ * 1 = fused fast path, 2 = generic fallback, 0 = unsupported shape. */
+int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
+
+/*
+ * Device-side error flags of the current device (bit 0: a kernel gave up
+ * waiting on a shared-memory barrier after its iteration limit). Reading is
+ * SYNCHRONOUS (it waits for the device) and clears the flags. Returns
+ * M2SCAN_OK and stores the flags in *flags.
+ */
+m2scan_status m2scan_read_device_flags(uint32_t* flags);
+
+/* Number of CUDA kernels launched by the most recent successful m2scan_fwd
+ * or m2scan_bwd call on the calling thread. */
+int m2scan_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M2SCAN_H */

@@ -1,0 +1,72 @@
+"""Host-only checks of the C ABI, run in a child process with no visible GPU.
+
+Every call below must be rejected by the host-side argument checks before the
+library touches CUDA. The child hides all GPUs (CUDA_VISIBLE_DEVICES=""), so
+even a check that wrongly passed could not launch a kernel on the fake
+addresses used here. Prints one JSON object with the observed results.
+"""
+import json
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import gated_ssm_temporal_gb300 as g  # noqa: E402
+
+A = 1 << 32  # fake, 16-byte aligned device addresses far apart
+W = [A + i * (1 << 24) for i in range(20)]
+B, K, SH2, D = 8, 8, 32, 4
+res = {}
+
+
+def fwd(**kw):
+    args = dict(h_history=W[0], h_s2=W[1], W_A=W[2], W_B=W[3], W_C=W[4], W_O=W[5], tw=0.5,
+                B=B, K=K, SH2=SH2, D=D, h_enriched=W[6], stream=0)
+    args.update(kw)
+    return g.m2scan_fwd(**args)
+
+
+def bwd(**kw):
+    ws = g.m2scan_bwd_workspace_bytes(B, K, SH2, D)
+    args = dict(h_history=W[0], h_s2=W[1], W_A=W[2], W_B=W[3], W_C=W[4], W_O=W[5], tw=0.5,
+                d_h_enriched=W[7], B=B, K=K, SH2=SH2, D=D, d_h_history=W[8], d_h_s2=W[9],
+                dW_A=W[10], dW_B=W[11], dW_C=W[12], dW_O=W[13], workspace=W[14],
+                workspace_bytes=ws, stream=0)
+    args.update(kw)
+    return g.m2scan_bwd(**args)
+
+
+res["fwd_null_WA"] = fwd(W_A=0)
+res["fwd_null_h"] = fwd(h_history=0)
+res["fwd_null_out"] = fwd(h_enriched=0)
+res["fwd_B_neg"] = fwd(B=-1)
+res["fwd_K0"] = fwd(K=0)
+res["fwd_SH2_not4"] = fwd(SH2=30)
+res["fwd_SH2_small"] = fwd(SH2=0)
+res["fwd_D0"] = fwd(D=0)
+res["fwd_misaligned_h"] = fwd(h_history=W[0] + 4)
+res["fwd_misaligned_out"] = fwd(h_enriched=W[6] + 8)
+res["fwd_alias_out_h"] = fwd(h_enriched=W[0] + 64)
+res["fwd_alias_out_WO"] = fwd(h_enriched=W[5])
+res["fwd_B0_ok"] = fwd(B=0, h_history=0, h_s2=0, h_enriched=0)
+res["fwd_launches_B0"] = g.m2scan_last_launch_count()
+res["bwd_null_ws"] = bwd(workspace=0)
+res["bwd_short_ws"] = bwd(workspace_bytes=g.m2scan_bwd_workspace_bytes(B, K, SH2, D) - 16)
+res["bwd_null_dWO"] = bwd(dW_O=0)
+res["bwd_null_g"] = bwd(d_h_enriched=0)
+res["bwd_shape"] = bwd(K=-3)
+res["bwd_misaligned_ws"] = bwd(workspace=W[14] + 4)
+res["bwd_alias_out_out"] = bwd(dW_B=W[10] + 16)
+res["bwd_alias_ws_in"] = bwd(workspace=W[0])
+res["bwd_alias_dh_g"] = bwd(d_h_history=W[7])
+res["ws_bytes_pages"] = g.m2scan_bwd_workspace_bytes(8192, 8, 256, 16)
+res["ws_bytes_small_B"] = g.m2scan_bwd_workspace_bytes(3, 8, 256, 16)
+res["ws_bytes_B0"] = g.m2scan_bwd_workspace_bytes(0, 8, 256, 16)
+res["ws_bytes_bad"] = g.m2scan_bwd_workspace_bytes(5, 0, 256, 16)
+res["path_pages"] = g.m2scan_path_for(8, 256, 16)
+res["path_long"] = g.m2scan_path_for(64, 256, 16)
+res["path_tiny"] = g.m2scan_path_for(8, 32, 4)
+res["path_wide"] = g.m2scan_path_for(16, 512, 64)
+res["path_K129"] = g.m2scan_path_for(129, 256, 16)
+res["path_huge"] = g.m2scan_path_for(100000, 256, 64)
+res["status_str_ok"] = g.m2scan_status_str(0)
+print(json.dumps(res))

@@ -1,0 +1,75 @@
+"""The C-ABI library loads, exports what include/m2scan.h declares, and rejects
+bad arguments on the host (no GPU needed)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import gated_ssm_temporal_gb300 as g
+from gated_ssm_temporal_gb300 import build as gbuild
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return g.load_library()
+
+
+def test_exports_every_header_function(lib):
+    names = g.header_functions()
+    assert "m2scan_fwd" in names and "m2scan_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), "libm2scan.so does not export %s" % n
+
+
+def test_library_built_for_sm103a(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", gbuild.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    for n in g.header_functions():
+        assert (" T %s" % n) in out
+
+
+@pytest.fixture(scope="module")
+def probe(lib):
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(HERE, "abi_host_probe.py")], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+NULL, SHAPE, ALIGN, ALIAS, WORKSPACE = 1, 2, 3, 4, 5
+
+
+@pytest.mark.parametrize("key,expect", [
+    ("fwd_null_WA", NULL), ("fwd_null_h", NULL), ("fwd_null_out", NULL), ("fwd_B_neg", SHAPE),
+    ("fwd_K0", SHAPE), ("fwd_SH2_not4", SHAPE), ("fwd_SH2_small", SHAPE), ("fwd_D0", SHAPE),
+    ("fwd_misaligned_h", ALIGN), ("fwd_misaligned_out", ALIGN), ("fwd_alias_out_h", ALIAS),
+    ("fwd_alias_out_WO", ALIAS), ("fwd_B0_ok", 0), ("fwd_launches_B0", 0),
+    ("bwd_null_ws", WORKSPACE), ("bwd_short_ws", WORKSPACE), ("bwd_null_dWO", NULL),
+    ("bwd_null_g", NULL), ("bwd_shape", SHAPE), ("bwd_misaligned_ws", ALIGN),
+    ("bwd_alias_out_out", ALIAS), ("bwd_alias_ws_in", ALIAS), ("bwd_alias_dh_g", ALIAS),
+])
+def test_host_validation(probe, key, expect):
+    assert probe[key] == expect, (key, probe[key])
+
+
+def test_workspace_query(probe):
+    assert probe["ws_bytes_pages"] == 152 * 4 * 256 * 16 * 4
+    assert probe["ws_bytes_small_B"] == 3 * 4 * 256 * 16 * 4
+    assert probe["ws_bytes_B0"] == 0
+    assert probe["ws_bytes_bad"] == 0
+
+
+def test_path_choice(probe):
+    assert probe["path_pages"] == 1
+    assert probe["path_long"] == 1
+    assert probe["path_tiny"] == 1
+    assert probe["path_wide"] == 2
+    assert probe["path_K129"] == 2
+    assert probe["path_huge"] == 0
+    assert probe["status_str_ok"] == "ok"

@@ -1,0 +1,187 @@
+"""CUDA path against the fp64 oracle, element by element (needs a GB300)."""
+import numpy as np
+import pytest
+
+from gated_ssm_temporal_gb300.workloads import WORKLOADS, Workload, make_inputs
+from golden_io import hand_k2
+from gpu_helpers import OUTPUTS, ensure_built, oracle_all, run_all, run_bwd, run_fwd, to_dev
+from tolerance import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("h_enriched",) + OUTPUTS
+
+
+def check(x, force_generic=False):
+    got = run_all(x, force_generic=force_generic)
+    ref = oracle_all(x)
+    return {n: assert_parity(n, got[n], ref[n]) for n in NAMES}
+
+
+def custom(B, K, SH2, D, seed, tw=0.3, wa_scale=1.0, odd=1.0):
+    return make_inputs(Workload("custom", B, K, SH2, D, tw, seed, wa_scale, odd))
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_tiny_workload(seed):
+    check(make_inputs(WORKLOADS["tiny"].with_batch(4, seed)))
+
+
+@pytest.mark.parametrize("name", ["pages", "long_history", "wide_state", "stress"])
+def test_full_size_workloads(name):
+    """Every output of the full workload, in the launch configuration the benchmark times."""
+    check(make_inputs(WORKLOADS[name]))
+
+
+@pytest.mark.parametrize("B", [1, 2, 5, 17, 151, 152, 153, 1000, 8191])
+def test_ragged_batches(B):
+    check(custom(B, 8, 256, 16, seed=100 + B, tw=0.1))
+
+
+@pytest.mark.parametrize("K,SH2,D", [
+    (1, 256, 16), (2, 64, 16), (3, 96, 8), (5, 160, 16), (7, 32, 4), (16, 128, 8),
+    (33, 64, 16), (100, 256, 16), (128, 64, 4), (8, 256, 8), (8, 512, 8)])
+def test_fast_path_shapes(K, SH2, D):
+    check(custom(37, K, SH2, D, seed=K * 1000 + SH2 + D, wa_scale=2.0))
+
+
+@pytest.mark.parametrize("K,SH2,D", [
+    (8, 36, 16), (129, 64, 4), (4, 4, 1), (6, 20, 3), (8, 256, 16), (16, 512, 64), (3, 64, 24)])
+def test_generic_path_shapes(K, SH2, D):
+    force = (K, SH2, D) == (8, 256, 16)
+    check(custom(23, K, SH2, D, seed=7 + K + SH2 + D, wa_scale=2.0), force_generic=force)
+
+
+def test_generic_path_matches_on_pages_dims():
+    check(custom(600, 8, 256, 16, seed=5, tw=0.1), force_generic=True)
+
+
+def test_saturated_gates():
+    """W_A x 200: sigmoid saturates to exactly 0 or 1 in fp32; no NaN may appear."""
+    check(custom(64, 8, 256, 16, seed=11, wa_scale=200.0))
+
+
+def test_heavy_tailed_history():
+    check(custom(300, 8, 256, 16, seed=12, odd=30.0))
+
+
+def _padded_golden(SH2, D):
+    """The hand-derived example embedded in SH2 features and D states with zero padding."""
+    x = hand_k2()
+    f = np.float32
+    out = {"tw": x["tw"]}
+    h = np.zeros((1, 2, SH2), f); h[:, :, :2] = x["h_history"]
+    hs = np.zeros((1, SH2), f); hs[:, :2] = x["h_s2"]
+    g = np.zeros((1, SH2), f); g[:, :2] = x["d_h_enriched"]
+    out.update(h_history=h, h_s2=hs, d_h_enriched=g)
+    for k in ("W_A", "W_B", "W_C"):
+        w = np.zeros((SH2, D), f); w[:2, :1] = x[k]; out[k] = w
+    wo = np.zeros((D, SH2), f); wo[:1, :2] = x["W_O"]; out["W_O"] = wo
+    exp = {}
+    y = hs.copy(); y[:, :2] = x["h_enriched"]; exp["h_enriched"] = y
+    dh = np.zeros((1, 2, SH2)); dh[:, :, :2] = x["d_h_history"]; exp["d_h_history"] = dh
+    dhs = g.astype(np.float64).copy(); dhs[:, :2] = x["d_h_s2"]; exp["d_h_s2"] = dhs
+    for k in ("dW_A", "dW_B", "dW_C"):
+        w = np.zeros((SH2, D)); w[:2, :1] = x[k]; exp[k] = w
+    wo = np.zeros((D, SH2)); wo[:1, :2] = x["dW_O"]; exp["dW_O"] = wo
+    return out, exp
+
+
+@pytest.mark.parametrize("SH2,D,force", [(32, 4, False), (4, 1, False), (32, 4, True)])
+def test_golden_hand_example(SH2, D, force):
+    x, exp = _padded_golden(SH2, D)
+    got = run_all(x, force_generic=force)
+    for n in NAMES:
+        np.testing.assert_allclose(got[n], exp[n], rtol=0, atol=1e-6, err_msg=n)
+
+
+def test_bwd_bitwise_reproducible_and_stream_independent():
+    import torch
+    ensure_built()
+    x = make_inputs(WORKLOADS["pages"])
+    d = to_dev(x)
+    r1 = {k: v.clone() for k, v in run_bwd(d).items()}
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        r2 = run_bwd(d, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    r3 = run_bwd(d)
+    torch.cuda.synchronize()
+    for k in OUTPUTS:
+        assert torch.equal(r1[k], r2[k]), k
+        assert torch.equal(r1[k], r3[k]), k
+    y1 = run_fwd(d).clone()
+    y2 = run_fwd(d)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_guard_bands_untouched():
+    """Outputs sit inside larger buffers filled with a sentinel; nothing outside is written."""
+    import torch
+    import gated_ssm_temporal_gb300 as g
+    ensure_built()
+    x = custom(153, 8, 256, 16, seed=3, tw=0.1)
+    d = to_dev(x)
+    B, K, SH2, D = 153, 8, 256, 16
+    pad = 64
+    sentinel = 12345.5
+
+    def guarded(shape):
+        n = int(np.prod(shape))
+        buf = torch.full((n + 2 * pad,), sentinel, device="cuda", dtype=torch.float32)
+        return buf, buf[pad:pad + n].view(*shape)
+
+    bufs = {}
+    outs = {}
+    shapes = {"d_h_history": (B, K, SH2), "d_h_s2": (B, SH2), "dW_A": (SH2, D), "dW_B": (SH2, D),
+              "dW_C": (SH2, D), "dW_O": (D, SH2)}
+    for k, sh in shapes.items():
+        bufs[k], outs[k] = guarded(sh)
+    ybuf, y = guarded((B, SH2))
+    wsn = g.m2scan_bwd_workspace_bytes(B, K, SH2, D) // 4
+    wsbuf, ws = guarded((wsn,))
+    g.fwd(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"], out=y)
+    run_bwd(d, outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    for buf in list(bufs.values()) + [ybuf, wsbuf]:
+        assert torch.all(buf[:pad] == sentinel) and torch.all(buf[-pad:] == sentinel)
+    ref = oracle_all(x)
+    assert_parity("h_enriched", y.cpu().numpy(), ref["h_enriched"])
+    for k in OUTPUTS:
+        assert_parity(k, outs[k].cpu().numpy(), ref[k])
+
+
+def test_empty_batch():
+    import torch
+    import gated_ssm_temporal_gb300 as g
+    ensure_built()
+    x = custom(0, 8, 256, 16, seed=1)
+    d = to_dev(x)
+    y = run_fwd(d)
+    assert y.shape == (0, 256)
+    outs = g.alloc_bwd_outputs(0, 8, 256, 16, "cuda")
+    for k in ("dW_A", "dW_B", "dW_C", "dW_O"):
+        outs[k].fill_(7.0)
+    run_bwd(d, outs=outs)
+    torch.cuda.synchronize()
+    for k in ("dW_A", "dW_B", "dW_C", "dW_O"):
+        assert torch.all(outs[k] == 0)
+
+
+def test_launch_counts():
+    import gated_ssm_temporal_gb300 as g
+    ensure_built()
+    d = to_dev(custom(64, 8, 256, 16, seed=2))
+    run_fwd(d)
+    assert g.m2scan_last_launch_count() == 1
+    run_bwd(d)
+    assert g.m2scan_last_launch_count() == 2
+
+
+def test_no_device_wait_timeouts():
+    import gated_ssm_temporal_gb300 as g
+    ensure_built()
+    run_all(custom(64, 8, 256, 16, seed=4))
+    assert g.m2scan_read_device_flags() == 0
