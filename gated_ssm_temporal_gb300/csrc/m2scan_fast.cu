@@ -312,11 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
         }
         sCtx[s * D + d] = sC[s * D + d] * x;
       } else {
-        for (int t = 0; t < K; ++t) {
+        for (int t = 0; t < K; ++t) {  // replay: A stays in place, B_t is replaced by x_t
           float* pr = pcol + t * PS;
-          const float sg = sigmoidf_(pr[d]);
-          x = fmaf(sg, x, pr[D + d]);
-          pr[d] = sg;
+          x = fmaf(sigmoidf_(pr[d]), x, pr[D + d]);
           pr[D + d] = x;
         }
         const float Cv = sC[s * D + d], dctx = sDctx[s * D + d];
@@ -325,10 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
         float dx = dctx * Cv;  // gradient with respect to x_{K-1}
         for (int t = K - 1; t >= 0; --t) {
           float* pr = pcol + t * PS;
-          const float sg = pr[d];
+          const float at = pr[d];
+          const float sg = sigmoidf_(at);
+          // sigmoid'(a) = sigmoid(a) * sigmoid(-a): 1 - sigmoid(a) taken as sigmoid(-a)
+          // keeps full relative precision when the gate is saturated near 1.
+          const float dsg = sg * sigmoidf_(-at);
           const float xprev = t > 0 ? pr[D + d - PS] : 0.f;
-          pr[D + d] = dx;                              // dB_t
-          pr[d] = dx * xprev * (sg * (1.f - sg));      // dA_t
+          pr[D + d] = dx;                   // dB_t
+          pr[d] = dx * xprev * dsg;         // dA_t
           dx *= sg;
         }
       }

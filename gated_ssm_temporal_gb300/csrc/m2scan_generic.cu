@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
   extern __shared__ float4 smem_f4[];
   float* sm = reinterpret_cast<float*>(smem_f4);
   const int K = a.K, SH2 = a.SH2, D = a.D, TD = 2 * D;
-  float* sAB = sm;            // [K][2D]: A|B, then sigmoid|x, then dA|dB
+  float* sAB = sm;            // [K][2D]: A|B, then A|x, then dA|dB
   float* sHs = sAB + K * TD;  // [SH2]
   float* sG = sHs + SH2;      // [SH2]
   float* sC = sG + SH2;       // [D]
@@ -65,12 +65,8 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
       float x = 0.f;
       for (int t = 0; t < K; ++t) {
         float* pr = sAB + t * TD;
-        const float sg = sigmoidf_(pr[d]);
-        x = fmaf(sg, x, pr[D + d]);
-        if (BWD) {
-          pr[d] = sg;
-          pr[D + d] = x;
-        }
+        x = fmaf(sigmoidf_(pr[d]), x, pr[D + d]);
+        if (BWD) pr[D + d] = x;  // A stays in place, B_t is replaced by x_t
       }
       sCtx[d] = sC[d] * x;
       if (BWD) {
@@ -78,10 +74,12 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
         float dx = sDctx[d] * sC[d];
         for (int t = K - 1; t >= 0; --t) {
           float* pr = sAB + t * TD;
-          const float sg = pr[d];
+          const float at = pr[d];
+          const float sg = sigmoidf_(at);
+          const float dsg = sg * sigmoidf_(-at);  // sigmoid' without cancellation near 1
           const float xprev = t > 0 ? pr[D + d - TD] : 0.f;
           pr[D + d] = dx;
-          pr[d] = dx * xprev * (sg * (1.f - sg));
+          pr[d] = dx * xprev * dsg;
           dx *= sg;
         }
       }
