@@ -60,6 +60,9 @@ def load_library(path: str | None = None):
         lib.m2scan_bwd.argtypes = ([vp] * 6 + [f32, vp, i64, i32, i32, i32] + [vp] * 6
                                    + [vp, sz, vp])
         lib.m2scan_bwd.restype = ctypes.c_int
+        lib.m2scan_bwd_noalloc.argtypes = ([vp] * 6 + [f32, vp, i64, i32, i32, i32] + [vp] * 6
+                                           + [vp])
+        lib.m2scan_bwd_noalloc.restype = ctypes.c_int
         lib.m2scan_bwd_workspace_bytes.argtypes = [i64, i32, i32, i32]
         lib.m2scan_bwd_workspace_bytes.restype = sz
         lib.m2scan_status_str.argtypes = [ctypes.c_int]
@@ -91,6 +94,17 @@ def m2scan_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2,
     return load_library().m2scan_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, float(tw),
                                      d_h_enriched, B, K, SH2, D, d_h_history, d_h_s2, dW_A,
                                      dW_B, dW_C, dW_O, workspace, workspace_bytes, stream)
+
+
+def m2scan_bwd_noalloc(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2, D,
+                       d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O, stream=0):
+    """m2scan_bwd for callers that cannot allocate: scratch is the library's static array."""
+    return load_library().m2scan_bwd_noalloc(h_history, h_s2, W_A, W_B, W_C, W_O, float(tw),
+                                             d_h_enriched, B, K, SH2, D, d_h_history, d_h_s2,
+                                             dW_A, dW_B, dW_C, dW_O, stream)
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 def m2scan_bwd_workspace_bytes(B, K, SH2, D):

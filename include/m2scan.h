@@ -109,6 +109,37 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
                          float* dW_B, float* dW_C, float* dW_O, void* workspace,
                          size_t workspace_bytes, m2scan_stream_t stream);
 
+/*
+ * Backward pass for callers that cannot allocate device memory themselves:
+ * code running where the device allocator belongs to someone else (a host
+ * framework whose memory pool must account for every byte), latency-critical
+ * paths that cannot afford cudaMalloc's implicit device synchronisation, and
+ * minimal C hosts that only own the tensors they pass in. The pages have no
+ * counterpart of this call; it is a packaging variant of m2scan_bwd.
+ *
+ * Same arguments and results as m2scan_bwd, without `workspace`: the
+ * weight-gradient slots live in a static array of
+ * M2SCAN_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library
+ * holds until the process exits. The call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine); the caller still passes every
+ * input and output. Shapes whose slots need more than
+ * M2SCAN_NOALLOC_SCRATCH_BYTES (m2scan_bwd_workspace_bytes > the maximum)
+ * return M2SCAN_ERR_WORKSPACE without launching anything.
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, a synchronous runtime call); make that first
+ * call before any stream capture. Every call on a device shares the one
+ * array and nothing in it needs to start at zero, but calls that overlap on
+ * the GPU (different streams, or different host threads, without ordering
+ * between them) race on it and produce wrong weight gradients.
+ */
+#define M2SCAN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+m2scan_status m2scan_bwd_noalloc(const float* h_history, const float* h_s2, const float* W_A,
+                                 const float* W_B, const float* W_C, const float* W_O,
+                                 float tw, const float* d_h_enriched, int64_t B, int32_t K,
+                                 int32_t SH2, int32_t D, float* d_h_history, float* d_h_s2,
+                                 float* dW_A, float* dW_B, float* dW_C, float* dW_O,
+                                 m2scan_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* m2scan_status_str(m2scan_status status);
 
