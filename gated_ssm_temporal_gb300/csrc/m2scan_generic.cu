@@ -138,12 +138,20 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const float* __restric
   const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
   const long long total = 4ll * n;
   const long long e0 = static_cast<long long>(blockIdx.x) * 128 + 4 * lane;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (e0 < total) {
-    for (int p = grp; p < P; p += 8) {
-      const float4 v = *reinterpret_cast<const float4*>(ws + static_cast<size_t>(p) * total + e0);
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-    }
+  // all loads of a thread are issued before the first add (P <= 152 = 8 x 19)
+  constexpr int kPerGroup = (kMaxSlots + 7) / 8;
+  float4 v[kPerGroup];
+#pragma unroll
+  for (int i = 0; i < kPerGroup; ++i) {
+    const int p = grp + 8 * i;
+    v[i] = (p < P && e0 < total)
+               ? *reinterpret_cast<const float4*>(ws + static_cast<size_t>(p) * total + e0)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float4 s = v[0];
+#pragma unroll
+  for (int i = 1; i < kPerGroup; ++i) {
+    s.x += v[i].x; s.y += v[i].y; s.z += v[i].z; s.w += v[i].w;
   }
   red[grp][lane] = s;
   __syncthreads();
