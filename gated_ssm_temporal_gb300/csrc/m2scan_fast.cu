@@ -67,7 +67,7 @@ __device__ __forceinline__ float dot4(const float4& a, const float4& b, float ac
   return fmaf(a.w, b.w, acc);
 }
 
-template <int D, bool BWD>
+template <int D, bool BWD, bool TC>
 __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant__ FastArgs a) {
   constexpr int NQ = D / 4;    // A (and B) columns per lane in the projection loop
   constexpr int TD = 2 * D;    // columns of A|B
@@ -86,6 +86,16 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   float* sDctx = reinterpret_cast<float*>(base + a.off_dctx); // d_ctx [S_max][D]
   float* sDC = reinterpret_cast<float*>(base + a.off_dc);     // dC [S_max][D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + a.off_bar);
+  // tensor-core path
+  float* sHlo = reinterpret_cast<float*>(base + a.off_hlo);   // 2 x [128][32], swizzled
+  float* sWt = reinterpret_cast<float*>(base + a.off_wt);     // NC tiles [2D][32], swizzled
+  float* sWtlo = reinterpret_cast<float*>(base + a.off_wtlo);
+  uint64_t* mbars = reinterpret_cast<uint64_t*>(base + a.off_mbar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(base + a.off_tslot);
+  const int NST = a.n_stages;
+  // loads are issued this many items ahead; the tensor-core path keeps one stage
+  // back for the MMAs still reading it
+  const int PF = TC ? NST - 1 : NST;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, SH2 = a.SH2, S_max = a.S_max, SG = a.SG;
@@ -104,14 +114,14 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   };
 
   // ---- copy producer (thread 0): issues the loads of the next item into the
-  // ring, kStages items ahead of the consumers.
+  // ring, PF items ahead of the consumers.
   int pf_tile = 0, pf_idx = 0, pf_seq = 0;
   auto issue_next = [&]() {
     if (pf_tile >= T) return;
     const long long tb0 = tile_start(pf_tile);
     const int S_t = static_cast<int>(tile_start(pf_tile + 1) - tb0);
     const int NSI = (S_t + SG - 1) / SG;
-    const int stage = pf_seq % kStages;
+    const int stage = pf_seq % NST;
     unsigned char* st = base + static_cast<size_t>(stage) * a.stage_bytes;
     uint64_t* bar = &bars[stage];
     const int idx = pf_idx;
@@ -143,21 +153,39 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   };
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    if (TC)
+      for (int s = 0; s < 2; ++s) mbar_init(&mbars[s], 1);
     fence_barrier_init();
   }
+  if (TC && warp == 0) tmem_alloc(tslot, a.tmem_cols);
+  if (TC) tc_fence_before();
   __syncthreads();
+  if (TC) tc_fence_after();
+  const uint32_t tmem_acc = TC ? *tslot : 0u;
   if (tid == 0)
-    for (int s = 0; s < kStages; ++s) issue_next();
+    for (int s = 0; s < PF; ++s) issue_next();
 
   // weights into shared memory (overlaps the first loads)
   for (int i = tid; i < SH2 * D; i += kThreads) {
     const int j = i / D, d = i - j * D;
-    sW_AB[wab_idx<D>(j, d)] = a.W_A[i];
-    sW_AB[wab_idx<D>(j, D + d)] = a.W_B[i];
+    const float wa = a.W_A[i], wb = a.W_B[i];
+    if (!TC || BWD) {
+      sW_AB[wab_idx<D>(j, d)] = wa;
+      sW_AB[wab_idx<D>(j, D + d)] = wb;
+    }
+    if (TC) {  // B operand of the projection MMA: tile q = [2D rows][32 columns of SH2]
+      const int tq = (j >> 5) * TD * 32, jj = j & 31;
+      const float ha = tf32_rn(wa), hb = tf32_rn(wb);
+      sWt[tq + sw128_idx(d, jj)] = ha;
+      sWtlo[tq + sw128_idx(d, jj)] = wa - ha;
+      sWt[tq + sw128_idx(D + d, jj)] = hb;
+      sWtlo[tq + sw128_idx(D + d, jj)] = wb - hb;
+    }
     sW_Ct[d * SH2 + j] = a.W_C[i];
   }
   for (int i = tid; i < D * SH2; i += kThreads) sW_O[i] = a.W_O[i];
+  if (TC) fence_proxy_async_smem();
   __syncthreads();
 
   // ---- per-thread ownership of weight-gradient entries (backward)
@@ -184,6 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   const int sd_s = (tid >> 2) / NQ;
 
   int seq = 0;
+  int mma_id = 0;       // chunks whose MMAs have been issued (all threads count)
+  int prev_chunk = -1;  // thread 0: MMA id of the previous item if it was a chunk
+  // thread 0, end of an item: the stage of the previous item is refilled; on the
+  // tensor-core path its MMAs must have finished reading it first
+  auto refill = [&](int this_chunk) {
+    if (TC && prev_chunk >= 0) bounded_wait(&mbars[prev_chunk & 1], (prev_chunk >> 1) & 1, a.err);
+    prev_chunk = this_chunk;
+    issue_next();
+  };
   for (int tile = 0; tile < T; ++tile) {
     const long long tb0 = tile_start(tile);
     const int S_t = static_cast<int>(tile_start(tile + 1) - tb0);
@@ -201,12 +238,26 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     float cacc[4] = {0.f, 0.f, 0.f, 0.f}, dacc[4] = {0.f, 0.f, 0.f, 0.f};
 
     for (int q = 0; q < NC; ++q, ++seq) {
-      const int stage = seq % kStages;
-      bounded_wait(&bars[stage], (seq / kStages) & 1, a.err);
+      const int stage = seq % NST;
+      bounded_wait(&bars[stage], (seq / NST) & 1, a.err);
       const float* Hc = reinterpret_cast<const float*>(base + static_cast<size_t>(stage) * a.stage_bytes);
       const float* Sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_S);
       const float* Gc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_G);
-      if (gemm_active) {
+      float* hlo = sHlo + (mma_id & 1) * (kTileRows * 32);
+      if constexpr (TC) {
+        // the MMAs of chunk mma_id-2 read this h_lo buffer: wait for them
+        if (mma_id >= 2) bounded_wait(&mbars[mma_id & 1], ((mma_id - 2) >> 1) & 1, a.err);
+        // h = hi + lo: hi = tf32_rn(h) overwrites the h box in place, lo goes to hlo.
+        // Only the box's own rows are touched (the h_s2 box may follow it); rows of
+        // the 128-row MMA tile past the box are don't-care rows of the result.
+        float* Hw = const_cast<float*>(Hc);
+        for (int i = 4 * tid; i < a.hc_bytes / 4; i += 4 * kThreads) {
+          const float4 v = lds4(Hc + i);
+          const float4 h = make_float4(tf32_rn(v.x), tf32_rn(v.y), tf32_rn(v.z), tf32_rn(v.w));
+          sts4(Hw + i, h);
+          sts4(hlo + i, make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w));
+        }
+      } else if (gemm_active) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int jj = 16 * jh + 4 * u;  // first column (within the chunk) of this step
@@ -254,12 +305,60 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
           }
         }
       }
+      if (TC) fence_proxy_async_smem();
       __syncthreads();
-      if (tid == 0) issue_next();
+      if (tid == 0) {
+        if constexpr (TC) {
+          // A|B = sum over chunks of h_hi.W_hi, plus the corrections
+          // h_hi.W_lo + h_lo.W_hi (3 x tf32, hi = tf32_rn, lo = remainder). Each chunk's main
+          // product has its own TMEM accumulator (columns q*2D) and the corrections
+          // share one (columns NC*2D): few accumulation steps per accumulator keep
+          // the tensor cores' accumulation error at the level of fp32 FMA.
+          tc_fence_after();
+          constexpr uint32_t idesc = umma_idesc_tf32(128, TD);
+          const uint32_t ah = smem_addr(Hc), al = smem_addr(hlo);
+          const uint32_t bh = smem_addr(sWt + q * TD * 32), bl = smem_addr(sWtlo + q * TD * 32);
+          const uint32_t d_main = tmem_acc + q * TD, d_corr = tmem_acc + NC * TD;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t o = 32u * ks;
+            umma_tf32(d_main, umma_desc_sw128(ah + o), umma_desc_sw128(bh + o), idesc, ks != 0);
+            umma_tf32(d_corr, umma_desc_sw128(ah + o), umma_desc_sw128(bl + o), idesc,
+                      (q | ks) != 0);
+            umma_tf32(d_corr, umma_desc_sw128(al + o), umma_desc_sw128(bh + o), idesc, 1u);
+          }
+          umma_commit(&mbars[mma_id & 1]);
+          refill(mma_id);
+        } else {
+          issue_next();
+        }
+      }
+      if (TC) ++mma_id;
     }
 
-    // ---- combine the two column halves into the A|B tile; finish C, d_ctx
-    if (gemm_active && jh == 1) {
+    // ---- A|B tile into shared memory; finish C, d_ctx
+    if constexpr (TC) {
+      const int last = mma_id - 1;
+      bounded_wait(&mbars[last & 1], (last >> 1) & 1, a.err);
+      tc_fence_after();
+      float v[D], w[D];
+      const int c0 = (warp >> 2) * D;  // warps 0-3: A columns, warps 4-7: B columns
+      const uint32_t lane_base = tmem_acc + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + c0;
+      tmem_ld<D>(lane_base, v);
+      for (int qq = 1; qq < NC; ++qq) {  // fixed order: chunk 0, 1, ..., then the corrections
+        tmem_ld<D>(lane_base + qq * TD, w);
+#pragma unroll
+        for (int i = 0; i < D; ++i) v[i] += w[i];
+      }
+      tmem_ld<D>(lane_base + NC * TD, w);
+#pragma unroll
+      for (int i = 0; i < D; ++i) v[i] += w[i];
+      float* pr = sP + (32 * (warp & 3) + lane) * PS + c0;
+#pragma unroll
+      for (int i = 0; i < D; i += 4) sts4(pr + i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+      tc_fence_before();
+    }
+    if (!TC && gemm_active && jh == 1) {
 #pragma unroll
       for (int rg = 0; rg < 4; ++rg) {
         float* pr = sP + (wrow0 + r_lane + 8 * rg) * PS;
@@ -287,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
       }
     }
     __syncthreads();
-    if (gemm_active && jh == 0) {
+    if (!TC && gemm_active && jh == 0) {
 #pragma unroll
       for (int rg = 0; rg < 4; ++rg) {
         float* pr = sP + (wrow0 + r_lane + 8 * rg) * PS;
@@ -340,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     // ================= pass 2a: per-sample outputs =======================
     const int njq = SH2 / 4;
     for (int k = 0; k < NSI; ++k, ++seq) {
-      const int stage = seq % kStages;
-      bounded_wait(&bars[stage], (seq / kStages) & 1, a.err);
+      const int stage = seq % NST;
+      bounded_wait(&bars[stage], (seq / NST) & 1, a.err);
       float* hsb = reinterpret_cast<float*>(base + static_cast<size_t>(stage) * a.stage_bytes);
       const int s0 = k * SG, ns = min(SG, S_t - s0);
       const int nit = ((ns + 3) / 4) * njq;
@@ -435,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
         bulk_store(dst, hsb, static_cast<uint32_t>(ns) * SH2 * 4u);
         bulk_commit();
         bulk_wait_read_all();
-        issue_next();
+        if (TC) refill(-1); else issue_next();
       }
     }
 
@@ -443,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     if constexpr (BWD) {
       const int NRI = (R_t + kRowsPerItem - 1) / kRowsPerItem;
       for (int k = 0; k < NRI; ++k, ++seq) {
-        const int stage = seq % kStages;
-        bounded_wait(&bars[stage], (seq / kStages) & 1, a.err);
+        const int stage = seq % NST;
+        bounded_wait(&bars[stage], (seq / NST) & 1, a.err);
         float* hb = reinterpret_cast<float*>(base + static_cast<size_t>(stage) * a.stage_bytes);
         const int r0 = k * kRowsPerItem, nr = min(kRowsPerItem, R_t - r0);
         // dW_A | dW_B partial sums: sum over rows of h[row, j] * dAB[row, col]
@@ -501,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
           bulk_store(a.out0 + (tb0 * K + r0) * SH2, hb, static_cast<uint32_t>(nr) * SH2 * 4u);
           bulk_commit();
           bulk_wait_read_all();
-          issue_next();
+          if (TC) refill(-1); else issue_next();
         }
       }
     }
@@ -534,6 +633,11 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     }
   }
   if (tid == 0) bulk_wait_all();
+  if constexpr (TC) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem_acc, a.tmem_cols);
+  }
 }
 
 }  // namespace
@@ -543,10 +647,14 @@ bool fast_path_ok(int K, int SH2, int D) {
          SH2 * D <= 4096 && K >= 1 && K <= kTileRows;
 }
 
+// The tensor-core variant: forward, D in {8, 16} (MMA N = 2D must be a multiple of 16).
+bool tc_path_ok(bool bwd, int D) { return !bwd && (D == 8 || D == 16); }
+
 static int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a) {
   if (!fast_path_ok(K, SH2, D)) return false;
+  const bool tc = tc_path_ok(bwd, D);
   int S_max = kTileRows / K;
   if (S_max > 32) S_max = 32;
   if (S_max > kThreads / D) S_max = kThreads / D;
@@ -559,10 +667,18 @@ bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a) {
   const int sample_bytes = (bwd ? 2 : 1) * SG * SH2 * 4;
   if (sample_bytes > stage) stage = sample_bytes;
   if (bwd && kRowsPerItem * SH2 * 4 > stage) stage = kRowsPerItem * SH2 * 4;
-  if (kTileRows * 128 > stage) stage = kTileRows * 128;  // partially used warps read up to row 127
+  if (kTileRows * 128 > stage) stage = kTileRows * 128;  // a 128-row tile is always read
   stage = round_up(stage, 1024);
-  int off = kStages * stage;
-  a->off_wab = off; off += SH2 * 2 * D * 4;
+  const int n_stages = tc ? 3 : kStages;
+  int off = n_stages * stage;
+  a->off_hlo = a->off_wt = a->off_wtlo = off;
+  if (tc) {
+    a->off_hlo = off;  off += 2 * kTileRows * 128;
+    a->off_wt = off;   off += SH2 * 2 * D * 4;
+    a->off_wtlo = off; off += SH2 * 2 * D * 4;
+  }
+  a->off_wab = off;
+  if (!tc || bwd) off += SH2 * 2 * D * 4;
   a->off_wct = off; off += D * SH2 * 4;
   a->off_wo = off;  off += D * SH2 * 4;
   a->off_p = off;   off += kTileRows * (2 * D + 4) * 4;
@@ -571,7 +687,9 @@ bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a) {
   a->off_dctx = off; off += S_max * D * 4;
   a->off_dc = off;  off += S_max * D * 4;
   off = round_up(off, 16);
-  a->off_bar = off; off += kStages * 8;
+  a->off_bar = off;  off += kMaxStages * 8;
+  a->off_mbar = off; off += 2 * 8;
+  a->off_tslot = off; off += 16;
   a->smem_bytes = off + 1024;  // slack to align the start to 1024 bytes
   a->S_max = S_max;
   a->SG = SG;
@@ -582,33 +700,46 @@ bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a) {
   a->off_G = off_G;
   a->K = K;
   a->SH2 = SH2;
+  a->n_stages = n_stages;
+  a->tc = tc ? 1 : 0;
+  // TMEM: one accumulator block per SH2 chunk plus one for the correction terms
+  int cols = 32;
+  while (cols < (SH2 / kChunk + 1) * 2 * D) cols *= 2;
+  a->tmem_cols = cols;
   return a->smem_bytes <= 227 * 1024;
 }
 
-template <int D, bool BWD>
+template <int D, bool BWD, bool TC>
 static cudaError_t launch_one(const FastArgs& a, int grid, cudaStream_t stream) {
   static_assert(D % 4 == 0, "D must be a multiple of 4");
-  fast_kernel<D, BWD><<<grid, kThreads, a.smem_bytes, stream>>>(a);
+  fast_kernel<D, BWD, TC><<<grid, kThreads, a.smem_bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream) {
+  if (a.tc) {
+    switch (D) {
+      case 8: return launch_one<8, false, true>(a, grid, stream);
+      case 16: return launch_one<16, false, true>(a, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (D) {
-    case 4: return bwd ? launch_one<4, true>(a, grid, stream) : launch_one<4, false>(a, grid, stream);
-    case 8: return bwd ? launch_one<8, true>(a, grid, stream) : launch_one<8, false>(a, grid, stream);
-    case 16: return bwd ? launch_one<16, true>(a, grid, stream) : launch_one<16, false>(a, grid, stream);
+    case 4: return bwd ? launch_one<4, true, false>(a, grid, stream) : launch_one<4, false, false>(a, grid, stream);
+    case 8: return bwd ? launch_one<8, true, false>(a, grid, stream) : launch_one<8, false, false>(a, grid, stream);
+    case 16: return bwd ? launch_one<16, true, false>(a, grid, stream) : launch_one<16, false, false>(a, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t prepare_fast_kernels(int max_smem) {
   cudaError_t e = cudaSuccess;
-#define M2_SET(DD, BB)                                                                      \
-  if (e == cudaSuccess)                                                                     \
-    e = cudaFuncSetAttribute(fast_kernel<DD, BB>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define M2_SET(DD, BB, TT)                                                                       \
+  if (e == cudaSuccess)                                                                          \
+    e = cudaFuncSetAttribute(fast_kernel<DD, BB, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              max_smem);
-  M2_SET(4, false) M2_SET(4, true) M2_SET(8, false) M2_SET(8, true) M2_SET(16, false)
-  M2_SET(16, true)
+  M2_SET(4, false, false) M2_SET(4, true, false) M2_SET(8, false, false) M2_SET(8, true, false)
+  M2_SET(16, false, false) M2_SET(16, true, false) M2_SET(8, false, true) M2_SET(16, false, true)
 #undef M2_SET
   return e;
 }

@@ -10,7 +10,8 @@
 namespace m2scan {
 
 constexpr int kThreads = 256;     // threads per CTA, every kernel
-constexpr int kStages = 3;        // depth of the copy ring of the fast kernels
+constexpr int kStages = 3;        // depth of the copy ring of the FP32-FMA fast kernels
+constexpr int kMaxStages = 4;     // ring depth, at most (any fast kernel)
 constexpr int kMaxSlots = 152;    // CTAs (= weight-gradient slots) per call, at most
 constexpr int kTileRows = 128;    // rows (samples x K) per pass-1 tile, at most
 constexpr int kChunk = 32;        // SH2 columns per pass-1 chunk (128 bytes)
@@ -47,6 +48,14 @@ struct alignas(128) FastArgs {
   int off_S;     // offset of the h_s2 box inside a chunk stage
   int off_G;     // offset of the d_h_enriched box inside a chunk stage
   int off_wab, off_wct, off_wo, off_p, off_cs, off_ctx, off_dctx, off_dc, off_bar;
+  int off_hlo;    // tensor-core path: two [128 x 32] buffers of h - tf32(h)
+  int off_wt;     // tensor-core path: W_A|W_B transposed, K-major tiles (tf32 part)
+  int off_wtlo;   // tensor-core path: the remainder W - tf32(W), same layout
+  int off_mbar;   // tensor-core path: two MMA-completion barriers
+  int off_tslot;  // tensor-core path: TMEM base address written by tcgen05.alloc
+  int n_stages;   // depth of the copy ring
+  int tc;         // 1 when the projections run on the tensor cores
+  int tmem_cols;  // TMEM columns allocated by each CTA (power of two)
   int smem_bytes;
   float tw;
 };
@@ -73,6 +82,8 @@ struct GenericArgs {
 bool fast_path_ok(int K, int SH2, int D);
 // Fills the shared-memory plan of a fast kernel. Returns false if it does not fit.
 bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a);
+// Whether the tensor-core variant of the fast kernels covers this direction and D.
+bool tc_path_ok(bool bwd, int D);
 size_t generic_smem_bytes(bool bwd, int K, int SH2, int D);
 
 cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream);
