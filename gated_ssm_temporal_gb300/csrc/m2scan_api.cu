@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -15,6 +16,7 @@
 namespace m2scan {
 cudaError_t prepare_fast_kernels(int max_smem);
 cudaError_t prepare_generic_kernels(int max_smem);
+cudaError_t prepare_fwd_tc_kernels(int max_smem);
 }  // namespace m2scan
 
 using namespace m2scan;
@@ -64,6 +66,7 @@ m2scan_status prepare_device(int* dev_out) {
   if (major != 10 || minor != 3) return M2SCAN_ERR_DEVICE;  // built for sm_103a only
   if ((e = prepare_fast_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_generic_kernels(smem)) != cudaSuccess) return cuda_fail(e);
+  if ((e = prepare_fwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   void* p = nullptr;
   if ((e = cudaGetSymbolAddress(&p, g_m2scan_err_word)) != cudaSuccess) return cuda_fail(e);
   if (!g_encode) {
@@ -78,6 +81,20 @@ m2scan_status prepare_device(int* dev_out) {
   g_max_smem[dev] = smem;
   g_prepared[dev] = true;
   return M2SCAN_OK;
+}
+
+// Debug timeline of the fused kernels (builds with M2SCAN_TRACE): the address
+// of a device buffer given by M2SCAN_TRACE_PTR, else none.
+unsigned long long* trace_buffer() {
+#ifdef M2SCAN_TRACE
+  static unsigned long long* p = [] {
+    const char* s = getenv("M2SCAN_TRACE_PTR");
+    return s ? reinterpret_cast<unsigned long long*>(strtoull(s, nullptr, 0)) : nullptr;
+  }();
+  return p;
+#else
+  return nullptr;
+#endif
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -106,12 +123,14 @@ m2scan_status check_shape(int64_t B, int32_t K, int32_t SH2, int32_t D) {
 
 int slots_for(int64_t B) { return B < kMaxSlots ? static_cast<int>(B) : kMaxSlots; }
 
-// 1 = fast path, 2 = generic, 0 = unsupported.
+// 1 = fast path (plan->tc set when the tensor-core kernel is used), 2 = generic,
+// 0 = unsupported.
 int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_smem,
                 FastArgs* plan) {
-  if (!g_force_generic.load() && B <= 0x7fffffffll && fast_plan(bwd, K, SH2, D, plan) &&
-      plan->smem_bytes <= max_smem)
-    return 1;
+  if (!g_force_generic.load() && B <= 0x7fffffffll) {
+    if (!bwd && fwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
+    if (fast_plan(bwd, K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
+  }
   if (generic_smem_bytes(bwd, K, SH2, D) <= static_cast<size_t>(max_smem)) return 2;
   return 0;
 }
@@ -227,9 +246,9 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
     fa.h_history = h_history; fa.h_s2 = h_s2; fa.g = nullptr;
     fa.W_A = W_A; fa.W_B = W_B; fa.W_C = W_C; fa.W_O = W_O;
     fa.out0 = h_enriched; fa.out1 = nullptr; fa.ws = nullptr;
-    fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw;
+    fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, nullptr, B)) return M2SCAN_ERR_UNSUPPORTED;
-    e = launch_fast(false, D, fa, grid, stream);
+    e = fa.tc ? launch_fwd_tc(D, fa, grid, stream) : launch_fast(false, D, fa, grid, stream);
   } else {
     GenericArgs ga{h_history, h_s2, nullptr, W_A, W_B, W_C, W_O, h_enriched, nullptr, nullptr,
                    B, K, SH2, D, tw};
@@ -290,7 +309,7 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
     fa.h_history = h_history; fa.h_s2 = h_s2; fa.g = d_h_enriched;
     fa.W_A = W_A; fa.W_B = W_B; fa.W_C = W_C; fa.W_O = W_O;
     fa.out0 = d_h_history; fa.out1 = d_h_s2; fa.ws = ws;
-    fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw;
+    fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, d_h_enriched, B)) return M2SCAN_ERR_UNSUPPORTED;
     e = launch_fast(true, D, fa, grid, stream);
   } else {

@@ -33,6 +33,23 @@
 namespace m2scan {
 namespace {
 
+// Debug timeline (compiled in with -DM2SCAN_TRACE only): thread 0 of CTA 0
+// records %globaltimer at phase boundaries into FastArgs::trace.
+#ifdef M2SCAN_TRACE
+#define M2_TRACE(tag)                                                        \
+  do {                                                                       \
+    if (a.trace && blockIdx.x == 0 && threadIdx.x == 0 && trace_n < 4096) {  \
+      a.trace[2 * trace_n] = (tag);                                          \
+      a.trace[2 * trace_n + 1] = global_timer_ns();                          \
+      ++trace_n;                                                             \
+    }                                                                        \
+  } while (0)
+#else
+#define M2_TRACE(tag) \
+  do {                \
+  } while (0)
+#endif
+
 // Index of W_A|W_B element (j, col) in the swizzled shared copy: rows of 2D
 // floats, 16-byte chunk index XORed with bits of j so that both the
 // projection loop (one row, four lanes) and the d_h_history loop (rows
@@ -87,26 +104,36 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   float* sDC = reinterpret_cast<float*>(base + a.off_dc);     // dC [S_max][D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + a.off_bar);
   // tensor-core path
-  float* sHlo = reinterpret_cast<float*>(base + a.off_hlo);   // 2 x [128][32], swizzled
   float* sWt = reinterpret_cast<float*>(base + a.off_wt);     // NC tiles [2D][32], swizzled
   float* sWtlo = reinterpret_cast<float*>(base + a.off_wtlo);
   uint64_t* mbars = reinterpret_cast<uint64_t*>(base + a.off_mbar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + a.off_tslot);
   const int NST = a.n_stages;
-  // loads are issued this many items ahead; the tensor-core path keeps one stage
-  // back for the MMAs still reading it
-  const int PF = TC ? NST - 1 : NST;
+  // loads are issued this many items ahead (a stage is free once the threads
+  // have read it: the MMAs read their operands from TMEM and the weight tiles)
+  const int PF = NST;
+
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int trace_n = 0;
+  (void)trace_n;
+  M2_TRACE(1);
   const int K = a.K, SH2 = a.SH2, S_max = a.S_max, SG = a.SG;
   const int NC = SH2 / kChunk;
+  // TMEM columns: [0, NC*2D) one accumulator per chunk, then the corrections,
+  // then two A-operand buffers of 64 columns (32 hi + 32 lo) at a_col0
+  const uint32_t a_col0 = static_cast<uint32_t>((NC + 1) * TD);
   const long long B = a.B;
   const int P = gridDim.x, cta = blockIdx.x;
   const long long cb0 = B * cta / P;
   const int n_c = static_cast<int>(B * (cta + 1) / P - cb0);
   const int T = (n_c + S_max - 1) / S_max;
 
-  auto tile_start = [&](int i) -> long long { return cb0 + static_cast<long long>(n_c) * i / T; };
+  // tile i holds base (+1 for the first `extra` tiles) samples: no division per tile
+  const int t_base = n_c / T, t_extra = n_c - (n_c / T) * T;
+  auto tile_start = [&](int i) -> long long {
+    return cb0 + static_cast<long long>(i) * t_base + (i < t_extra ? i : t_extra);
+  };
   auto tile_items = [&](int S_t) -> int {
     int n = NC + (S_t + SG - 1) / SG;
     if (BWD) n += (S_t * K + kRowsPerItem - 1) / kRowsPerItem;
@@ -125,12 +152,15 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     unsigned char* st = base + static_cast<size_t>(stage) * a.stage_bytes;
     uint64_t* bar = &bars[stage];
     const int idx = pf_idx;
+    M2_TRACE(60);
     if (idx < NC) {
       const uint32_t bytes = a.hc_bytes + a.sc_bytes * (BWD ? 2 : 1);
       mbar_arrive_expect_tx(bar, bytes);
+      M2_TRACE(61);
       tma_load_3d(st, &a.tm_h, idx * kChunk, 0, static_cast<int>(tb0), bar);
       tma_load_2d(st + a.off_S, &a.tm_hs, idx * kChunk, static_cast<int>(tb0), bar);
       if (BWD) tma_load_2d(st + a.off_G, &a.tm_g, idx * kChunk, static_cast<int>(tb0), bar);
+      M2_TRACE(62);
     } else if (idx < NC + NSI) {
       const int s0 = (idx - NC) * SG;
       const int ns = min(SG, S_t - s0);
@@ -153,6 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   };
 
   if (tid == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_h)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_hs)) : "memory");
+    if (BWD) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_g)) : "memory");
     for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
     if (TC)
       for (int s = 0; s < 2; ++s) mbar_init(&mbars[s], 1);
@@ -166,27 +199,42 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   if (tid == 0)
     for (int s = 0; s < PF; ++s) issue_next();
 
-  // weights into shared memory (overlaps the first loads)
-  for (int i = tid; i < SH2 * D; i += kThreads) {
+  // weights into shared memory (overlaps the first loads); SH2*D <= 4096 gives at
+  // most 16 elements per thread: all global loads are issued before any store
+  constexpr int kWPer = 4096 / kThreads;
+  float wa[kWPer], wb[kWPer], wc[kWPer], wo[kWPer];
+#pragma unroll
+  for (int u = 0; u < kWPer; ++u) {
+    const int i = tid + u * kThreads;
+    const bool ok = i < SH2 * D;
+    wa[u] = ok ? __ldg(a.W_A + i) : 0.f;
+    wb[u] = ok ? __ldg(a.W_B + i) : 0.f;
+    wc[u] = ok ? __ldg(a.W_C + i) : 0.f;
+    wo[u] = ok ? __ldg(a.W_O + i) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kWPer; ++u) {
+    const int i = tid + u * kThreads;
+    if (i >= SH2 * D) break;
     const int j = i / D, d = i - j * D;
-    const float wa = a.W_A[i], wb = a.W_B[i];
     if (!TC || BWD) {
-      sW_AB[wab_idx<D>(j, d)] = wa;
-      sW_AB[wab_idx<D>(j, D + d)] = wb;
+      sW_AB[wab_idx<D>(j, d)] = wa[u];
+      sW_AB[wab_idx<D>(j, D + d)] = wb[u];
     }
     if (TC) {  // B operand of the projection MMA: tile q = [2D rows][32 columns of SH2]
       const int tq = (j >> 5) * TD * 32, jj = j & 31;
-      const float ha = tf32_rn(wa), hb = tf32_rn(wb);
+      const float ha = tf32_rn(wa[u]), hb = tf32_rn(wb[u]);
       sWt[tq + sw128_idx(d, jj)] = ha;
-      sWtlo[tq + sw128_idx(d, jj)] = wa - ha;
+      sWtlo[tq + sw128_idx(d, jj)] = wa[u] - ha;
       sWt[tq + sw128_idx(D + d, jj)] = hb;
-      sWtlo[tq + sw128_idx(D + d, jj)] = wb - hb;
+      sWtlo[tq + sw128_idx(D + d, jj)] = wb[u] - hb;
     }
-    sW_Ct[d * SH2 + j] = a.W_C[i];
+    sW_Ct[d * SH2 + j] = wc[u];
+    sW_O[i] = wo[u];
   }
-  for (int i = tid; i < D * SH2; i += kThreads) sW_O[i] = a.W_O[i];
   if (TC) fence_proxy_async_smem();
   __syncthreads();
+  M2_TRACE(2);
 
   // ---- per-thread ownership of weight-gradient entries (backward)
   const int pjq_ab = tid / KQN, pkq = tid - (tid / KQN) * KQN;  // dW_A|dW_B: 4 rows x 8 cols
@@ -212,15 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
   const int sd_s = (tid >> 2) / NQ;
 
   int seq = 0;
-  int mma_id = 0;       // chunks whose MMAs have been issued (all threads count)
-  int prev_chunk = -1;  // thread 0: MMA id of the previous item if it was a chunk
-  // thread 0, end of an item: the stage of the previous item is refilled; on the
-  // tensor-core path its MMAs must have finished reading it first
-  auto refill = [&](int this_chunk) {
-    if (TC && prev_chunk >= 0) bounded_wait(&mbars[prev_chunk & 1], (prev_chunk >> 1) & 1, a.err);
-    prev_chunk = this_chunk;
-    issue_next();
-  };
+  int mma_id = 0;  // chunks whose MMAs have been issued (all threads count)
   for (int tile = 0; tile < T; ++tile) {
     const long long tb0 = tile_start(tile);
     const int S_t = static_cast<int>(tile_start(tile + 1) - tb0);
@@ -239,24 +279,36 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
 
     for (int q = 0; q < NC; ++q, ++seq) {
       const int stage = seq % NST;
+      M2_TRACE(10);
       bounded_wait(&bars[stage], (seq / NST) & 1, a.err);
+      M2_TRACE(11);
       const float* Hc = reinterpret_cast<const float*>(base + static_cast<size_t>(stage) * a.stage_bytes);
       const float* Sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_S);
       const float* Gc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_G);
-      float* hlo = sHlo + (mma_id & 1) * (kTileRows * 32);
       if constexpr (TC) {
-        // the MMAs of chunk mma_id-2 read this h_lo buffer: wait for them
+        // A operand into TMEM: thread = tile row (lane), warps 0-3 take columns
+        // 0-15 of the chunk and warps 4-7 columns 16-31; h = hi + lo with
+        // hi = tf32_rn(h). Rows past the h box hold don't-care values.
+        // The MMAs of chunk mma_id-2 read this TMEM buffer: wait for them.
         if (mma_id >= 2) bounded_wait(&mbars[mma_id & 1], ((mma_id - 2) >> 1) & 1, a.err);
-        // h = hi + lo: hi = tf32_rn(h) overwrites the h box in place, lo goes to hlo.
-        // Only the box's own rows are touched (the h_s2 box may follow it); rows of
-        // the 128-row MMA tile past the box are don't-care rows of the result.
-        float* Hw = const_cast<float*>(Hc);
-        for (int i = 4 * tid; i < a.hc_bytes / 4; i += 4 * kThreads) {
-          const float4 v = lds4(Hc + i);
-          const float4 h = make_float4(tf32_rn(v.x), tf32_rn(v.y), tf32_rn(v.z), tf32_rn(v.w));
-          sts4(Hw + i, h);
-          sts4(hlo + i, make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w));
+        const int row = 32 * (warp & 3) + lane, half = warp >> 2;
+        float hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = lds4(Hc + row * 32 + ((((4 * half + i) ^ (row & 7))) << 2));
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[4 * i + e] = tf32_rn(vv[e]);
+            lo[4 * i + e] = vv[e] - hi[4 * i + e];
+          }
         }
+        const uint32_t ta = tmem_acc + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + a_col0 +
+                            64u * (mma_id & 1) + 16u * half;
+        tmem_st16(ta, hi);
+        tmem_st16(ta + 32, lo);
+        tmem_st_wait();
+        tc_fence_before();
       } else if (gemm_active) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -305,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
           }
         }
       }
-      if (TC) fence_proxy_async_smem();
+      M2_TRACE(12);
       __syncthreads();
+      M2_TRACE(13);
       if (tid == 0) {
         if constexpr (TC) {
           // A|B = sum over chunks of h_hi.W_hi, plus the corrections
@@ -315,20 +368,23 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
           // share one (columns NC*2D): few accumulation steps per accumulator keep
           // the tensor cores' accumulation error at the level of fp32 FMA.
           tc_fence_after();
+          M2_TRACE(14);
+          issue_next();  // the stage just read is free
+          M2_TRACE(15);
           constexpr uint32_t idesc = umma_idesc_tf32(128, TD);
-          const uint32_t ah = smem_addr(Hc), al = smem_addr(hlo);
+          const uint32_t ah = tmem_acc + a_col0 + 64u * (mma_id & 1), al = ah + 32u;
           const uint32_t bh = smem_addr(sWt + q * TD * 32), bl = smem_addr(sWtlo + q * TD * 32);
           const uint32_t d_main = tmem_acc + q * TD, d_corr = tmem_acc + NC * TD;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t o = 32u * ks;
-            umma_tf32(d_main, umma_desc_sw128(ah + o), umma_desc_sw128(bh + o), idesc, ks != 0);
-            umma_tf32(d_corr, umma_desc_sw128(ah + o), umma_desc_sw128(bl + o), idesc,
-                      (q | ks) != 0);
-            umma_tf32(d_corr, umma_desc_sw128(al + o), umma_desc_sw128(bh + o), idesc, 1u);
+            umma_tf32_ta(d_main, ah + 8u * ks, umma_desc_sw128(bh + o), idesc, ks != 0);
+            umma_tf32_ta(d_corr, ah + 8u * ks, umma_desc_sw128(bl + o), idesc, (q | ks) != 0);
+            umma_tf32_ta(d_corr, al + 8u * ks, umma_desc_sw128(bh + o), idesc, 1u);
           }
+          M2_TRACE(16);
           umma_commit(&mbars[mma_id & 1]);
-          refill(mma_id);
+          M2_TRACE(17);
         } else {
           issue_next();
         }
@@ -336,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
       if (TC) ++mma_id;
     }
 
+    M2_TRACE(20);
     // ---- A|B tile into shared memory; finish C, d_ctx
     if constexpr (TC) {
       const int last = mma_id - 1;
@@ -399,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     }
     __syncthreads();
 
+    M2_TRACE(21);
     // ================= scan (one thread per sample and state) ============
     if (tid < S_t * D) {
       const int s = tid / D, d = tid - (tid / D) * D;
@@ -436,11 +494,14 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     }
     __syncthreads();
 
+    M2_TRACE(22);
     // ================= pass 2a: per-sample outputs =======================
     const int njq = SH2 / 4;
     for (int k = 0; k < NSI; ++k, ++seq) {
       const int stage = seq % NST;
+      M2_TRACE(30);
       bounded_wait(&bars[stage], (seq / NST) & 1, a.err);
+      M2_TRACE(31);
       float* hsb = reinterpret_cast<float*>(base + static_cast<size_t>(stage) * a.stage_bytes);
       const int s0 = k * SG, ns = min(SG, S_t - s0);
       const int nit = ((ns + 3) / 4) * njq;
@@ -531,10 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
       __syncthreads();
       if (tid == 0) {
         float* dst = (BWD ? a.out1 : a.out0) + (tb0 + s0) * SH2;
+        M2_TRACE(32);
         bulk_store(dst, hsb, static_cast<uint32_t>(ns) * SH2 * 4u);
         bulk_commit();
         bulk_wait_read_all();
-        if (TC) refill(-1); else issue_next();
+        M2_TRACE(33);
+        issue_next();
       }
     }
 
@@ -543,7 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
       const int NRI = (R_t + kRowsPerItem - 1) / kRowsPerItem;
       for (int k = 0; k < NRI; ++k, ++seq) {
         const int stage = seq % NST;
+        M2_TRACE(40);
         bounded_wait(&bars[stage], (seq / NST) & 1, a.err);
+        M2_TRACE(41);
         float* hb = reinterpret_cast<float*>(base + static_cast<size_t>(stage) * a.stage_bytes);
         const int r0 = k * kRowsPerItem, nr = min(kRowsPerItem, R_t - r0);
         // dW_A | dW_B partial sums: sum over rows of h[row, j] * dAB[row, col]
@@ -597,10 +662,12 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
+          M2_TRACE(42);
           bulk_store(a.out0 + (tb0 * K + r0) * SH2, hb, static_cast<uint32_t>(nr) * SH2 * 4u);
           bulk_commit();
           bulk_wait_read_all();
-          if (TC) refill(-1); else issue_next();
+          M2_TRACE(43);
+          issue_next();
         }
       }
     }
@@ -632,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
         }
     }
   }
+  M2_TRACE(50);
   if (tid == 0) bulk_wait_all();
   if constexpr (TC) {
     tc_fence_before();
@@ -647,8 +715,13 @@ bool fast_path_ok(int K, int SH2, int D) {
          SH2 * D <= 4096 && K >= 1 && K <= kTileRows;
 }
 
-// The tensor-core variant: forward, D in {8, 16} (MMA N = 2D must be a multiple of 16).
-bool tc_path_ok(bool bwd, int D) { return !bwd && (D == 8 || D == 16); }
+// The TC variant of this kernel is not used (the forward has its own
+// warp-specialised tensor-core kernel).
+bool tc_path_ok(bool bwd, int D) {
+  (void)bwd;
+  (void)D;
+  return false;
+}
 
 static int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -669,11 +742,17 @@ bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a) {
   if (bwd && kRowsPerItem * SH2 * 4 > stage) stage = kRowsPerItem * SH2 * 4;
   if (kTileRows * 128 > stage) stage = kTileRows * 128;  // a 128-row tile is always read
   stage = round_up(stage, 1024);
-  const int n_stages = tc ? 3 : kStages;
+  // the rest of the plan does not depend on the ring depth: lay it out after a
+  // ring of kMaxStages and shrink the ring if that does not fit
+  int rest = 0;
+  if (tc) rest += 2 * SH2 * 2 * D * 4;
+  if (!tc || bwd) rest += SH2 * 2 * D * 4;
+  rest += 2 * D * SH2 * 4 + kTileRows * (2 * D + 4) * 4 + 4 * S_max * D * 4 + 1024 + 1024;
+  int n_stages = tc ? kMaxStages : kStages;
+  while (n_stages > 2 && n_stages * stage + rest > 227 * 1024) --n_stages;
   int off = n_stages * stage;
   a->off_hlo = a->off_wt = a->off_wtlo = off;
   if (tc) {
-    a->off_hlo = off;  off += 2 * kTileRows * 128;
     a->off_wt = off;   off += SH2 * 2 * D * 4;
     a->off_wtlo = off; off += SH2 * 2 * D * 4;
   }
@@ -702,9 +781,10 @@ bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a) {
   a->SH2 = SH2;
   a->n_stages = n_stages;
   a->tc = tc ? 1 : 0;
-  // TMEM: one accumulator block per SH2 chunk plus one for the correction terms
+  // TMEM: one accumulator block per SH2 chunk, one for the correction terms and
+  // two 64-column A-operand buffers
   int cols = 32;
-  while (cols < (SH2 / kChunk + 1) * 2 * D) cols *= 2;
+  while (cols < (SH2 / kChunk + 1) * 2 * D + 128) cols *= 2;
   a->tmem_cols = cols;
   return a->smem_bytes <= 227 * 1024;
 }
@@ -717,13 +797,6 @@ static cudaError_t launch_one(const FastArgs& a, int grid, cudaStream_t stream) 
 }
 
 cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream) {
-  if (a.tc) {
-    switch (D) {
-      case 8: return launch_one<8, false, true>(a, grid, stream);
-      case 16: return launch_one<16, false, true>(a, grid, stream);
-      default: return cudaErrorInvalidValue;
-    }
-  }
   switch (D) {
     case 4: return bwd ? launch_one<4, true, false>(a, grid, stream) : launch_one<4, false, false>(a, grid, stream);
     case 8: return bwd ? launch_one<8, true, false>(a, grid, stream) : launch_one<8, false, false>(a, grid, stream);
@@ -739,7 +812,7 @@ cudaError_t prepare_fast_kernels(int max_smem) {
     e = cudaFuncSetAttribute(fast_kernel<DD, BB, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              max_smem);
   M2_SET(4, false, false) M2_SET(4, true, false) M2_SET(8, false, false) M2_SET(8, true, false)
-  M2_SET(16, false, false) M2_SET(16, true, false) M2_SET(8, false, true) M2_SET(16, false, true)
+  M2_SET(16, false, false) M2_SET(16, true, false)
 #undef M2_SET
   return e;
 }

@@ -11,7 +11,7 @@ namespace m2scan {
 
 constexpr int kThreads = 256;     // threads per CTA, every kernel
 constexpr int kStages = 3;        // depth of the copy ring of the FP32-FMA fast kernels
-constexpr int kMaxStages = 4;     // ring depth, at most (any fast kernel)
+constexpr int kMaxStages = 6;     // ring depth, at most (any fast kernel)
 constexpr int kMaxSlots = 152;    // CTAs (= weight-gradient slots) per call, at most
 constexpr int kTileRows = 128;    // rows (samples x K) per pass-1 tile, at most
 constexpr int kChunk = 32;        // SH2 columns per pass-1 chunk (128 bytes)
@@ -37,6 +37,7 @@ struct alignas(128) FastArgs {
   float* out1;  // backward: d_h_s2
   float* ws;    // backward: weight-gradient slots [P][4][SH2*D]
   unsigned* err;
+  unsigned long long* trace;  // debug timeline buffer (builds with M2SCAN_TRACE), else null
   long long B;
   int K;
   int SH2;
@@ -87,6 +88,9 @@ bool tc_path_ok(bool bwd, int D);
 size_t generic_smem_bytes(bool bwd, int K, int SH2, int D);
 
 cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream);
+// Warp-specialised tensor-core forward (D in {8, 16}).
+bool fwd_tc_plan(int K, int SH2, int D, FastArgs* a);
+cudaError_t launch_fwd_tc(int D, const FastArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem,
                            cudaStream_t stream);
 cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float* dW_B,
