@@ -17,6 +17,7 @@ namespace m2scan {
 cudaError_t prepare_fast_kernels(int max_smem);
 cudaError_t prepare_generic_kernels(int max_smem);
 cudaError_t prepare_fwd_tc_kernels(int max_smem);
+cudaError_t prepare_bwd_tc_kernels(int max_smem);
 }  // namespace m2scan
 
 using namespace m2scan;
@@ -67,6 +68,7 @@ m2scan_status prepare_device(int* dev_out) {
   if ((e = prepare_fast_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_generic_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_fwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
+  if ((e = prepare_bwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   void* p = nullptr;
   if ((e = cudaGetSymbolAddress(&p, g_m2scan_err_word)) != cudaSuccess) return cuda_fail(e);
   if (!g_encode) {
@@ -129,6 +131,7 @@ int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_
                 FastArgs* plan) {
   if (!g_force_generic.load() && B <= 0x7fffffffll) {
     if (!bwd && fwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
+    if (bwd && bwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (fast_plan(bwd, K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
   }
   if (generic_smem_bytes(bwd, K, SH2, D) <= static_cast<size_t>(max_smem)) return 2;
@@ -311,7 +314,7 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
     fa.out0 = d_h_history; fa.out1 = d_h_s2; fa.ws = ws;
     fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, d_h_enriched, B)) return M2SCAN_ERR_UNSUPPORTED;
-    e = launch_fast(true, D, fa, grid, stream);
+    e = fa.tc ? launch_bwd_tc(fa, grid, stream) : launch_fast(true, D, fa, grid, stream);
   } else {
     GenericArgs ga{h_history, h_s2, d_h_enriched, W_A, W_B, W_C, W_O, d_h_history, d_h_s2, ws,
                    B, K, SH2, D, tw};

@@ -314,4 +314,22 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Debug timeline (builds with -DM2SCAN_TRACE): CTA 0 records %globaltimer per
+// role into the kernel argument's trace buffer (compute thread 0: entries 0.., producer: 1024..,
+// MMA issuer: 2048..).
+#ifdef M2SCAN_TRACE
+#define TRACE_AT(region, tag)                                                    \
+  do {                                                                           \
+    if (a.trace && blockIdx.x == 0 && trace_n < 1000) {                          \
+      a.trace[2 * ((region) * 1024 + trace_n)] = (tag);                          \
+      a.trace[2 * ((region) * 1024 + trace_n) + 1] = global_timer_ns();          \
+      ++trace_n;                                                                 \
+    }                                                                            \
+  } while (0)
+#else
+#define TRACE_AT(region, tag) \
+  do {                        \
+  } while (0)
+#endif
+
 }  // namespace m2scan

@@ -30,24 +30,6 @@
 namespace m2scan {
 namespace {
 
-// Debug timeline (builds with -DM2SCAN_TRACE): CTA 0 records %globaltimer per
-// role into FastArgs::trace (compute thread 0: entries 0.., producer: 1024..,
-// MMA issuer: 2048..).
-#ifdef M2SCAN_TRACE
-#define TRACE_AT(region, tag)                                                    \
-  do {                                                                           \
-    if (a.trace && blockIdx.x == 0 && trace_n < 1000) {                          \
-      a.trace[2 * ((region) * 1024 + trace_n)] = (tag);                          \
-      a.trace[2 * ((region) * 1024 + trace_n) + 1] = global_timer_ns();          \
-      ++trace_n;                                                                 \
-    }                                                                            \
-  } while (0)
-#else
-#define TRACE_AT(region, tag) \
-  do {                        \
-  } while (0)
-#endif
-
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kFwdThreads = kComputeThreads + 64;

@@ -91,6 +91,9 @@ cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream
 // Warp-specialised tensor-core forward (D in {8, 16}).
 bool fwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_fwd_tc(int D, const FastArgs& a, int grid, cudaStream_t stream);
+// Warp-specialised tensor-core backward (D = 16).
+bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a);
+cudaError_t launch_bwd_tc(const FastArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem,
                            cudaStream_t stream);
 cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float* dW_B,
