@@ -1,75 +1,93 @@
-// Backward of the gated temporal scan layer with two of its three large
-// contractions on the tensor cores, warp-specialised (D = 16, SH2 % 32 == 0,
-// SH2 <= 256, K <= 128).
+// Backward of the gated temporal scan layer with its three large contractions
+// on the tensor cores, warp-specialised (D = 16, SH2 % 32 == 0, SH2 <= 256,
+// K <= 128).
 //
-// Per tile of at most 128 rows (S samples x K) of one persistent CTA:
-//   pass 1   (as in the forward) the producer warp streams 32-column chunks of
-//            h_history, h_s2 and d_h_enriched; the compute warps split each h
-//            row into tf32 hi/lo parts stored in TMEM; the MMA warp accumulates
-//            A|B = h . [W_A|W_B] (3 x tf32); the compute warps also form
+// One persistent CTA per weight-gradient slot walks its samples in tiles of at
+// most 128 rows (S samples x K). Per tile:
+//   pass 1   the producer warp streams 32-column chunks of h_history, h_s2 and
+//            d_h_enriched (TMA boxes, 128-byte swizzle). The MMA warp
+//            recomputes A|B = h . [W_A|W_B] with the chunk as the A operand
+//            straight from shared memory (the tensor core reads the top 19 bits
+//            of each fp32, i.e. trunc(h)); the compute warps then overwrite the
+//            chunk with h - trunc(h) (rounded to tf32) and the MMA warp adds
+//            that remainder's product. The compute warps also form
 //            C = h_s2 . W_C and d_ctx = tw dY . W_O^T on the FMA pipe.
 //   scan     replay of the forward scan and the reverse scan of the
 //            implementation plan's Task 2 ("Custom Kernel Optimization
 //            Implementation Plan"): dB_t = dx, dA_t = dx x_{t-1} sigmoid'(A_t),
-//            dx <- dx sigmoid(A_t); dA|dB are left in shared memory split into a
-//            tf32 part and an exact remainder (the MMA's B operand).
-//   d_h      the MMA warp computes d_h_history transposed,
-//            D[j, row] = [W_A|W_B][j, :] . dA|dB[row, :], A operand [W_A|W_B]
-//            (hi/lo, kept in TMEM for the whole kernel), B operand dA|dB
-//            (hi/lo), 3 x tf32; the compute warps read D back (thread = column
-//            j, so each store instruction writes one contiguous row segment).
-//   per row  dW_A|dW_B partial sums on the FMA pipe over the tile's rows,
-//            streamed again as 16-row items (register accumulators).
-//   per sample dW_C, dW_O partial sums and d_h_s2 = dY + dC . W_C^T.
-// Weight-gradient partial sums are written once to the CTA's workspace slot;
-// the slot reduction adds the slots in a fixed order.
+//            dx <- dx sigmoid(A_t). dA|dB is stored split into a tf32 part
+//            and the remainder, row-major (B operand of d_h); each 16-row
+//            item copies its rows transposed (B operand of dW_A|dW_B).
+//   d_h      d_h_history^T[j, row] = [W_A|W_B][j, :] . dA|dB[row, :] per
+//            64-row half of the tile, 3 x tf32, the weights (split the same
+//            way) held in tensor memory as the A operand.
+//   per row  the producer streams the tile's h_history rows again, 16 at a
+//            time; the compute warps write them transposed into tensor memory
+//            (h and h - trunc(h)) and the MMA warp accumulates
+//            dW_A|dW_B^T += h^T . dA|dB over every tile of the CTA. The same
+//            stage then carries the 16 rows of d_h_history out: the producer
+//            warp issues that bulk copy before it reuses the stage, so the
+//            output stream is spread over the tile and the compute warps
+//            never wait for it.
+//   per sample dW_C, dW_O partial sums and d_h_s2 = dY + dC . W_C^T (FMA pipe).
+// The weight-gradient partial sums are written once to the CTA's workspace
+// slot; the slot reduction adds the slots in a fixed order.
 #include "m2scan_device.cuh"
 #include "m2scan_internal.h"
 
 namespace m2scan {
 namespace {
 
-constexpr int kComputeWarps = 8;
+constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kBwdThreads = kComputeThreads + 64;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kRowItem = 16;      // h_history rows per dW item
+constexpr int kProducerWarp = kComputeWarps;
+constexpr int kMmaWarp = kComputeWarps + 1;
+constexpr int kRowItem = 16;       // h_history rows per dW item
 constexpr int kBwdSampleItem = 8;  // samples per dW_C/dW_O/d_h_s2 item
 
 struct BwdBars {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t aready[2];
-  uint64_t afree[2];
-  uint64_t accfull;  // MMA -> compute: projections of the tile done
-  uint64_t bready;   // compute -> MMA: dA|dB operand tiles written
-  uint64_t bdone;    // MMA -> compute: d_h MMAs of the tile done
-  uint64_t dhfree;   // compute -> MMA: d_h read back, TMEM [0, 256) free
+  uint64_t full[kMaxStages];   // producer -> all: stage loaded
+  uint64_t empty[kMaxStages];  // stage free (MMA commit for chunks, compute otherwise)
+  uint64_t maindone[2];        // MMA -> compute: chunk read as h, may be overwritten
+  uint64_t loready[2];         // compute -> MMA: chunk holds h - trunc(h)
+  uint64_t accfull;            // MMA -> compute: projections of the tile done
+  uint64_t bready;             // compute -> MMA: dA|dB operands written
+  uint64_t dhready[2];         // MMA -> compute: d_h of a 64-row half done
+  uint64_t dhfree[2];          // compute -> MMA: that d_h read back
+  uint64_t htready[2];         // compute -> MMA: transposed rows in TMEM
+  uint64_t htfree[2];          // MMA -> compute: transposed rows consumed
+  uint64_t dwdone;             // MMA -> compute: every dW MMA done
   uint32_t tslot;
   uint32_t pad;
 };
 
-// TMEM columns: [0, 256) projection accumulators (4 pairs of [main | corrections],
-// 64 columns each), later the transposed d_h (two 128-row halves of SH2);
-// [256, 384) two A-operand buffers of the projection (32 hi + 32 lo);
-// [384, 512) [W_A|W_B] as the d_h A operand: per half of SH2, 32 hi + 32 lo.
-constexpr uint32_t kAcolA = 256;
-constexpr uint32_t kWcol = 384;
+// TMEM columns (128 lanes each):
+//   [0, 128)    projection accumulators, two [main | corrections] pairs of 64;
+//               later d_h^T of one 64-row half: j-half h at 64 h (N = 64 rows)
+//   [128, 256)  transposed h rows, two buffers p of [j-half 0 | j-half 1],
+//               each 16 columns of h then 16 of h - trunc(h)
+//   [256, 384)  dW_A|dW_B^T accumulators: j-half h at 256 + 64 h,
+//               [h . dAB_hi (32) | h . dAB_lo + (h - trunc h) . dAB_hi (32)]
+//   [384, 512)  [W_A|W_B] rows as the d_h A operand: j-half h at 384 + 64 h,
+//               32 columns tf32 part, 32 columns remainder
+constexpr uint32_t kColHT = 128;
+constexpr uint32_t kColDW = 256;
+constexpr uint32_t kColW = 384;
 
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_constant__ FastArgs a) {
   constexpr int D = 16, TD = 32, FD = 64;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  float* sW = reinterpret_cast<float*>(base + a.off_wt);      // NC tiles [FD][32], swizzled
-  float* sW_Ct = reinterpret_cast<float*>(base + a.off_wct);  // W_C transposed [D][SH2]
-  float* sW_O = reinterpret_cast<float*>(base + a.off_wo);    // W_O [D][SH2]
-  float* sPh = reinterpret_cast<float*>(base + a.off_p);      // A|B, then dA|dB (tf32 part) [128][32] swizzled
-  float* sPl = reinterpret_cast<float*>(base + a.off_hlo);    // dA|dB remainder, same layout
-  float* sC = reinterpret_cast<float*>(base + a.off_cs);      // C [S_max][D]
-  float* sCtx = reinterpret_cast<float*>(base + a.off_ctx);   // ctx [S_max][D]
-  float* sDctx = reinterpret_cast<float*>(base + a.off_dctx); // d_ctx [S_max][D]
-  float* sDC = reinterpret_cast<float*>(base + a.off_dc);     // dC [S_max][D]
+  float* sW = reinterpret_cast<float*>(base + a.off_wt);       // NC tiles [FD][32], swizzled
+  float* sW_Ct = reinterpret_cast<float*>(base + a.off_wct);   // W_C transposed [D][SH2]
+  float* sPh = reinterpret_cast<float*>(base + a.off_p);       // A|B, then dA|dB tf32 part [128][32] swizzled
+  float* sPl = reinterpret_cast<float*>(base + a.off_hlo);     // dA|dB remainder, same layout
+  float* sDT = reinterpret_cast<float*>(base + a.off_wab);     // dA|dB^T [hi 32 | lo 32][2 x 16 rows], swizzled
+  float* sC = reinterpret_cast<float*>(base + a.off_cs);       // C [S_max][D]
+  float* sCtx = reinterpret_cast<float*>(base + a.off_ctx);    // ctx [S_max][D]
+  float* sDctx = reinterpret_cast<float*>(base + a.off_dctx);  // d_ctx [S_max][D]
+  float* sDC = reinterpret_cast<float*>(base + a.off_dc);      // dC [S_max][D]
   BwdBars* bb = reinterpret_cast<BwdBars*>(base + a.off_bar);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -77,7 +95,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   (void)trace_n;
   if (tid == 0) TRACE_AT(0, 1);
   const int K = a.K, SH2 = a.SH2, S_max = a.S_max, NST = a.n_stages;
-  const int NC = SH2 / kChunk;
+  const int NC = SH2 / kChunk, NP = NC < 2 ? NC : 2;
+  const int hc_rows = a.hc_bytes / 128;
   const long long B = a.B;
   const int P = gridDim.x, cta = blockIdx.x;
   const long long cb0 = B * cta / P;
@@ -96,16 +115,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_g)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
-      mbar_init(&bb->empty[s], kComputeWarps);
+      mbar_init(&bb->empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bb->aready[s], kComputeWarps);
-      mbar_init(&bb->afree[s], 1);
+      mbar_init(&bb->maindone[s], 1);
+      mbar_init(&bb->loready[s], kComputeWarps);
+      mbar_init(&bb->dhready[s], 1);
+      mbar_init(&bb->dhfree[s], 1);
+      mbar_init(&bb->htready[s], kComputeWarps);
+      mbar_init(&bb->htfree[s], 1);
     }
     mbar_init(&bb->accfull, 1);
     mbar_init(&bb->bready, 1);
-    mbar_init(&bb->bdone, 1);
-    mbar_init(&bb->dhfree, 1);
+    mbar_init(&bb->dwdone, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&bb->tslot, 512);
@@ -115,14 +137,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   const uint32_t tmem = bb->tslot;
   if (tid == 0) TRACE_AT(0, 3);
 
-  // ---- producer state: items per tile are NC chunks, sample items, row items
+  // ---- producer: per tile NC chunks, then sample items, then row items.
+  // A stage that held a sample or row item holds that item's output once the
+  // compute warps release it: the producer stores it before reusing the stage.
   int pseq = 0, ptile = 0, pit = 0;
+  int rseq = 0, rtile = 0, rit = 0;  // oldest item not yet released
+  auto release_one = [&]() {
+    const int st = rseq % NST;
+    bounded_wait(&bb->empty[st], (rseq / NST) & 1, a.err);
+    const long long tb0 = tile_start(rtile);
+    const int S_t = static_cast<int>(tile_start(rtile + 1) - tb0);
+    const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
+    const unsigned char* sp = base + static_cast<size_t>(st) * a.stage_bytes;
+    if (rit >= NC) {
+      if (rit < NC + NSI) {
+        const int s0 = (rit - NC) * kBwdSampleItem;
+        const int ns = min(kBwdSampleItem, S_t - s0);
+        bulk_store(a.out1 + (tb0 + s0) * SH2, sp, static_cast<uint32_t>(ns) * SH2 * 4u);
+      } else {
+        const int r0 = (rit - NC - NSI) * kRowItem;
+        const int nr = min(kRowItem, S_t * K - r0);
+        bulk_store(a.out0 + (tb0 * K + r0) * SH2, sp, static_cast<uint32_t>(nr) * SH2 * 4u);
+      }
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+    ++rseq;
+    if (++rit == NC + NSI + NRI) {
+      rit = 0;
+      ++rtile;
+    }
+  };
   auto produce_one = [&]() {
     const long long tb0 = tile_start(ptile);
     const int S_t = static_cast<int>(tile_start(ptile + 1) - tb0);
     const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
-    const int st = pseq % NST, use = pseq / NST;
-    if (use > 0) bounded_wait(&bb->empty[st], (use - 1) & 1, a.err);
+    const int st = pseq % NST;
+    if (pseq >= NST) release_one();
     unsigned char* sp = base + static_cast<size_t>(st) * a.stage_bytes;
     uint64_t* bar = &bb->full[st];
     if (pit < NC) {
@@ -153,11 +204,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   if (warp == kProducerWarp && lane == 0)
     for (int i = 0; i < NST && ptile < T; ++i) produce_one();
 
-  // ---- weights: projection B tiles and W_C^T, W_O into shared memory;
-  // [W_A|W_B] rows (hi/lo) into TMEM as the d_h A operand (compute warps)
+  // ---- weights: projection B tiles and W_C^T into shared memory
   constexpr int kWPer = (4096 + kBwdThreads - 1) / kBwdThreads;
   {
-    float wa[kWPer], wb[kWPer], wc[kWPer], wo[kWPer];
+    float wa[kWPer], wb[kWPer], wc[kWPer];
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
       const int i = tid + u * kBwdThreads;
@@ -165,7 +215,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       wa[u] = ok ? __ldg(a.W_A + i) : 0.f;
       wb[u] = ok ? __ldg(a.W_B + i) : 0.f;
       wc[u] = ok ? __ldg(a.W_C + i) : 0.f;
-      wo[u] = ok ? __ldg(a.W_O + i) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
@@ -174,30 +223,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       const int j = i / D, d = i - (i / D) * D;
       float* tile = sW + (j >> 5) * FD * 32;
       const int jj = j & 31;
-      const float ha = tf32_rna(wa[u]), hb = tf32_rna(wb[u]);
+      const float ha = tf32_rn(wa[u]), hb = tf32_rn(wb[u]);
       tile[sw128_idx(d, jj)] = ha;
       tile[sw128_idx(D + d, jj)] = hb;
       tile[sw128_idx(TD + d, jj)] = wa[u] - ha;
       tile[sw128_idx(TD + D + d, jj)] = wb[u] - hb;
       sW_Ct[d * SH2 + j] = wc[u];
-      sW_O[i] = wo[u];
     }
   }
+  // [W_A|W_B] rows into TMEM (thread = lane = row j within its j-half)
   if (warp < kComputeWarps) {
-    // thread = TMEM lane = row j of [W_A|W_B] within its half of SH2
-    const int half = warp >> 2, j = 128 * half + 32 * (warp & 3) + lane;
-    float hi[32], lo[32];
+    const int sub = warp >> 2, h = sub & 1, part = sub >> 1;
+    const int j = 128 * h + 32 * (warp & 3) + lane;
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float* src = (q < 4 ? a.W_A : a.W_B) + j * D + 4 * (q & 3);
+      const float4 w = j < SH2 ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+    }
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      const float w = j < SH2 ? __ldg((k < D ? a.W_A : a.W_B) + j * D + (k & (D - 1))) : 0.f;
-      hi[k] = tf32_rna(w);
-      lo[k] = w - hi[k];
+      const float hi = tf32_rn(v[k]);
+      v[k] = part == 0 ? hi : v[k] - hi;
     }
-    const uint32_t tw0 = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kWcol + 64u * half;
-    tmem_st16(tw0, hi);
-    tmem_st16(tw0 + 16u, hi + 16);
-    tmem_st16(tw0 + 32u, lo);
-    tmem_st16(tw0 + 48u, lo + 16);
+    const uint32_t tw0 = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kColW + 64u * h + 32u * part;
+    tmem_st16(tw0, v);
+    tmem_st16(tw0 + 16u, v + 16);
     tmem_st_wait();
   }
   fence_proxy_async_smem();
@@ -208,154 +260,194 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0)
+    if (lane == 0) {
       while (ptile < T) {
         TRACE_AT(1, 100 + pit);
         produce_one();
       }
+      while (rseq < pseq) release_one();
+      bulk_wait_all();
+    }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc_f = umma_idesc_tf32(128, FD);
-      constexpr uint32_t idesc_t = umma_idesc_tf32(128, TD);
-      constexpr uint32_t idesc_d = umma_idesc_tf32(128, 128);
-      const uint32_t ph = smem_addr(sPh), pl = smem_addr(sPl);
-      int c = 0;
-      for (int t = 0; t < T; ++t) {
-        if (t > 0) bounded_wait(&bb->dhfree, (t - 1) & 1, a.err);
-        TRACE_AT(2, 290);
-        for (int q = 0; q < NC; ++q, ++c) {
-          bounded_wait(&bb->aready[c & 1], (c >> 1) & 1, a.err);
-          TRACE_AT(2, 400 + q);
-          tc_fence_after();
-          const uint32_t ah = tmem + kAcolA + 64u * (c & 1), al = ah + 32u;
-          const uint32_t wt = smem_addr(sW + q * FD * 32);
-          const uint32_t d_pair = tmem + static_cast<uint32_t>((q >> 1) * FD);
+      constexpr uint32_t idesc64 = umma_idesc_tf32(128, 64);
+      constexpr uint32_t idesc32 = umma_idesc_tf32(128, 32);
+      const uint32_t ph = smem_addr(sPh), pl = smem_addr(sPl), dt = smem_addr(sDT);
+      const uint32_t ring = smem_addr(base);
+      auto issue_dh = [&](int rh) {
+        // d_h^T[j, 64 rh + n] for both j-halves; cross terms first
+        for (int h = 0; 128 * h < SH2; ++h) {
+          const uint32_t dd = tmem + 64u * h, wh = tmem + kColW + 64u * h, wl = wh + 32u;
+          const uint32_t bh0 = ph + 8192u * rh, bl0 = pl + 8192u * rh;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bdesc = umma_desc_sw128(wt + 32u * ks);
-            umma_tf32_ta(d_pair, ah + 8u * ks, bdesc, idesc_f, ((q & 1) | ks) != 0);
-            umma_tf32_ta(d_pair + TD, al + 8u * ks, bdesc, idesc_t, 1u);
-          }
-          umma_commit(&bb->afree[c & 1]);
-        }
-        umma_commit(&bb->accfull);
-        TRACE_AT(2, 500);
-        // d_h^T[j, row] = W[j, :] . dAB[row, :] per 128-row half of SH2
-        bounded_wait(&bb->bready, t & 1, a.err);
-        TRACE_AT(2, 600);
-        tc_fence_after();
-        for (int hh = 0; hh * 128 < SH2; ++hh) {
-          const uint32_t dd = tmem + 128u * hh;
-          const uint32_t wh = tmem + kWcol + 64u * hh, wl = wh + 32u;
-          // the two small cross terms first, then the main products on top
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bh = umma_desc_sw128(ph + 32u * ks), bl = umma_desc_sw128(pl + 32u * ks);
-            umma_tf32_ta(dd, wh + 8u * ks, bl, idesc_d, ks != 0);
-            umma_tf32_ta(dd, wl + 8u * ks, bh, idesc_d, 1u);
+            umma_tf32_ta(dd, wh + 8u * ks, umma_desc_sw128(bl0 + 32u * ks), idesc64, ks != 0);
+            umma_tf32_ta(dd, wl + 8u * ks, umma_desc_sw128(bh0 + 32u * ks), idesc64, 1u);
           }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_tf32_ta(dd, wh + 8u * ks, umma_desc_sw128(ph + 32u * ks), idesc_d, 1u);
+            umma_tf32_ta(dd, wh + 8u * ks, umma_desc_sw128(bh0 + 32u * ks), idesc64, 1u);
         }
-        umma_commit(&bb->bdone);
+      };
+      int seq = 0, c = 0, ri = 0;
+      bool dw_first = true;
+      for (int t = 0; t < T; ++t) {
+        const long long tb0 = tile_start(t);
+        const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
+        const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
+        TRACE_AT(2, 290);
+        if (t > 0) bounded_wait(&bb->dhfree[1], (t - 1) & 1, a.err);
+        tc_fence_after();
+        // pass 1: main products of chunk q, then the remainder products of q - 1
+        for (int q = 0; q <= NC; ++q) {
+          if (q < NC) {
+            const int it = seq + q, st = it % NST;
+            bounded_wait(&bb->full[st], (it / NST) & 1, a.err);
+            tc_fence_after();
+            const uint32_t as = ring + static_cast<uint32_t>(st) * a.stage_bytes;
+            const uint32_t wt = smem_addr(sW + q * FD * 32);
+            const uint32_t dp = tmem + 64u * (q & 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_tf32(dp, umma_desc_sw128(as + 32u * ks), umma_desc_sw128(wt + 32u * ks), idesc64,
+                        (q >= 2 || ks > 0) ? 1u : 0u);
+            umma_commit(&bb->maindone[(c + q) & 1]);
+          }
+          if (q > 0) {
+            const int qp = q - 1, cp = c + qp, it = seq + qp, st = it % NST;
+            bounded_wait(&bb->loready[cp & 1], (cp >> 1) & 1, a.err);
+            TRACE_AT(2, 400 + qp);
+            tc_fence_after();
+            const uint32_t as = ring + static_cast<uint32_t>(st) * a.stage_bytes;
+            const uint32_t wt = smem_addr(sW + qp * FD * 32);
+            const uint32_t dp = tmem + 64u * (qp & 1) + TD;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_tf32(dp, umma_desc_sw128(as + 32u * ks), umma_desc_sw128(wt + 32u * ks), idesc32, 1u);
+            umma_commit(&bb->empty[st]);
+          }
+        }
+        c += NC;
+        seq += NC + NSI + NRI;
+        umma_commit(&bb->accfull);
+        TRACE_AT(2, 500);
+        // d_h of rows [0, 64), then per 16 rows the dW MMAs; rows [64, 128)
+        // once the first half has been read back
+        bounded_wait(&bb->bready, t & 1, a.err);
+        TRACE_AT(2, 600);
+        tc_fence_after();
+        issue_dh(0);
+        umma_commit(&bb->dhready[0]);
+        for (int k = 0; k < NRI; ++k, ++ri) {
+          if (k == 4) {
+            bounded_wait(&bb->dhfree[0], t & 1, a.err);
+            tc_fence_after();
+            issue_dh(1);
+            umma_commit(&bb->dhready[1]);
+          }
+          bounded_wait(&bb->htready[ri & 1], (ri >> 1) & 1, a.err);
+          tc_fence_after();
+          const uint32_t bt = dt + 64u * (ri & 1);
+          for (int h = 0; 128 * h < SH2; ++h) {
+            const uint32_t araw = tmem + kColHT + 64u * (ri & 1) + 32u * h, alo = araw + 16u;
+            const uint32_t dw = tmem + kColDW + 64u * h;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              const uint64_t bd = umma_desc_sw128(bt + 32u * ks);
+              umma_tf32_ta(dw, araw + 8u * ks, bd, idesc64, (dw_first && ks == 0) ? 0u : 1u);
+              umma_tf32_ta(dw + TD, alo + 8u * ks, bd, idesc32, 1u);
+            }
+          }
+          dw_first = false;
+          umma_commit(&bb->htfree[ri & 1]);
+        }
+        if (NRI <= 4) {
+          bounded_wait(&bb->dhfree[0], t & 1, a.err);
+          tc_fence_after();
+          issue_dh(1);
+          umma_commit(&bb->dhready[1]);
+        }
         TRACE_AT(2, 601);
       }
+      umma_commit(&bb->dwdone);
     }
   } else {
     // ------------------------------------------------------------- compute
-    const int row = 32 * (warp & 3) + lane, half = warp >> 2;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    const int sd_jo = tid & 3, sd_dq = (tid >> 2) & 3, sd_s = tid >> 4;  // D = 16: 4 state groups
-    // weight-gradient ownership: dW_A|dW_B 4 rows x 8 columns, dW_C, dW_O 4 x 4
-    const int pjq_ab = tid >> 2, pkq = tid & 3;
-    const bool own_ab = pjq_ab < SH2 / 4;
-    const int pjq_c = tid >> 2, pdq = tid & 3;
-    const bool own_c = pjq_c < SH2 / 4;
-    float accAB[4][8], accC[4][4], accO[4][4];
+    const int qd = warp & 3, sub = warp >> 2;
+    const int row = 32 * qd + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    // C / d_ctx partial dots: thread = (role, sample half, state, column quad);
+    // role 0 sums h_s2 . W_C, role 1 dY . W_O^T, for 8 samples at once
+    const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_sh = (tid >> 7) & 1, sd_role = tid >> 8;
+    const int sd_s0 = 8 * sd_sh;
+    const int sd_ns = min(8, S_max - sd_s0);
+    // dW_C / dW_O: row j of SH2, states 8 dh .. 8 dh + 7
+    const int cj = tid >> 1, cdh = tid & 1;
+    const bool own_c = cj < SH2;
+    float accC[8], accO[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) accAB[i][e] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) accC[i][e] = accO[i][e] = 0.f;
-    }
-    int seq = 0, c = 0;
+    for (int e = 0; e < 8; ++e) accC[e] = accO[e] = 0.f;
+    int seq = 0, c = 0, ri = 0;
     for (int t = 0; t < T; ++t) {
       const long long tb0 = tile_start(t);
       const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
       const int R_t = S_t * K;
       const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
-      const bool sd_active = sd_s < S_t;
-      float cacc[4] = {0.f, 0.f, 0.f, 0.f}, dacc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sacc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sacc[i] = 0.f;
       // ====================================================== pass 1 chunks
       for (int q = 0; q < NC; ++q, ++seq, ++c) {
         const int st = seq % NST;
         if (tid == 0) TRACE_AT(0, 10);
         bounded_wait(&bb->full[st], (seq / NST) & 1, a.err);
         if (tid == 0) TRACE_AT(0, 11);
-        const float* Hc = reinterpret_cast<const float*>(base + static_cast<size_t>(st) * a.stage_bytes);
+        float* Hc = reinterpret_cast<float*>(base + static_cast<size_t>(st) * a.stage_bytes);
         const float* Sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_S);
         const float* Gc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_G);
-        if (c >= 2) bounded_wait(&bb->afree[c & 1], ((c - 2) >> 1) & 1, a.err);
-        float hi[16], lo[16];
+        {
+          const int jb = q * kChunk + 4 * sd_jq;
+          const float4 w = sd_role == 0 ? lds4(sW_Ct + sd_d * SH2 + jb)
+                                        : __ldg(reinterpret_cast<const float4*>(a.W_O + sd_d * SH2 + jb));
+          const float* box = sd_role == 0 ? Sc : Gc;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = lds4(Hc + row * 32 + ((((4 * half + i) ^ (row & 7))) << 2));
-          const float vv[4] = {v.x, v.y, v.z, v.w};
+          for (int i = 0; i < 8; ++i)
+            if (i < sd_ns) {
+              const int s = sd_s0 + i;
+              const float4 v = lds4(box + s * 32 + ((sd_jq ^ (s & 7)) << 2));
+              float x = sacc[i];
+              x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
+              sacc[i] = x;
+            }
+        }
+        // the MMA warp has read the chunk as h: replace it by h - trunc(h)
+        bounded_wait(&bb->maindone[c & 1], (c >> 1) & 1, a.err);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            hi[4 * i + e] = tf32_rna(vv[e]);
-            lo[4 * i + e] = vv[e] - hi[4 * i + e];
+        for (int v = 0; v < 2; ++v) {
+          const int i4 = tid + v * kComputeThreads;  // float4 index, 8 per 128-byte row
+          if ((i4 >> 3) < hc_rows) {
+            const float4 x = lds4(Hc + 4 * i4);
+            sts4(Hc + 4 * i4, make_float4(tf32_rn(x.x - tf32_trunc(x.x)), tf32_rn(x.y - tf32_trunc(x.y)),
+                                          tf32_rn(x.z - tf32_trunc(x.z)), tf32_rn(x.w - tf32_trunc(x.w))));
           }
         }
-        const uint32_t ta = lane_base + kAcolA + 64u * (c & 1) + 16u * half;
-        tmem_st16(ta, hi);
-        tmem_st16(ta + 32u, lo);
-        if (sd_active) {  // C and d_ctx partial dot products, 8 columns of this chunk
-          const int s = sd_s, ch0 = 2 * sd_jo;
-          const float4 h0 = lds4(Sc + s * 32 + ((ch0 ^ (s & 7)) << 2));
-          const float4 h1 = lds4(Sc + s * 32 + (((ch0 + 1) ^ (s & 7)) << 2));
-          const float4 g0 = lds4(Gc + s * 32 + ((ch0 ^ (s & 7)) << 2));
-          const float4 g1 = lds4(Gc + s * 32 + (((ch0 + 1) ^ (s & 7)) << 2));
-          const int jb = q * kChunk + 8 * sd_jo;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float* wc = sW_Ct + (4 * sd_dq + i) * SH2 + jb;
-            const float* wo = sW_O + (4 * sd_dq + i) * SH2 + jb;
-            const float4 c0 = lds4(wc), c1 = lds4(wc + 4), o0 = lds4(wo), o1 = lds4(wo + 4);
-            float x = cacc[i], y = dacc[i];
-            x = fmaf(h0.x, c0.x, x); x = fmaf(h0.y, c0.y, x); x = fmaf(h0.z, c0.z, x); x = fmaf(h0.w, c0.w, x);
-            x = fmaf(h1.x, c1.x, x); x = fmaf(h1.y, c1.y, x); x = fmaf(h1.z, c1.z, x); x = fmaf(h1.w, c1.w, x);
-            y = fmaf(g0.x, o0.x, y); y = fmaf(g0.y, o0.y, y); y = fmaf(g0.z, o0.z, y); y = fmaf(g0.w, o0.w, y);
-            y = fmaf(g1.x, o1.x, y); y = fmaf(g1.y, o1.y, y); y = fmaf(g1.z, o1.z, y); y = fmaf(g1.w, o1.w, y);
-            cacc[i] = x;
-            dacc[i] = y;
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bb->aready[c & 1]);
-          mbar_arrive(&bb->empty[st]);
-        }
+        if (lane == 0) mbar_arrive(&bb->loready[c & 1]);
         if (tid == 0) TRACE_AT(0, 13);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        cacc[i] += __shfl_xor_sync(0xffffffffu, cacc[i], 1);
-        cacc[i] += __shfl_xor_sync(0xffffffffu, cacc[i], 2);
-        dacc[i] += __shfl_xor_sync(0xffffffffu, dacc[i], 1);
-        dacc[i] += __shfl_xor_sync(0xffffffffu, dacc[i], 2);
-      }
-      if (sd_active && sd_jo == 0) {
+      for (int i = 0; i < 8; ++i) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          sC[sd_s * D + 4 * sd_dq + i] = cacc[i];
-          sDctx[sd_s * D + 4 * sd_dq + i] = a.tw * dacc[i];
-        }
+        for (int m = 1; m < 8; m <<= 1) sacc[i] += __shfl_xor_sync(0xffffffffu, sacc[i], m);
+      }
+      if (sd_jq == 0) {
+        float* dst = sd_role == 0 ? sC : sDctx;
+        const float scale = sd_role == 0 ? 1.f : a.tw;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (sd_s0 + i < S_t) dst[(sd_s0 + i) * D + sd_d] = scale * sacc[i];
       }
       // ==================================== projections: TMEM -> shared memory
       if (tid == 0) TRACE_AT(0, 20);
@@ -363,69 +455,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       if (tid == 0) TRACE_AT(0, 21);
       tc_fence_after();
       {
-        const int c0 = half * D;  // warps 0-3: A columns, 4-7: B columns
-        float v[D];
+        const int c0 = 8 * sub;  // columns c0 .. c0 + 7 of A|B
+        float v[8];
 #pragma unroll
-        for (int i = 0; i < D; ++i) v[i] = 0.f;
-        for (int p = 0; 2 * p < NC; ++p) {
-          uint32_t r0[D], r1[D];
-          tmem_ld16_nowait(lane_base + p * FD + c0, r0);
-          tmem_ld16_nowait(lane_base + p * FD + TD + c0, r1);
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        for (int p = 0; p < NP; ++p) {
+          uint32_t r0[8], r1[8];
+          tmem_ld8_nowait(lane_base + 64u * p + c0, r0);
+          tmem_ld8_nowait(lane_base + 64u * p + TD + c0, r1);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < D; ++i) v[i] += __uint_as_float(r0[i]);
-#pragma unroll
-          for (int i = 0; i < D; ++i) v[i] += __uint_as_float(r1[i]);
+          for (int i = 0; i < 8; ++i) v[i] += __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
         }
-#pragma unroll
-        for (int i = 0; i < D; i += 4)
-          sts4(sPh + sw128_idx(row, c0 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        sts4(sPh + sw128_idx(row, c0), make_float4(v[0], v[1], v[2], v[3]));
+        sts4(sPh + sw128_idx(row, c0 + 4), make_float4(v[4], v[5], v[6], v[7]));
       }
       tc_fence_before();
       named_sync(1, kComputeThreads);
       if (tid == 0) TRACE_AT(0, 22);
       // ================================ scan and reverse scan per (sample, state)
       if (tid < S_t * D) {
-        const int s = tid >> 4, d = tid & 15;
+        const int s = tid >> 4, d = tid & 15, rb = s * K;
         float x = 0.f;
-        for (int k = 0; k < K; ++k) {  // replay: A stays, B_t is replaced by x_t
-          const int r = s * K + k;
-          float* pb = sPh + sw128_idx(r, D + d);
-          x = fmaf(sigmoidf_(sPh[sw128_idx(r, d)]), x, *pb);
-          *pb = x;
+        for (int k0 = 0; k0 < K; k0 += 8) {  // replay: B_t is replaced by x_t
+          const int n = min(8, K - k0);
+          float av[8], bv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < n) {
+              av[u] = sPh[sw128_idx(rb + k0 + u, d)];
+              bv[u] = sPh[sw128_idx(rb + k0 + u, D + d)];
+            }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < n) av[u] = sigmoid_fast(av[u]);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < n) {
+              x = fmaf(av[u], x, bv[u]);
+              sPh[sw128_idx(rb + k0 + u, D + d)] = x;
+            }
         }
         const float Cv = sC[s * D + d], dctx = sDctx[s * D + d];
         sCtx[s * D + d] = Cv * x;
         sDC[s * D + d] = dctx * x;
         float dx = dctx * Cv;
-        for (int k = K - 1; k >= 0; --k) {
-          const int r = s * K + k;
-          float* pa = sPh + sw128_idx(r, d);
-          float* pb = sPh + sw128_idx(r, D + d);
-          const float at = *pa;
-          const float sg = sigmoidf_(at);
-          const float dsg = sg * sigmoidf_(-at);
-          const float xprev = k > 0 ? sPh[sw128_idx(r - 1, D + d)] : 0.f;
-          *pb = dx;                   // dB
-          *pa = dx * xprev * dsg;     // dA
-          dx *= sg;
+        for (int k1 = K; k1 > 0; k1 -= 8) {
+          const int k0 = k1 > 8 ? k1 - 8 : 0, n = k1 - k0;
+          float av[8], xp[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < n) {
+              const int r = rb + k0 + u;
+              av[u] = sPh[sw128_idx(r, d)];
+              xp[u] = (k0 + u > 0) ? sPh[sw128_idx(r - 1, D + d)] : 0.f;
+            }
+#pragma unroll
+          for (int u = 7; u >= 0; --u)
+            if (u < n) {
+              const int r = rb + k0 + u;
+              float sg, dsg;
+              sigmoid_and_slope(av[u], sg, dsg);
+              const float dB = dx, dA = dx * xp[u] * dsg;
+              dx *= sg;
+              const float ah = tf32_rn(dA), bh = tf32_rn(dB);
+              const float al = dA - ah, bl = dB - bh;
+              sPh[sw128_idx(r, d)] = ah;
+              sPh[sw128_idx(r, D + d)] = bh;
+              sPl[sw128_idx(r, d)] = al;
+              sPl[sw128_idx(r, D + d)] = bl;
+            }
         }
-      }
-      named_sync(1, kComputeThreads);
-      if (tid == 0) TRACE_AT(0, 23);
-      // dA|dB = hi + lo: hi stays in sPh, the exact remainder goes to sPl
-      for (int i = 4 * tid; i < kTileRows * 32; i += 4 * kComputeThreads) {
-        const float4 v = lds4(sPh + i);
-        const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
-        sts4(sPh + i, h);
-        sts4(sPl + i, make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w));
       }
       fence_proxy_async_smem();
       named_sync(1, kComputeThreads);
       if (tid == 0) mbar_arrive(&bb->bready);
       if (tid == 0) TRACE_AT(0, 24);
       // ===================== per sample: dW_C, dW_O partial sums and d_h_s2
-      const int njq = SH2 / 4;
       for (int k = 0; k < NSI; ++k, ++seq) {
         const int st = seq % NST;
         bounded_wait(&bb->full[st], (seq / NST) & 1, a.err);
@@ -435,140 +541,142 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         const int s0 = k * kBwdSampleItem, ns = min(kBwdSampleItem, S_t - s0);
         if (own_c) {
           for (int s = 0; s < ns; ++s) {
-            const float4 hv = lds4(hsb + s * SH2 + 4 * pjq_c);
-            const float4 gv = lds4(gb + s * SH2 + 4 * pjq_c);
-            const float4 dc = lds4(sDC + (s0 + s) * D + 4 * pdq);
-            const float4 cx = lds4(sCtx + (s0 + s) * D + 4 * pdq);
-            const float hvv[4] = {hv.x, hv.y, hv.z, hv.w}, gvv[4] = {gv.x, gv.y, gv.z, gv.w};
-            const float dcv[4] = {dc.x, dc.y, dc.z, dc.w}, cxv[4] = {cx.x, cx.y, cx.z, cx.w};
+            const float hv = hsb[s * SH2 + cj], gv = gb[s * SH2 + cj];
+            const float4 dc0 = lds4(sDC + (s0 + s) * D + 8 * cdh), dc1 = lds4(sDC + (s0 + s) * D + 8 * cdh + 4);
+            const float4 cx0 = lds4(sCtx + (s0 + s) * D + 8 * cdh), cx1 = lds4(sCtx + (s0 + s) * D + 8 * cdh + 4);
+            const float dcv[8] = {dc0.x, dc0.y, dc0.z, dc0.w, dc1.x, dc1.y, dc1.z, dc1.w};
+            const float cxv[8] = {cx0.x, cx0.y, cx0.z, cx0.w, cx1.x, cx1.y, cx1.z, cx1.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                accC[i][e] = fmaf(hvv[i], dcv[e], accC[i][e]);
-                accO[i][e] = fmaf(gvv[i], cxv[e], accO[i][e]);
-              }
+            for (int e = 0; e < 8; ++e) {
+              accC[e] = fmaf(hv, dcv[e], accC[e]);
+              accO[e] = fmaf(gv, cxv[e], accO[e]);
+            }
           }
         }
         named_sync(1, kComputeThreads);  // h_s2 rows no longer needed: d_h_s2 goes there
-        const int nit = ((ns + 3) / 4) * njq;
-        for (int it = tid; it < nit; it += kComputeThreads) {
-          const int jq = it % njq, sq = it / njq;
-          float o[4][4];
-          int sidx[4];
-#pragma unroll
-          for (int si = 0; si < 4; ++si) {
-            sidx[si] = min(4 * sq + si, ns - 1);
-            const float4 gv = lds4(gb + sidx[si] * SH2 + 4 * jq);
-            o[si][0] = gv.x; o[si][1] = gv.y; o[si][2] = gv.z; o[si][3] = gv.w;
-          }
+        {
+          const int jq = tid & 63, s = tid >> 6;
+          if (s < ns && 4 * jq < SH2) {
+            float4 o = lds4(gb + s * SH2 + 4 * jq);
+            const float* dcr = sDC + (s0 + s) * D;
 #pragma unroll 4
-          for (int d = 0; d < D; ++d) {
-            const float4 w = lds4(sW_Ct + d * SH2 + 4 * jq);
-#pragma unroll
-            for (int si = 0; si < 4; ++si) {
-              const float dcv = sDC[(s0 + sidx[si]) * D + d];
-              o[si][0] = fmaf(dcv, w.x, o[si][0]);
-              o[si][1] = fmaf(dcv, w.y, o[si][1]);
-              o[si][2] = fmaf(dcv, w.z, o[si][2]);
-              o[si][3] = fmaf(dcv, w.w, o[si][3]);
+            for (int d = 0; d < D; ++d) {
+              const float4 w = lds4(sW_Ct + d * SH2 + 4 * jq);
+              const float dcv = dcr[d];
+              o.x = fmaf(dcv, w.x, o.x);
+              o.y = fmaf(dcv, w.y, o.y);
+              o.z = fmaf(dcv, w.z, o.z);
+              o.w = fmaf(dcv, w.w, o.w);
             }
-          }
-#pragma unroll
-          for (int si = 0; si < 4; ++si) {
-            const int s = 4 * sq + si;
-            if (s < ns) sts4(hsb + s * SH2 + 4 * jq, make_float4(o[si][0], o[si][1], o[si][2], o[si][3]));
+            sts4(hsb + s * SH2 + 4 * jq, o);
           }
         }
         fence_proxy_async_smem();
         named_sync(1, kComputeThreads);
         if (tid == 0) {
-          bulk_store(a.out1 + (tb0 + s0) * SH2, hsb, static_cast<uint32_t>(ns) * SH2 * 4u);
-          bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(&bb->empty[st], kComputeWarps);
+          mbar_arrive(&bb->empty[st]);  // the producer stores d_h_s2 from the stage
           TRACE_AT(0, 33);
         }
       }
-      // ================================= per 16 rows: dW_A|dW_B partial sums
-      for (int k = 0; k < NRI; ++k, ++seq) {
-        const int st = seq % NST;
-        bounded_wait(&bb->full[st], (seq / NST) & 1, a.err);
-        if (tid == 0) TRACE_AT(0, 41);
-        const float* hb = reinterpret_cast<const float*>(base + static_cast<size_t>(st) * a.stage_bytes);
-        const int r0 = k * kRowItem, nr = min(kRowItem, R_t - r0);
-        if (own_ab) {
-          const float* hrow = hb + 4 * pjq_ab;
-#pragma unroll 2
-          for (int r = 0; r < nr; ++r) {
-            const int rr = r0 + r;
-            const float4 hv = lds4(hrow + r * SH2);
-            const float4 p0 = lds4(sPh + sw128_idx(rr, 8 * pkq)), p1 = lds4(sPh + sw128_idx(rr, 8 * pkq + 4));
-            const float4 q0 = lds4(sPl + sw128_idx(rr, 8 * pkq)), q1 = lds4(sPl + sw128_idx(rr, 8 * pkq + 4));
-            const float hvv[4] = {hv.x, hv.y, hv.z, hv.w};
-            const float pv[8] = {p0.x + q0.x, p0.y + q0.y, p0.z + q0.z, p0.w + q0.w,
-                                 p1.x + q1.x, p1.y + q1.y, p1.z + q1.z, p1.w + q1.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) accAB[i][e] = fmaf(hvv[i], pv[e], accAB[i][e]);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bb->empty[st]);
-        if (tid == 0) TRACE_AT(0, 42);
-      }
-      // ========================= d_h_history from TMEM: thread = column j
-      bounded_wait(&bb->bdone, t & 1, a.err);
-      if (tid == 0) TRACE_AT(0, 45);
-      tc_fence_after();
+      // ========== per 16 rows: h^T into TMEM for dW, d_h_history rows out
       {
-        const int j = 128 * half + 32 * (warp & 3) + lane;
-        float* dst = a.out0 + tb0 * K * SH2 + j;
-        for (int cb = 0; cb * 32 < R_t; ++cb) {
-          float v[32];
-          tmem_ld<16>(lane_base + 128u * half + 32u * cb, v);
-          tmem_ld<16>(lane_base + 128u * half + 32u * cb + 16u, v + 16);
-          if (j < SH2) {
-            const int nrow = R_t - 32 * cb;
-            float* d0 = dst + static_cast<long long>(32 * cb) * SH2;
+        const int h = sub & 1, rg = sub >> 1;
+        const int j = 128 * h + 32 * qd + lane;
+        const bool jok = j < SH2;
+        for (int k = 0; k < NRI; ++k, ++seq, ++ri) {
+          const int st = seq % NST;
+          bounded_wait(&bb->full[st], (seq / NST) & 1, a.err);
+          if (tid == 0) TRACE_AT(0, 41);
+          float* hb = reinterpret_cast<float*>(base + static_cast<size_t>(st) * a.stage_bytes);
+          const int r0 = k * kRowItem, nr = min(kRowItem, R_t - r0);
+          if (ri >= 2) bounded_wait(&bb->htfree[ri & 1], ((ri - 2) >> 1) & 1, a.err);
+          tc_fence_after();
+          {
+            float raw[8], lo[8];
 #pragma unroll
-            for (int r = 0; r < 32; ++r)
-              if (r < nrow) d0[static_cast<long long>(r) * SH2] = v[r];
+            for (int i = 0; i < 8; ++i) {
+              const int r = 8 * rg + i;
+              const float x = (r < nr && jok) ? hb[r * SH2 + j] : 0.f;
+              raw[i] = x;
+              lo[i] = tf32_rn(x - tf32_trunc(x));
+            }
+            const uint32_t tb = lane_base + kColHT + 64u * (ri & 1) + 32u * h + 8u * rg;
+            tmem_st8(tb, raw);
+            tmem_st8(tb + 16u, lo);
+          }
+          {  // dA|dB of these rows, transposed: [hi 32 | lo 32] x 16 rows; zero past the tile
+            const int m = tid >> 3, rr = 2 * (tid & 7);
+            const float* src = m < TD ? sPh : sPl;
+            const int col = m & (TD - 1);
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              const int r = rr + v;
+              sDT[sw128_idx(m, 16 * (ri & 1) + r)] = r < nr ? src[sw128_idx(r0 + r, col)] : 0.f;
+            }
+          }
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bb->htready[ri & 1]);
+          const int rh = k >> 2;
+          if ((k & 3) == 0) {
+            if (tid == 0) TRACE_AT(0, 44);
+            bounded_wait(&bb->dhready[rh], t & 1, a.err);
+            if (tid == 0) TRACE_AT(0, 45);
+          }
+          tc_fence_after();
+          named_sync(1, kComputeThreads);  // every read of the h rows done
+          {
+            float v[8];
+            tmem_ld<8>(lane_base + 64u * h + 16u * (k & 3) + 8u * rg, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 8 * rg + i;
+              if (r < nr && jok) hb[r * SH2 + j] = v[i];
+            }
+          }
+          const bool last_of_half = (k & 3) == 3 || k == NRI - 1;
+          tc_fence_before();
+          fence_proxy_async_smem();
+          named_sync(1, kComputeThreads);
+          if (tid == 0) {
+            if (last_of_half) mbar_arrive(&bb->dhfree[rh]);
+            mbar_arrive(&bb->empty[st]);  // the producer stores the d_h rows from the stage
+            TRACE_AT(0, 42);
           }
         }
+        if (NRI <= 4 && tid == 0) mbar_arrive(&bb->dhfree[1]);
       }
-      tc_fence_before();
-      named_sync(1, kComputeThreads);
-      if (tid == 0) mbar_arrive(&bb->dhfree);
       if (tid == 0) TRACE_AT(0, 46);
     }
     // ===================================== partial sums into the CTA's slot
     float* slot = a.ws + static_cast<size_t>(cta) * 4 * SH2 * D;
     const int n = SH2 * D;
-    if (own_ab) {
+    bounded_wait(&bb->dwdone, 0, a.err);
+    tc_fence_after();
+    {
+      const int h = sub & 1, cp = sub >> 1;  // cp 0: dW_A row, 1: dW_B row
+      const int j = 128 * h + 32 * qd + lane;
+      float m[16], r[16];
+      tmem_ld<16>(lane_base + kColDW + 64u * h + 16u * cp, m);
+      tmem_ld<16>(lane_base + kColDW + 64u * h + TD + 16u * cp, r);
+      if (j < SH2) {
+        float4* dst = reinterpret_cast<float4*>(slot + cp * n + j * D);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = 4 * pjq_ab + i, col = 8 * pkq + e;
-          if (col < D)
-            slot[j * D + col] = accAB[i][e];
-          else
-            slot[n + j * D + (col - D)] = accAB[i][e];
-        }
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_float4(m[4 * i] + r[4 * i], m[4 * i + 1] + r[4 * i + 1], m[4 * i + 2] + r[4 * i + 2],
+                               m[4 * i + 3] + r[4 * i + 3]);
+      }
     }
     if (own_c) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * pjq_c + i, d = 4 * pdq + e;
-          slot[2 * n + j * D + d] = accC[i][e];
-          slot[3 * n + d * SH2 + j] = a.tw * accO[i][e];
-        }
+      for (int e = 0; e < 8; ++e) {
+        const int d = 8 * cdh + e;
+        slot[2 * n + cj * D + d] = accC[e];
+        slot[3 * n + d * SH2 + cj] = a.tw * accO[e];
+      }
     }
-    if (tid == 0) bulk_wait_all();
     if (tid == 0) TRACE_AT(0, 50);
   }
   tc_fence_before();
@@ -583,33 +691,33 @@ int round_up_b(int x, int m) { return (x + m - 1) / m * m; }
 bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a) {
   if (!fast_path_ok(K, SH2, D) || D != 16) return false;
   int S_max = kTileRows / K;
-  if (S_max > 32) S_max = 32;
-  if (S_max > kComputeThreads / D) S_max = kComputeThreads / D;
+  if (S_max > kComputeWarps) S_max = kComputeWarps;  // one warp per sample in the dots
   const int hc = S_max * K * 128, sc = S_max * 128;
   const int off_S = round_up_b(hc, 1024);
   const int off_G = off_S + round_up_b(sc, 1024);
   int stage = off_G + sc;
   if (2 * kBwdSampleItem * SH2 * 4 > stage) stage = 2 * kBwdSampleItem * SH2 * 4;
   if (kRowItem * SH2 * 4 > stage) stage = kRowItem * SH2 * 4;
+  // the projection MMAs read 128 rows of 128 bytes from the start of a stage
   if (kTileRows * 128 > stage) stage = kTileRows * 128;
   stage = round_up_b(stage, 1024);
   const int wbytes = SH2 * 4 * D * 4;
-  const int rest = wbytes + 2 * D * SH2 * 4 + 2 * kTileRows * 128 + 4 * S_max * D * 4 +
-                   static_cast<int>(sizeof(BwdBars)) + 1024 + 64;
+  const int rest = wbytes + 2 * kTileRows * 128 + 64 * 32 * 4 + D * SH2 * 4 +
+                   4 * S_max * D * 4 + static_cast<int>(sizeof(BwdBars)) + 16 + 1024;
   int n_stages = kMaxStages;
   while (n_stages > 2 && n_stages * stage + rest > 227 * 1024) --n_stages;
   int off = n_stages * stage;
-  a->off_wt = off;  off += wbytes;
-  a->off_p = off;   off += kTileRows * 128;
-  a->off_hlo = off; off += kTileRows * 128;
-  a->off_wct = off; off += D * SH2 * 4;
-  a->off_wo = off;  off += D * SH2 * 4;
-  a->off_cs = off;  off += S_max * D * 4;
-  a->off_ctx = off; off += S_max * D * 4;
+  a->off_wt = off;   off += wbytes;
+  a->off_p = off;    off += kTileRows * 128;
+  a->off_hlo = off;  off += kTileRows * 128;
+  a->off_wab = off;  off += 64 * 32 * 4;
+  a->off_wct = off;  off += D * SH2 * 4;
+  a->off_cs = off;   off += S_max * D * 4;
+  a->off_ctx = off;  off += S_max * D * 4;
   a->off_dctx = off; off += S_max * D * 4;
-  a->off_dc = off;  off += S_max * D * 4;
+  a->off_dc = off;   off += S_max * D * 4;
   off = round_up_b(off, 16);
-  a->off_bar = off; off += static_cast<int>(sizeof(BwdBars));
+  a->off_bar = off;  off += static_cast<int>(sizeof(BwdBars));
   a->smem_bytes = off + 1024;
   a->S_max = S_max;
   a->SG = kBwdSampleItem;

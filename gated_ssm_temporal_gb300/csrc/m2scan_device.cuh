@@ -69,20 +69,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Same test, but a thread whose phase is not complete is suspended until it
+// completes or about `hint_ns` nanoseconds have passed, instead of returning
+// at once: a waiting warp then takes no issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Waits until the barrier phase with the given parity has completed. Gives up
 // after kWaitLimitNs, sets kErrWaitTimeout in *err and returns false; the
-// caller then carries on (its results are garbage but the kernel ends).
+// caller then carries on (its results are garbage but the kernel ends). Once
+// any wait of any kernel has given up (the bit is set), every later wait that
+// has to spin gives up at its next check instead of waiting out its own
+// limit, so a broken hand-off ends the kernel in about one limit.
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((i & 15u) == 0u) {
+      if ((*reinterpret_cast<volatile unsigned*>(err) & kErrWaitTimeout) != 0u) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         atomicOr(err, kErrWaitTimeout);
         return false;
       }
-      __nanosleep(32);
     }
   }
 }
@@ -147,6 +165,24 @@ __device__ __forceinline__ void sts4(float* p, float4 v) {
 }
 
 __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
+
+// sigmoid(a) from e = exp(-|a|) and r = 1 / (1 + e): sigmoid(|a|) = r and
+// sigmoid(-|a|) = e r, so neither side cancels. Uses the fast exponential and
+// division intrinsics (a few ulp; the layer's results are checked to 1e-4).
+__device__ __forceinline__ float sigmoid_fast(float a) {
+  const float e = __expf(-fabsf(a));
+  const float r = __fdividef(1.0f, 1.0f + e);
+  return a >= 0.f ? r : e * r;
+}
+
+// sigmoid(a) and its slope sigmoid(a) sigmoid(-a) = e r^2 from one exponential.
+__device__ __forceinline__ void sigmoid_and_slope(float a, float& sg, float& slope) {
+  const float e = __expf(-fabsf(a));
+  const float r = __fdividef(1.0f, 1.0f + e);
+  const float er = e * r;
+  sg = a >= 0.f ? r : er;
+  slope = er * r;
+}
 
 // ---------------------------------------------------------------- tcgen05
 // Tensor-core MMA with the accumulator in tensor memory (TMEM), operands in
@@ -229,6 +265,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
       "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+// Whole warp: lane l writes 8 consecutive columns of TMEM lane (taddr.lane + l).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
       : "memory");
 }
 

@@ -157,9 +157,11 @@ int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
 
 /*
  * Device-side error flags of the current device (bit 0: a kernel gave up
- * waiting on a shared-memory barrier after its iteration limit). Reading is
- * SYNCHRONOUS (it waits for the device) and clears the flags. Returns
- * M2SCAN_OK and stores the flags in *flags.
+ * waiting on a shared-memory barrier after its time limit). While bit 0 is
+ * set, kernels that would have to wait give up at once, so every result
+ * computed after the first failure is garbage until the flags are read.
+ * Reading is SYNCHRONOUS (it waits for the device) and clears the flags.
+ * Returns M2SCAN_OK and stores the flags in *flags.
  */
 m2scan_status m2scan_read_device_flags(uint32_t* flags);
 
