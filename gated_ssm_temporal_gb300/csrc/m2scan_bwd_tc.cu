@@ -8,9 +8,11 @@
 //            d_h_enriched (TMA boxes, 128-byte swizzle). The MMA warp
 //            recomputes A|B = h . [W_A|W_B] with the chunk as the A operand
 //            straight from shared memory (the tensor core reads the top 19 bits
-//            of each fp32, i.e. trunc(h)); the compute warps then overwrite the
-//            chunk with h - trunc(h) (rounded to tf32) and the MMA warp adds
-//            that remainder's product. The compute warps also form
+//            of each fp32, i.e. trunc(h)); meanwhile the compute warps write
+//            h - trunc(h) (rounded to tf32) into tensor memory and the MMA warp
+//            adds that remainder's product. A stage is free as soon as its
+//            main MMAs are done and the compute warps have read it. The
+//            compute warps also form
 //            C = h_s2 . W_C and d_ctx = tw dY . W_O^T on the FMA pipe.
 //   scan     replay of the forward scan and the reverse scan of the
 //            implementation plan's Task 2 ("Custom Kernel Optimization
@@ -45,12 +47,18 @@ constexpr int kProducerWarp = kComputeWarps;
 constexpr int kMmaWarp = kComputeWarps + 1;
 constexpr int kRowItem = 16;       // h_history rows per dW item
 constexpr int kBwdSampleItem = 8;  // samples per dW_C/dW_O/d_h_s2 item
+constexpr int kChunkRing = 6;      // chunk hand-off barriers (>= the copy ring's depth)
+// A chunk stage is free once its main MMAs are done (commit) and the compute
+// warps have read it (the MMA warp arrives when it sees loready); other stages
+// are released by the compute warps with both arrivals at once.
+constexpr uint32_t kEmptyArrivals = 2;
+constexpr int kLoBufs = 3;  // TMEM buffers of h - trunc(h) for the projections
 
 struct BwdBars {
-  uint64_t full[kMaxStages];   // producer -> all: stage loaded
-  uint64_t empty[kMaxStages];  // stage free (MMA commit for chunks, compute otherwise)
-  uint64_t maindone[2];        // MMA -> compute: chunk read as h, may be overwritten
-  uint64_t loready[2];         // compute -> MMA: chunk holds h - trunc(h)
+  uint64_t full[kMaxStages];          // producer -> all: stage loaded
+  uint64_t empty[kMaxStages];         // stage free: two arrivals (see kEmptyArrivals)
+  uint64_t loready[kChunkRing];       // compute -> MMA: chunk read, h - trunc(h) in TMEM
+  uint64_t lofree[3];                 // MMA -> compute: remainder buffer consumed
   uint64_t accfull;            // MMA -> compute: projections of the tile done
   uint64_t bready;             // compute -> MMA: dA|dB operands written
   uint64_t dhready[2];         // MMA -> compute: d_h of a 64-row half done
@@ -63,17 +71,94 @@ struct BwdBars {
 };
 
 // TMEM columns (128 lanes each):
-//   [0, 128)    projection accumulators, two [main | corrections] pairs of 64;
-//               later d_h^T of one 64-row half: j-half h at 64 h (N = 64 rows)
-//   [128, 256)  transposed h rows, two buffers p of [j-half 0 | j-half 1],
-//               each 16 columns of h then 16 of h - trunc(h)
+//   [0, 128)    projection accumulators trunc(h) . [W_hi | W_lo] of the even
+//               and of the odd chunks (64 columns each); later d_h^T of one
+//               64-row half: j-half h at 64 h (N = 64 rows)
+//   [128, 224)  during the projections: three buffers of h - trunc(h) for a
+//               chunk (A operand, 32 columns each)
+//   [224, 256)  during the projections: (h - trunc h) . W_hi, a sum of its own
+//               so that no accumulation order depends on timing
+//   [128, 256)  during the row items: transposed h rows, two buffers p of
+//               [j-half 0 | j-half 1], each 16 columns of h then 16 of
+//               h - trunc(h)
 //   [256, 384)  dW_A|dW_B^T accumulators: j-half h at 256 + 64 h,
 //               [h . dAB_hi (32) | h . dAB_lo + (h - trunc h) . dAB_hi (32)]
 //   [384, 512)  [W_A|W_B] rows as the d_h A operand: j-half h at 384 + 64 h,
 //               32 columns tf32 part, 32 columns remainder
+constexpr uint32_t kColCorr = 224;
+constexpr uint32_t kColLo = 128;
 constexpr uint32_t kColHT = 128;
 constexpr uint32_t kColDW = 256;
 constexpr uint32_t kColW = 384;
+
+// Position in a ring of n barriers: index and the parity of its current use.
+struct RingPos {
+  int i = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++i == n) {
+      i = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// Order of a tile's items after its NC chunks: sample item 0, row items 0-3,
+// the other sample items, then row items 4 on. While the compute warps work
+// on a sample item the MMA warp computes the next half of d_h.
+// kind 1: sample item idx, kind 2: row item idx.
+__device__ __forceinline__ void post_item(int p, int NSI, int NRI, int& kind, int& idx) {
+  if (NSI > 0) {
+    if (p == 0) {
+      kind = 1;
+      idx = 0;
+      return;
+    }
+    --p;
+  }
+  const int r1 = NRI < 4 ? NRI : 4;
+  if (p < r1) {
+    kind = 2;
+    idx = p;
+    return;
+  }
+  p -= r1;
+  const int s1 = NSI > 0 ? NSI - 1 : 0;
+  if (p < s1) {
+    kind = 1;
+    idx = 1 + p;
+    return;
+  }
+  kind = 2;
+  idx = 4 + (p - s1);
+}
+
+// Time limit for a thread that polls several barriers: call progress() after
+// every step, idle() when nothing was ready; idle() returns true once the
+// limit has passed (or another wait already gave up) and sets the error bit.
+struct IdleClock {
+  unsigned long long t0 = 0;
+  uint32_t n = 0;
+  __device__ __forceinline__ void progress() {
+    n = 0;
+    t0 = 0;
+  }
+  __device__ __forceinline__ bool idle(unsigned* err) {
+    if ((++n & 7u) != 0u) return false;
+    const unsigned long long now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+      return false;
+    }
+    if ((*reinterpret_cast<volatile unsigned*>(err) & kErrWaitTimeout) != 0u) return true;
+    if (now - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrWaitTimeout);
+      return true;
+    }
+    __nanosleep(100);
+    return false;
+  }
+};
 
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_constant__ FastArgs a) {
   constexpr int D = 16, TD = 32, FD = 64;
@@ -95,8 +180,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   (void)trace_n;
   if (tid == 0) TRACE_AT(0, 1);
   const int K = a.K, SH2 = a.SH2, S_max = a.S_max, NST = a.n_stages;
-  const int NC = SH2 / kChunk, NP = NC < 2 ? NC : 2;
-  const int hc_rows = a.hc_bytes / 128;
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.stage_bytes);
+  const int NC = SH2 / kChunk;
   const long long B = a.B;
   const int P = gridDim.x, cta = blockIdx.x;
   const long long cb0 = B * cta / P;
@@ -108,6 +193,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   };
   auto n_sample_items = [&](int S_t) { return (S_t + kBwdSampleItem - 1) / kBwdSampleItem; };
   auto n_row_items = [&](int S_t) { return (S_t * K + kRowItem - 1) / kRowItem; };
+  auto stage_ptr = [&](int st) { return base + static_cast<uint32_t>(st) * stage_bytes; };
 
   if (tid == kProducerWarp * 32) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_h)) : "memory");
@@ -115,11 +201,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_g)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
-      mbar_init(&bb->empty[s], 1);
+      mbar_init(&bb->empty[s], kEmptyArrivals);
     }
+    for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
+    for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bb->maindone[s], 1);
-      mbar_init(&bb->loready[s], kComputeWarps);
       mbar_init(&bb->dhready[s], 1);
       mbar_init(&bb->dhfree[s], 1);
       mbar_init(&bb->htready[s], kComputeWarps);
@@ -137,32 +223,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   const uint32_t tmem = bb->tslot;
   if (tid == 0) TRACE_AT(0, 3);
 
-  // ---- producer: per tile NC chunks, then sample items, then row items.
+  // ---- producer: per tile NC chunks, then the other items (post_item order).
   // A stage that held a sample or row item holds that item's output once the
   // compute warps release it: the producer stores it before reusing the stage.
-  int pseq = 0, ptile = 0, pit = 0;
-  int rseq = 0, rtile = 0, rit = 0;  // oldest item not yet released
+  RingPos lp, rp;                  // next stage to load, oldest stage not yet released
+  int pn = 0, ptile = 0, pit = 0;  // items loaded; tile and item of the next load
+  int rn = 0, rtile = 0, rit = 0;  // items released; tile and item of the next release
   auto release_one = [&]() {
-    const int st = rseq % NST;
-    bounded_wait(&bb->empty[st], (rseq / NST) & 1, a.err);
+    bounded_wait(&bb->empty[rp.i], rp.ph, a.err);
     const long long tb0 = tile_start(rtile);
     const int S_t = static_cast<int>(tile_start(rtile + 1) - tb0);
     const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
-    const unsigned char* sp = base + static_cast<size_t>(st) * a.stage_bytes;
     if (rit >= NC) {
-      if (rit < NC + NSI) {
-        const int s0 = (rit - NC) * kBwdSampleItem;
+      const unsigned char* sp = stage_ptr(rp.i);
+      int kind, idx;
+      post_item(rit - NC, NSI, NRI, kind, idx);
+      if (kind == 1) {
+        const int s0 = idx * kBwdSampleItem;
         const int ns = min(kBwdSampleItem, S_t - s0);
         bulk_store(a.out1 + (tb0 + s0) * SH2, sp, static_cast<uint32_t>(ns) * SH2 * 4u);
       } else {
-        const int r0 = (rit - NC - NSI) * kRowItem;
+        const int r0 = idx * kRowItem;
         const int nr = min(kRowItem, S_t * K - r0);
         bulk_store(a.out0 + (tb0 * K + r0) * SH2, sp, static_cast<uint32_t>(nr) * SH2 * 4u);
       }
       bulk_commit();
       bulk_wait_read_all();
     }
-    ++rseq;
+    rp.next(NST);
+    ++rn;
     if (++rit == NC + NSI + NRI) {
       rit = 0;
       ++rtile;
@@ -172,30 +261,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     const long long tb0 = tile_start(ptile);
     const int S_t = static_cast<int>(tile_start(ptile + 1) - tb0);
     const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
-    const int st = pseq % NST;
-    if (pseq >= NST) release_one();
-    unsigned char* sp = base + static_cast<size_t>(st) * a.stage_bytes;
-    uint64_t* bar = &bb->full[st];
-    if (pit < NC) {
+    if (pn >= NST) release_one();
+    unsigned char* sp = stage_ptr(lp.i);
+    uint64_t* bar = &bb->full[lp.i];
+    int kind = 0, idx = pit;
+    if (pit >= NC) post_item(pit - NC, NSI, NRI, kind, idx);
+    if (kind == 0) {
       mbar_arrive_expect_tx(bar, a.hc_bytes + 2 * a.sc_bytes);
       tma_load_3d(sp, &a.tm_h, pit * kChunk, 0, static_cast<int>(tb0), bar);
       tma_load_2d(sp + a.off_S, &a.tm_hs, pit * kChunk, static_cast<int>(tb0), bar);
       tma_load_2d(sp + a.off_G, &a.tm_g, pit * kChunk, static_cast<int>(tb0), bar);
-    } else if (pit < NC + NSI) {
-      const int s0 = (pit - NC) * kBwdSampleItem;
+    } else if (kind == 1) {
+      const int s0 = idx * kBwdSampleItem;
       const int ns = min(kBwdSampleItem, S_t - s0);
       const uint32_t rb = static_cast<uint32_t>(ns) * SH2 * 4u;
       mbar_arrive_expect_tx(bar, 2u * rb);
       bulk_load(sp, a.h_s2 + (tb0 + s0) * SH2, rb, bar);
       bulk_load(sp + static_cast<size_t>(kBwdSampleItem) * SH2 * 4, a.g + (tb0 + s0) * SH2, rb, bar);
     } else {
-      const int r0 = (pit - NC - NSI) * kRowItem;
+      const int r0 = idx * kRowItem;
       const int nr = min(kRowItem, S_t * K - r0);
       const uint32_t rb = static_cast<uint32_t>(nr) * SH2 * 4u;
       mbar_arrive_expect_tx(bar, rb);
       bulk_load(sp, a.h_history + (tb0 * K + r0) * SH2, rb, bar);
     }
-    ++pseq;
+    lp.next(NST);
+    ++pn;
     if (++pit == NC + NSI + NRI) {
       pit = 0;
       ++ptile;
@@ -204,9 +295,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   if (warp == kProducerWarp && lane == 0)
     for (int i = 0; i < NST && ptile < T; ++i) produce_one();
 
-  // ---- weights: projection B tiles and W_C^T into shared memory
+  // ---- weights: projection B tiles and W_C^T into shared memory, [W_A|W_B]
+  // rows into TMEM; every global load is issued before the first store
   constexpr int kWPer = (4096 + kBwdThreads - 1) / kBwdThreads;
   {
+    const int wsub = warp >> 2, wh = wsub & 1, wpart = wsub >> 1;
+    const int wj = 128 * wh + 32 * (warp & 3) + lane;
+    float4 wr[8];
+    if (warp < kComputeWarps) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float* src = (q < 4 ? a.W_A : a.W_B) + wj * D + 4 * (q & 3);
+        wr[q] = wj < SH2 ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     float wa[kWPer], wb[kWPer], wc[kWPer];
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
@@ -215,6 +317,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       wa[u] = ok ? __ldg(a.W_A + i) : 0.f;
       wb[u] = ok ? __ldg(a.W_B + i) : 0.f;
       wc[u] = ok ? __ldg(a.W_C + i) : 0.f;
+    }
+    if (warp < kComputeWarps) {
+      // thread = TMEM lane = row j of [W_A|W_B] within its j-half
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[4 * q] = wr[q].x; v[4 * q + 1] = wr[q].y; v[4 * q + 2] = wr[q].z; v[4 * q + 3] = wr[q].w;
+      }
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float hi = tf32_rn(v[k]);
+        v[k] = wpart == 0 ? hi : v[k] - hi;
+      }
+      const uint32_t tw0 = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kColW + 64u * wh + 32u * wpart;
+      tmem_st16(tw0, v);
+      tmem_st16(tw0 + 16u, v + 16);
     }
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
@@ -230,27 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       tile[sw128_idx(TD + D + d, jj)] = wb[u] - hb;
       sW_Ct[d * SH2 + j] = wc[u];
     }
-  }
-  // [W_A|W_B] rows into TMEM (thread = lane = row j within its j-half)
-  if (warp < kComputeWarps) {
-    const int sub = warp >> 2, h = sub & 1, part = sub >> 1;
-    const int j = 128 * h + 32 * (warp & 3) + lane;
-    float v[32];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float* src = (q < 4 ? a.W_A : a.W_B) + j * D + 4 * (q & 3);
-      const float4 w = j < SH2 ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
-    }
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const float hi = tf32_rn(v[k]);
-      v[k] = part == 0 ? hi : v[k] - hi;
-    }
-    const uint32_t tw0 = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kColW + 64u * h + 32u * part;
-    tmem_st16(tw0, v);
-    tmem_st16(tw0 + 16u, v + 16);
-    tmem_st_wait();
+    if (warp < kComputeWarps) tmem_st_wait();
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -265,7 +363,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         TRACE_AT(1, 100 + pit);
         produce_one();
       }
-      while (rseq < pseq) release_one();
+      while (rn < pn) release_one();
       bulk_wait_all();
     }
   } else if (warp == kMmaWarp) {
@@ -275,61 +373,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       constexpr uint32_t idesc32 = umma_idesc_tf32(128, 32);
       const uint32_t ph = smem_addr(sPh), pl = smem_addr(sPl), dt = smem_addr(sDT);
       const uint32_t ring = smem_addr(base);
+      const uint32_t w0 = smem_addr(sW);
+      // descriptor + 2 u advances its start address by 32 u bytes (one K step)
       auto issue_dh = [&](int rh) {
         // d_h^T[j, 64 rh + n] for both j-halves; cross terms first
         for (int h = 0; 128 * h < SH2; ++h) {
           const uint32_t dd = tmem + 64u * h, wh = tmem + kColW + 64u * h, wl = wh + 32u;
-          const uint32_t bh0 = ph + 8192u * rh, bl0 = pl + 8192u * rh;
+          const uint64_t bh0 = umma_desc_sw128(ph + 8192u * rh), bl0 = umma_desc_sw128(pl + 8192u * rh);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            umma_tf32_ta(dd, wh + 8u * ks, umma_desc_sw128(bl0 + 32u * ks), idesc64, ks != 0);
-            umma_tf32_ta(dd, wl + 8u * ks, umma_desc_sw128(bh0 + 32u * ks), idesc64, 1u);
+            umma_tf32_ta(dd, wh + 8u * ks, bl0 + 2u * ks, idesc64, ks != 0);
+            umma_tf32_ta(dd, wl + 8u * ks, bh0 + 2u * ks, idesc64, 1u);
           }
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_tf32_ta(dd, wh + 8u * ks, umma_desc_sw128(bh0 + 32u * ks), idesc64, 1u);
+          for (int ks = 0; ks < 4; ++ks) umma_tf32_ta(dd, wh + 8u * ks, bh0 + 2u * ks, idesc64, 1u);
         }
       };
-      int seq = 0, c = 0, ri = 0;
+      RingPos tp;  // stage of the tile's first item
+      RingPos lr;  // loready position of the next remainder
+      RingPos lf;  // lofree position of the next remainder
+      int ri = 0;
       bool dw_first = true;
       for (int t = 0; t < T; ++t) {
         const long long tb0 = tile_start(t);
         const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
         const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
         TRACE_AT(2, 290);
-        if (t > 0) bounded_wait(&bb->dhfree[1], (t - 1) & 1, a.err);
+        if (t > 0) {
+          bounded_wait(&bb->dhfree[1], (t - 1) & 1, a.err);
+          // the corrections accumulate over the previous tile's transposed rows
+          bounded_wait(&bb->htfree[(ri - 1) & 1], ((ri - 1) >> 1) & 1, a.err);
+        }
         tc_fence_after();
-        // pass 1: main products of chunk q, then the remainder products of q - 1
-        for (int q = 0; q <= NC; ++q) {
-          if (q < NC) {
-            const int it = seq + q, st = it % NST;
-            bounded_wait(&bb->full[st], (it / NST) & 1, a.err);
-            tc_fence_after();
-            const uint32_t as = ring + static_cast<uint32_t>(st) * a.stage_bytes;
-            const uint32_t wt = smem_addr(sW + q * FD * 32);
-            const uint32_t dp = tmem + 64u * (q & 1);
+        // pass 1: the remainder products of a chunk as soon as the compute
+        // warps have written it, else the main products of the next chunk that
+        // has landed (at most two chunks ahead, so that the remainders do not
+        // queue behind them); each kind in chunk order into its own accumulator
+        {
+          RingPos pm = tp, pc = tp;  // stages of the next main / remainder chunk
+          int qm = 0, qc = 0;
+          IdleClock clk;
+          while (qc < NC) {
+            bool did = false;
+            if (qc < qm && mbar_test_wait(&bb->loready[lr.i], lr.ph)) {
+              TRACE_AT(2, 400 + qc);
+              tc_fence_after();
+              mbar_arrive(&bb->empty[pc.i]);  // the compute warps are done with it
+              const uint32_t al = tmem + kColLo + 32u * lf.i;
+              const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_tf32(dp, umma_desc_sw128(as + 32u * ks), umma_desc_sw128(wt + 32u * ks), idesc64,
-                        (q >= 2 || ks > 0) ? 1u : 0u);
-            umma_commit(&bb->maindone[(c + q) & 1]);
-          }
-          if (q > 0) {
-            const int qp = q - 1, cp = c + qp, it = seq + qp, st = it % NST;
-            bounded_wait(&bb->loready[cp & 1], (cp >> 1) & 1, a.err);
-            TRACE_AT(2, 400 + qp);
-            tc_fence_after();
-            const uint32_t as = ring + static_cast<uint32_t>(st) * a.stage_bytes;
-            const uint32_t wt = smem_addr(sW + qp * FD * 32);
-            const uint32_t dp = tmem + 64u * (qp & 1) + TD;
+              for (int ks = 0; ks < 4; ++ks)
+                umma_tf32_ta(tmem + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
+              umma_commit(&bb->lofree[lf.i]);
+              lr.next(kChunkRing);
+              lf.next(kLoBufs);
+              pc.next(NST);
+              ++qc;
+              did = true;
+            }
+            if (!did && qm < NC && qm < qc + 2 && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
+              tc_fence_after();
+              const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
+              const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_tf32(dp, umma_desc_sw128(as + 32u * ks), umma_desc_sw128(wt + 32u * ks), idesc32, 1u);
-            umma_commit(&bb->empty[st]);
+              for (int ks = 0; ks < 4; ++ks)
+                umma_tf32(tmem + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
+              umma_commit(&bb->empty[pm.i]);  // first of the stage's two arrivals
+              pm.next(NST);
+              ++qm;
+              did = true;
+            }
+            if (did)
+              clk.progress();
+            else if (clk.idle(a.err))
+              break;
           }
         }
-        c += NC;
-        seq += NC + NSI + NRI;
+        for (int i = 0; i < NC + NSI + NRI; ++i) tp.next(NST);
         umma_commit(&bb->accfull);
         TRACE_AT(2, 500);
         // d_h of rows [0, 64), then per 16 rows the dW MMAs; rows [64, 128)
@@ -348,15 +468,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           }
           bounded_wait(&bb->htready[ri & 1], (ri >> 1) & 1, a.err);
           tc_fence_after();
-          const uint32_t bt = dt + 64u * (ri & 1);
+          const uint64_t bt = umma_desc_sw128(dt + 64u * (ri & 1));
           for (int h = 0; 128 * h < SH2; ++h) {
             const uint32_t araw = tmem + kColHT + 64u * (ri & 1) + 32u * h, alo = araw + 16u;
             const uint32_t dw = tmem + kColDW + 64u * h;
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
-              const uint64_t bd = umma_desc_sw128(bt + 32u * ks);
-              umma_tf32_ta(dw, araw + 8u * ks, bd, idesc64, (dw_first && ks == 0) ? 0u : 1u);
-              umma_tf32_ta(dw + TD, alo + 8u * ks, bd, idesc32, 1u);
+              umma_tf32_ta(dw, araw + 8u * ks, bt + 2u * ks, idesc64, (dw_first && ks == 0) ? 0u : 1u);
+              umma_tf32_ta(dw + TD, alo + 8u * ks, bt + 2u * ks, idesc32, 1u);
             }
           }
           dw_first = false;
@@ -382,13 +501,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_sh = (tid >> 7) & 1, sd_role = tid >> 8;
     const int sd_s0 = 8 * sd_sh;
     const int sd_ns = min(8, S_max - sd_s0);
-    // dW_C / dW_O: row j of SH2, states 8 dh .. 8 dh + 7
-    const int cj = tid >> 1, cdh = tid & 1;
-    const bool own_c = cj < SH2;
-    float accC[8], accO[8];
+    const int sd_box = (sd_role == 0 ? a.off_S : a.off_G) + sd_s0 * 128;  // bytes from the stage
+    const float* sd_w = sd_role == 0 ? sW_Ct + sd_d * SH2 + 4 * sd_jq : a.W_O + sd_d * SH2 + 4 * sd_jq;
+    // h of this thread in a chunk: its row, columns 8 sub .. 8 sub + 7
+    const int lo_off0 = row * 32 + (((2 * sub) ^ (row & 7)) << 2);
+    const int lo_off1 = row * 32 + (((2 * sub + 1) ^ (row & 7)) << 2);
+    // dW_C (role 0: h_s2 x dC) or dW_O (role 1: dY x ctx): 4 rows j x 4 states
+    const int cw_role = tid >> 8, cw_jq = tid & 63, cw_dq = (tid >> 6) & 3;
+    const bool cw_own = 4 * cw_jq < SH2;
+    float cacc[4][4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) accC[e] = accO[e] = 0.f;
-    int seq = 0, c = 0, ri = 0;
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cacc[i][e] = 0.f;
+    RingPos ip;  // stage of the next item
+    RingPos lr;  // loready position of the next chunk
+    RingPos lf;  // lofree position of the next chunk
+    int c = 0, ri = 0;
     for (int t = 0; t < T; ++t) {
       const long long tb0 = tile_start(t);
       const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
@@ -397,46 +526,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       float sacc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sacc[i] = 0.f;
+      // the remainder buffers share TMEM with the previous tile's transposed
+      // rows: wait until the dW MMAs of its last two row items are done
+      if (ri >= 1) bounded_wait(&bb->htfree[(ri - 1) & 1], ((ri - 1) >> 1) & 1, a.err);
+      if (ri >= 2) bounded_wait(&bb->htfree[ri & 1], ((ri - 2) >> 1) & 1, a.err);
       // ====================================================== pass 1 chunks
-      for (int q = 0; q < NC; ++q, ++seq, ++c) {
-        const int st = seq % NST;
+      // Per chunk: h - trunc(h) (rounded to tf32) into its TMEM buffer, thread
+      // = row, 8 of the chunk's 32 columns per warp; the C / d_ctx dots run
+      // while that store lands, and the chunk is handed to the MMA warp at the
+      // top of the next iteration (or after the last chunk).
+      float4 wnext = sd_role == 0 ? lds4(sd_w) : __ldg(reinterpret_cast<const float4*>(sd_w));
+      RingPos lr_prev = lr;
+      for (int q = 0; q < NC; ++q, ++c) {
+        const float4 w = wnext;
+        if (q + 1 < NC)
+          wnext = sd_role == 0 ? lds4(sd_w + (q + 1) * kChunk)
+                               : __ldg(reinterpret_cast<const float4*>(sd_w + (q + 1) * kChunk));
         if (tid == 0) TRACE_AT(0, 10);
-        bounded_wait(&bb->full[st], (seq / NST) & 1, a.err);
+        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
         if (tid == 0) TRACE_AT(0, 11);
-        float* Hc = reinterpret_cast<float*>(base + static_cast<size_t>(st) * a.stage_bytes);
-        const float* Sc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_S);
-        const float* Gc = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(Hc) + a.off_G);
+        const unsigned char* sp = stage_ptr(ip.i);
+        const float* Hc = reinterpret_cast<const float*>(sp);
+        float lo[8];
         {
-          const int jb = q * kChunk + 4 * sd_jq;
-          const float4 w = sd_role == 0 ? lds4(sW_Ct + sd_d * SH2 + jb)
-                                        : __ldg(reinterpret_cast<const float4*>(a.W_O + sd_d * SH2 + jb));
-          const float* box = sd_role == 0 ? Sc : Gc;
+          const float4 x0 = lds4(Hc + lo_off0), x1 = lds4(Hc + lo_off1);
+          const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) lo[i] = tf32_rn(xv[i] - tf32_trunc(xv[i]));
+        }
+        if (q > 0) {  // the previous chunk's remainder has landed: hand it over
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
+          lr_prev = lr;
+        }
+        if (c >= kLoBufs) bounded_wait(&bb->lofree[lf.i], lf.ph ^ 1u, a.err);
+        tc_fence_after();
+        tmem_st8(lane_base + kColLo + 32u * lf.i + 8u * sub, lo);
+        lr.next(kChunkRing);
+        lf.next(kLoBufs);
+        {
+          const float* bp = reinterpret_cast<const float*>(sp + sd_box);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             if (i < sd_ns) {
-              const int s = sd_s0 + i;
-              const float4 v = lds4(box + s * 32 + ((sd_jq ^ (s & 7)) << 2));
+              const float4 v = lds4(bp + i * 32 + ((sd_jq ^ i) << 2));  // row sd_s0 + i; (sd_s0 + i) & 7 == i
               float x = sacc[i];
               x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
               sacc[i] = x;
             }
         }
-        // the MMA warp has read the chunk as h: replace it by h - trunc(h)
-        bounded_wait(&bb->maindone[c & 1], (c >> 1) & 1, a.err);
-#pragma unroll
-        for (int v = 0; v < 2; ++v) {
-          const int i4 = tid + v * kComputeThreads;  // float4 index, 8 per 128-byte row
-          if ((i4 >> 3) < hc_rows) {
-            const float4 x = lds4(Hc + 4 * i4);
-            sts4(Hc + 4 * i4, make_float4(tf32_rn(x.x - tf32_trunc(x.x)), tf32_rn(x.y - tf32_trunc(x.y)),
-                                          tf32_rn(x.z - tf32_trunc(x.z)), tf32_rn(x.w - tf32_trunc(x.w))));
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bb->loready[c & 1]);
+        ip.next(NST);
         if (tid == 0) TRACE_AT(0, 13);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
 #pragma unroll
@@ -457,15 +604,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       {
         const int c0 = 8 * sub;  // columns c0 .. c0 + 7 of A|B
         float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        for (int p = 0; p < NP; ++p) {
-          uint32_t r0[8], r1[8];
-          tmem_ld8_nowait(lane_base + 64u * p + c0, r0);
-          tmem_ld8_nowait(lane_base + 64u * p + TD + c0, r1);
+        {
+          uint32_t r0[8], r1[8], r2[8], r3[8], r4[8];
+          tmem_ld8_nowait(lane_base + c0, r0);
+          tmem_ld8_nowait(lane_base + TD + c0, r1);
+          tmem_ld8_nowait(lane_base + 64u + c0, r2);
+          tmem_ld8_nowait(lane_base + 64u + TD + c0, r3);
+          tmem_ld8_nowait(lane_base + kColCorr + c0, r4);
           tmem_ld_wait();
+          const bool odd = NC > 1;  // the odd-chunk sum exists
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] += __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
+          for (int i = 0; i < 8; ++i) {
+            const float m1 = odd ? __uint_as_float(r2[i]) : 0.f;
+            const float c1 = odd ? __uint_as_float(r3[i]) : 0.f;
+            v[i] = (__uint_as_float(r0[i]) + m1) +
+                   ((__uint_as_float(r1[i]) + c1) + __uint_as_float(r4[i]));
+          }
         }
         sts4(sPh + sw128_idx(row, c0), make_float4(v[0], v[1], v[2], v[3]));
         sts4(sPh + sw128_idx(row, c0 + 4), make_float4(v[4], v[5], v[6], v[7]));
@@ -531,63 +685,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       named_sync(1, kComputeThreads);
       if (tid == 0) mbar_arrive(&bb->bready);
       if (tid == 0) TRACE_AT(0, 24);
-      // ===================== per sample: dW_C, dW_O partial sums and d_h_s2
-      for (int k = 0; k < NSI; ++k, ++seq) {
-        const int st = seq % NST;
-        bounded_wait(&bb->full[st], (seq / NST) & 1, a.err);
-        if (tid == 0) TRACE_AT(0, 31);
-        float* hsb = reinterpret_cast<float*>(base + static_cast<size_t>(st) * a.stage_bytes);
-        float* gb = hsb + static_cast<size_t>(kBwdSampleItem) * SH2;
-        const int s0 = k * kBwdSampleItem, ns = min(kBwdSampleItem, S_t - s0);
-        if (own_c) {
-          for (int s = 0; s < ns; ++s) {
-            const float hv = hsb[s * SH2 + cj], gv = gb[s * SH2 + cj];
-            const float4 dc0 = lds4(sDC + (s0 + s) * D + 8 * cdh), dc1 = lds4(sDC + (s0 + s) * D + 8 * cdh + 4);
-            const float4 cx0 = lds4(sCtx + (s0 + s) * D + 8 * cdh), cx1 = lds4(sCtx + (s0 + s) * D + 8 * cdh + 4);
-            const float dcv[8] = {dc0.x, dc0.y, dc0.z, dc0.w, dc1.x, dc1.y, dc1.z, dc1.w};
-            const float cxv[8] = {cx0.x, cx0.y, cx0.z, cx0.w, cx1.x, cx1.y, cx1.z, cx1.w};
+      // ======= sample items (dW_C, dW_O partial sums, d_h_s2) and 16-row items
+      // (h^T into TMEM for dW, d_h_history rows out), in post_item order
+      const int hh = sub & 1, rg = sub >> 1;
+      const int jrow = 128 * hh + 32 * qd + lane;
+      const bool jok = jrow < SH2;
+      for (int pi = 0; pi < NSI + NRI; ++pi) {
+        int kind, k;
+        post_item(pi, NSI, NRI, kind, k);
+        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        float* stg = reinterpret_cast<float*>(stage_ptr(ip.i));
+        const int st = ip.i;
+        ip.next(NST);
+        if (kind == 1) {
+          if (tid == 0) TRACE_AT(0, 31);
+          float* hsb = stg;
+          const float* gb = hsb + static_cast<size_t>(kBwdSampleItem) * SH2;
+          const int s0 = k * kBwdSampleItem, ns = min(kBwdSampleItem, S_t - s0);
+          if (cw_own) {
+            const float* rowp = (cw_role == 0 ? hsb : gb) + 4 * cw_jq;
+            const float* vecp = (cw_role == 0 ? sDC : sCtx) + s0 * D + 4 * cw_dq;
+            for (int s = 0; s < ns; ++s) {
+              const float4 hv = lds4(rowp + s * SH2);
+              const float4 vv = lds4(vecp + s * D);
+              const float hvv[4] = {hv.x, hv.y, hv.z, hv.w}, vvv[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              accC[e] = fmaf(hv, dcv[e], accC[e]);
-              accO[e] = fmaf(gv, cxv[e], accO[e]);
+              for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cacc[i][e] = fmaf(hvv[i], vvv[e], cacc[i][e]);
             }
           }
-        }
-        named_sync(1, kComputeThreads);  // h_s2 rows no longer needed: d_h_s2 goes there
-        {
-          const int jq = tid & 63, s = tid >> 6;
-          if (s < ns && 4 * jq < SH2) {
-            float4 o = lds4(gb + s * SH2 + 4 * jq);
-            const float* dcr = sDC + (s0 + s) * D;
-#pragma unroll 4
-            for (int d = 0; d < D; ++d) {
-              const float4 w = lds4(sW_Ct + d * SH2 + 4 * jq);
-              const float dcv = dcr[d];
-              o.x = fmaf(dcv, w.x, o.x);
-              o.y = fmaf(dcv, w.y, o.y);
-              o.z = fmaf(dcv, w.z, o.z);
-              o.w = fmaf(dcv, w.w, o.w);
+          named_sync(1, kComputeThreads);  // h_s2 rows no longer needed: d_h_s2 goes there
+          {
+            const int jq = tid & 63, s = tid >> 6;
+            if (s < ns && 4 * jq < SH2) {
+              float4 o = lds4(gb + s * SH2 + 4 * jq);
+              const float* dcr = sDC + (s0 + s) * D;
+#pragma unroll
+              for (int dq = 0; dq < 4; ++dq) {
+                const float4 dcv = lds4(dcr + 4 * dq);
+                const float dv[4] = {dcv.x, dcv.y, dcv.z, dcv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float4 w = lds4(sW_Ct + (4 * dq + e) * SH2 + 4 * jq);
+                  o.x = fmaf(dv[e], w.x, o.x);
+                  o.y = fmaf(dv[e], w.y, o.y);
+                  o.z = fmaf(dv[e], w.z, o.z);
+                  o.w = fmaf(dv[e], w.w, o.w);
+                }
+              }
+              sts4(hsb + s * SH2 + 4 * jq, o);
             }
-            sts4(hsb + s * SH2 + 4 * jq, o);
           }
-        }
-        fence_proxy_async_smem();
-        named_sync(1, kComputeThreads);
-        if (tid == 0) {
-          mbar_arrive(&bb->empty[st]);  // the producer stores d_h_s2 from the stage
-          TRACE_AT(0, 33);
-        }
-      }
-      // ========== per 16 rows: h^T into TMEM for dW, d_h_history rows out
-      {
-        const int h = sub & 1, rg = sub >> 1;
-        const int j = 128 * h + 32 * qd + lane;
-        const bool jok = j < SH2;
-        for (int k = 0; k < NRI; ++k, ++seq, ++ri) {
-          const int st = seq % NST;
-          bounded_wait(&bb->full[st], (seq / NST) & 1, a.err);
+          fence_proxy_async_smem();
+          named_sync(1, kComputeThreads);
+          if (tid == 0) {
+            mbar_arrive(&bb->empty[st], kEmptyArrivals);  // the producer stores d_h_s2 from the stage
+            TRACE_AT(0, 33);
+          }
+        } else {
           if (tid == 0) TRACE_AT(0, 41);
-          float* hb = reinterpret_cast<float*>(base + static_cast<size_t>(st) * a.stage_bytes);
+          float* hb = stg;
           const int r0 = k * kRowItem, nr = min(kRowItem, R_t - r0);
           if (ri >= 2) bounded_wait(&bb->htfree[ri & 1], ((ri - 2) >> 1) & 1, a.err);
           tc_fence_after();
@@ -596,11 +754,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int r = 8 * rg + i;
-              const float x = (r < nr && jok) ? hb[r * SH2 + j] : 0.f;
+              const float x = (r < nr && jok) ? hb[r * SH2 + jrow] : 0.f;
               raw[i] = x;
-              lo[i] = tf32_rn(x - tf32_trunc(x));
+              lo[i] = x - tf32_trunc(x);
             }
-            const uint32_t tb = lane_base + kColHT + 64u * (ri & 1) + 32u * h + 8u * rg;
+            const uint32_t tb = lane_base + kColHT + 64u * (ri & 1) + 32u * hh + 8u * rg;
             tmem_st8(tb, raw);
             tmem_st8(tb + 16u, lo);
           }
@@ -629,11 +787,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           named_sync(1, kComputeThreads);  // every read of the h rows done
           {
             float v[8];
-            tmem_ld<8>(lane_base + 64u * h + 16u * (k & 3) + 8u * rg, v);
+            tmem_ld<8>(lane_base + 64u * hh + 16u * (k & 3) + 8u * rg, v);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int r = 8 * rg + i;
-              if (r < nr && jok) hb[r * SH2 + j] = v[i];
+              if (r < nr && jok) hb[r * SH2 + jrow] = v[i];
             }
           }
           const bool last_of_half = (k & 3) == 3 || k == NRI - 1;
@@ -642,12 +800,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           named_sync(1, kComputeThreads);
           if (tid == 0) {
             if (last_of_half) mbar_arrive(&bb->dhfree[rh]);
-            mbar_arrive(&bb->empty[st]);  // the producer stores the d_h rows from the stage
+            mbar_arrive(&bb->empty[st], kEmptyArrivals);  // the producer stores the d_h rows from the stage
             TRACE_AT(0, 42);
           }
+          ++ri;
         }
-        if (NRI <= 4 && tid == 0) mbar_arrive(&bb->dhfree[1]);
       }
+      if (NRI <= 4 && tid == 0) mbar_arrive(&bb->dhfree[1]);
       if (tid == 0) TRACE_AT(0, 46);
     }
     // ===================================== partial sums into the CTA's slot
@@ -669,12 +828,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
                                m[4 * i + 3] + r[4 * i + 3]);
       }
     }
-    if (own_c) {
+    if (cw_own) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int d = 8 * cdh + e;
-        slot[2 * n + cj * D + d] = accC[e];
-        slot[3 * n + d * SH2 + cj] = a.tw * accO[e];
+      for (int i = 0; i < 4; ++i) {
+        const int j = 4 * cw_jq + i;
+        if (cw_role == 0) {
+          *reinterpret_cast<float4*>(slot + 2 * n + j * D + 4 * cw_dq) =
+              make_float4(cacc[i][0], cacc[i][1], cacc[i][2], cacc[i][3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) slot[3 * n + (4 * cw_dq + e) * SH2 + j] = a.tw * cacc[i][e];
+        }
       }
     }
     if (tid == 0) TRACE_AT(0, 50);
@@ -691,7 +855,7 @@ int round_up_b(int x, int m) { return (x + m - 1) / m * m; }
 bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a) {
   if (!fast_path_ok(K, SH2, D) || D != 16) return false;
   int S_max = kTileRows / K;
-  if (S_max > kComputeWarps) S_max = kComputeWarps;  // one warp per sample in the dots
+  if (S_max > 16) S_max = 16;  // the dots cover two halves of 8 samples, the scan 16 x D threads
   const int hc = S_max * K * 128, sc = S_max * 128;
   const int off_S = round_up_b(hc, 1024);
   const int off_G = off_S + round_up_b(sc, 1024);
