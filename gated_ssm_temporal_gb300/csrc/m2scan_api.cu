@@ -18,6 +18,7 @@ cudaError_t prepare_fast_kernels(int max_smem);
 cudaError_t prepare_generic_kernels(int max_smem);
 cudaError_t prepare_fwd_tc_kernels(int max_smem);
 cudaError_t prepare_bwd_tc_kernels(int max_smem);
+cudaError_t prepare_fwd_tc16_kernels(int max_smem);
 }  // namespace m2scan
 
 using namespace m2scan;
@@ -69,6 +70,7 @@ m2scan_status prepare_device(int* dev_out) {
   if ((e = prepare_generic_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_fwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_bwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
+  if ((e = prepare_fwd_tc16_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   void* p = nullptr;
   if ((e = cudaGetSymbolAddress(&p, g_m2scan_err_word)) != cudaSuccess) return cuda_fail(e);
   if (!g_encode) {
@@ -130,6 +132,7 @@ int slots_for(int64_t B) { return B < kMaxSlots ? static_cast<int>(B) : kMaxSlot
 int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_smem,
                 FastArgs* plan) {
   if (!g_force_generic.load() && B <= 0x7fffffffll) {
+    if (!bwd && fwd_tc16_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (!bwd && fwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (bwd && bwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (fast_plan(bwd, K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
@@ -251,7 +254,9 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
     fa.out0 = h_enriched; fa.out1 = nullptr; fa.ws = nullptr;
     fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, nullptr, B)) return M2SCAN_ERR_UNSUPPORTED;
-    e = fa.tc ? launch_fwd_tc(D, fa, grid, stream) : launch_fast(false, D, fa, grid, stream);
+    e = fa.tc == 2 ? launch_fwd_tc16(fa, grid, stream)
+        : fa.tc    ? launch_fwd_tc(D, fa, grid, stream)
+                   : launch_fast(false, D, fa, grid, stream);
   } else {
     GenericArgs ga{h_history, h_s2, nullptr, W_A, W_B, W_C, W_O, h_enriched, nullptr, nullptr,
                    B, K, SH2, D, tw};

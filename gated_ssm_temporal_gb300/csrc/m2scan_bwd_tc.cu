@@ -292,8 +292,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       ++ptile;
     }
   };
-  if (warp == kProducerWarp && lane == 0)
-    for (int i = 0; i < NST && ptile < T; ++i) produce_one();
 
   // ---- weights: projection B tiles and W_C^T into shared memory, [W_A|W_B]
   // rows into TMEM; every global load is issued before the first store
@@ -318,6 +316,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       wb[u] = ok ? __ldg(a.W_B + i) : 0.f;
       wc[u] = ok ? __ldg(a.W_C + i) : 0.f;
     }
+    // the first stages are requested after the weights, so that the weight
+    // loads are not queued behind them
+    if (warp == kProducerWarp && lane == 0)
+      for (int i = 0; i < NST && ptile < T; ++i) produce_one();
     if (warp < kComputeWarps) {
       // thread = TMEM lane = row j of [W_A|W_B] within its j-half
       float v[32];
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           const float4 x0 = lds4(Hc + lo_off0), x1 = lds4(Hc + lo_off1);
           const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) lo[i] = tf32_rn(xv[i] - tf32_trunc(xv[i]));
+          for (int i = 0; i < 8; ++i) lo[i] = xv[i] - tf32_trunc(xv[i]);
         }
         if (q > 0) {  // the previous chunk's remainder has landed: hand it over
           tmem_st_wait();

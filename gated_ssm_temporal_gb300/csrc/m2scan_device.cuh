@@ -391,4 +391,38 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
   } while (0)
 #endif
 
+// Debug time accounting (builds with -DM2SCAN_TRACE): a thread adds the time
+// between PROF_BEGIN() and PROF_END(slot) to its slot (0..15); PROF_FLUSH(tag)
+// writes the slots of CTA 0 to trace entries 3072 + 16 * tag ...
+#ifdef M2SCAN_TRACE
+#define PROF_DECL                            \
+  unsigned long long prof_acc[16] = {};     \
+  unsigned long long prof_t0 = 0;           \
+  (void)prof_acc;                           \
+  (void)prof_t0
+#define PROF_BEGIN() (prof_t0 = global_timer_ns())
+#define PROF_END(slot) (prof_acc[slot] += global_timer_ns() - prof_t0)
+#define PROF_FLUSH(tag)                                                         \
+  do {                                                                          \
+    if (a.trace && blockIdx.x == 0)                                             \
+      for (int pi_ = 0; pi_ < 16; ++pi_) {                                      \
+        a.trace[2 * (3072 + 16 * (tag) + pi_)] = 1000 + 16 * (tag) + pi_;       \
+        a.trace[2 * (3072 + 16 * (tag) + pi_) + 1] = prof_acc[pi_];             \
+      }                                                                         \
+  } while (0)
+#else
+#define PROF_DECL \
+  do {            \
+  } while (0)
+#define PROF_BEGIN() \
+  do {               \
+  } while (0)
+#define PROF_END(slot) \
+  do {                 \
+  } while (0)
+#define PROF_FLUSH(tag) \
+  do {                  \
+  } while (0)
+#endif
+
 }  // namespace m2scan

@@ -1,0 +1,530 @@
+// Forward of the gated temporal scan layer for D = 16 with the projections on
+// the tensor cores, warp-specialised like the backward kernel (SH2 % 32 == 0,
+// SH2 <= 256, K <= 128).
+//
+// One persistent CTA per slot range of samples walks them in tiles of at most
+// 128 rows (S samples x K) ("Custom Kernel Optimization -- cuBLAS Projections
+// + Batch-Parallel Scans", Design 1, Steps 1-2; output step as the layer fixes
+// it). Per tile:
+//   pass 1   the producer warp streams 32-column chunks of h_history and h_s2
+//            (TMA boxes, 128-byte swizzle). The MMA warp computes
+//            A|B = h . [W_A|W_B] with the chunk as the A operand straight from
+//            shared memory (the tensor core reads trunc(h)); the compute warps
+//            write h - trunc(h) (rounded to tf32) into tensor memory and the MMA
+//            warp adds that product (3 x tf32 in all). A stage is free once its
+//            main MMAs are done and the compute warps have read it. The compute
+//            warps form C = h_s2 . W_C on the FMA pipe meanwhile.
+//   scan     x_t = sigmoid(A_t) x_{t-1} + B_t, one thread per (sample, state);
+//            ctx = C x_{K-1}.
+//   output   h_enriched = h_s2 + tw ctx . W_O over the tile's h_s2 rows, in
+//            place in their stage; the producer warp stores them before it
+//            reuses the stage.
+#include "m2scan_device.cuh"
+#include "m2scan_internal.h"
+
+namespace m2scan {
+namespace {
+
+constexpr int kComputeWarps = 16;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kFwdThreads = kComputeThreads + 64;
+constexpr int kProducerWarp = kComputeWarps;
+constexpr int kMmaWarp = kComputeWarps + 1;
+constexpr int kChunkRing = 6;
+constexpr uint32_t kEmptyArrivals = 2;
+constexpr int kLoBufs = 3;
+
+struct FwdBars {
+  uint64_t full[kMaxStages];     // producer -> all: stage loaded
+  uint64_t empty[kMaxStages];    // stage free: two arrivals
+  uint64_t loready[kChunkRing];  // compute -> MMA: chunk read, h - trunc(h) in TMEM
+  uint64_t lofree[kLoBufs];      // MMA -> compute: remainder buffer consumed
+  uint64_t accfull;              // MMA -> compute: projections of the tile done
+  uint64_t accempty;             // compute -> MMA: projections read back
+  uint32_t tslot;
+  uint32_t pad;
+};
+
+// TMEM columns: [0, 128) trunc(h) . [W_hi | W_lo] of the even and of the odd
+// chunks; [128, 224) three buffers of h - trunc(h); [224, 256)
+// (h - trunc h) . W_hi.
+constexpr uint32_t kColLo = 128;
+constexpr uint32_t kColCorr = 224;
+
+struct RingPos {
+  int i = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++i == n) {
+      i = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+struct IdleClock {
+  unsigned long long t0 = 0;
+  uint32_t n = 0;
+  __device__ __forceinline__ void progress() {
+    n = 0;
+    t0 = 0;
+  }
+  __device__ __forceinline__ bool idle(unsigned* err) {
+    if ((++n & 7u) != 0u) return false;
+    const unsigned long long now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+      return false;
+    }
+    if ((*reinterpret_cast<volatile unsigned*>(err) & kErrWaitTimeout) != 0u) return true;
+    if (now - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrWaitTimeout);
+      return true;
+    }
+    __nanosleep(100);
+    return false;
+  }
+};
+
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_constant__ FastArgs a) {
+  constexpr int D = 16, TD = 32, FD = 64;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  float* sW = reinterpret_cast<float*>(base + a.off_wt);      // NC tiles [FD][32], swizzled
+  float* sW_Ct = reinterpret_cast<float*>(base + a.off_wct);  // W_C transposed [D][SH2]
+  float* sW_O = reinterpret_cast<float*>(base + a.off_wo);    // W_O [D][SH2]
+  float* sP = reinterpret_cast<float*>(base + a.off_p);       // A|B [128][32] swizzled
+  float* sC = reinterpret_cast<float*>(base + a.off_cs);      // C [S_max][D]
+  float* sCtx = reinterpret_cast<float*>(base + a.off_ctx);   // ctx [S_max][D]
+  FwdBars* bb = reinterpret_cast<FwdBars*>(base + a.off_bar);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K, SH2 = a.SH2, S_max = a.S_max, NST = a.n_stages;
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.stage_bytes);
+  const int NC = SH2 / kChunk;
+  const long long B = a.B;
+  const int P = gridDim.x, cta = blockIdx.x;
+  const long long cb0 = B * cta / P;
+  const int n_c = static_cast<int>(B * (cta + 1) / P - cb0);
+  const int T = (n_c + S_max - 1) / S_max;
+  const int t_base = n_c / T, t_extra = n_c - (n_c / T) * T;
+  auto tile_start = [&](int i) -> long long {
+    return cb0 + static_cast<long long>(i) * t_base + (i < t_extra ? i : t_extra);
+  };
+  auto stage_ptr = [&](int st) { return base + static_cast<uint32_t>(st) * stage_bytes; };
+
+  if (tid == kProducerWarp * 32) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_h)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_hs)) : "memory");
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&bb->full[s], 1);
+      mbar_init(&bb->empty[s], kEmptyArrivals);
+    }
+    for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
+    for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
+    mbar_init(&bb->accfull, 1);
+    mbar_init(&bb->accempty, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&bb->tslot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bb->tslot;
+
+  // ---- producer: per tile NC chunks, then one item of the tile's h_s2 rows
+  // (h_enriched is written over them; the producer stores it before it reuses
+  // the stage)
+  RingPos lp, rp;
+  int pn = 0, ptile = 0, pit = 0;
+  int rn = 0, rtile = 0, rit = 0;
+  auto release_one = [&]() {
+    bounded_wait(&bb->empty[rp.i], rp.ph, a.err);
+    if (rit == NC) {
+      const long long tb0 = tile_start(rtile);
+      const int S_t = static_cast<int>(tile_start(rtile + 1) - tb0);
+      bulk_store(a.out0 + tb0 * SH2, stage_ptr(rp.i), static_cast<uint32_t>(S_t) * SH2 * 4u);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+    rp.next(NST);
+    ++rn;
+    if (++rit == NC + 1) {
+      rit = 0;
+      ++rtile;
+    }
+  };
+  auto produce_one = [&]() {
+    const long long tb0 = tile_start(ptile);
+    const int S_t = static_cast<int>(tile_start(ptile + 1) - tb0);
+    if (pn >= NST) release_one();
+    unsigned char* sp = stage_ptr(lp.i);
+    uint64_t* bar = &bb->full[lp.i];
+    if (pit < NC) {
+      mbar_arrive_expect_tx(bar, a.hc_bytes + a.sc_bytes);
+      tma_load_3d(sp, &a.tm_h, pit * kChunk, 0, static_cast<int>(tb0), bar);
+      tma_load_2d(sp + a.off_S, &a.tm_hs, pit * kChunk, static_cast<int>(tb0), bar);
+    } else {
+      const uint32_t rb = static_cast<uint32_t>(S_t) * SH2 * 4u;
+      mbar_arrive_expect_tx(bar, rb);
+      bulk_load(sp, a.h_s2 + tb0 * SH2, rb, bar);
+    }
+    lp.next(NST);
+    ++pn;
+    if (++pit == NC + 1) {
+      pit = 0;
+      ++ptile;
+    }
+  };
+
+  // ---- weights: projection B tiles, W_C^T and W_O into shared memory
+  constexpr int kWPer = (4096 + kFwdThreads - 1) / kFwdThreads;
+  {
+    float wa[kWPer], wb[kWPer], wc[kWPer], wo[kWPer];
+#pragma unroll
+    for (int u = 0; u < kWPer; ++u) {
+      const int i = tid + u * kFwdThreads;
+      const bool ok = i < SH2 * D;
+      wa[u] = ok ? __ldg(a.W_A + i) : 0.f;
+      wb[u] = ok ? __ldg(a.W_B + i) : 0.f;
+      wc[u] = ok ? __ldg(a.W_C + i) : 0.f;
+      wo[u] = ok ? __ldg(a.W_O + i) : 0.f;
+    }
+    // the first stages are requested after the weights, so that the weight
+    // loads are not queued behind them
+    if (warp == kProducerWarp && lane == 0)
+      for (int i = 0; i < NST && ptile < T; ++i) produce_one();
+#pragma unroll
+    for (int u = 0; u < kWPer; ++u) {
+      const int i = tid + u * kFwdThreads;
+      if (i >= SH2 * D) break;
+      const int j = i / D, d = i - (i / D) * D;
+      float* tile = sW + (j >> 5) * FD * 32;
+      const int jj = j & 31;
+      const float ha = tf32_rn(wa[u]), hb = tf32_rn(wb[u]);
+      tile[sw128_idx(d, jj)] = ha;
+      tile[sw128_idx(D + d, jj)] = hb;
+      tile[sw128_idx(TD + d, jj)] = wa[u] - ha;
+      tile[sw128_idx(TD + D + d, jj)] = wb[u] - hb;
+      sW_Ct[d * SH2 + j] = wc[u];
+      sW_O[i] = wo[u];
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      while (ptile < T) produce_one();
+      while (rn < pn) release_one();
+      bulk_wait_all();
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc64 = umma_idesc_tf32(128, 64);
+      constexpr uint32_t idesc32 = umma_idesc_tf32(128, 32);
+      const uint32_t ring = smem_addr(base);
+      const uint32_t w0 = smem_addr(sW);
+      RingPos tp, lr, lf;
+      for (int t = 0; t < T; ++t) {
+        if (t > 0) bounded_wait(&bb->accempty, (t - 1) & 1, a.err);
+        tc_fence_after();
+        // remainder products of a chunk as soon as it is written, else main
+        // products of the next landed chunk (at most two ahead); each kind in
+        // chunk order into its own accumulator. descriptor + 2 u = 32 u bytes on.
+        RingPos pm = tp, pc = tp;
+        int qm = 0, qc = 0;
+        IdleClock clk;
+        while (qc < NC) {
+          bool did = false;
+          if (qc < qm && mbar_test_wait(&bb->loready[lr.i], lr.ph)) {
+            tc_fence_after();
+            mbar_arrive(&bb->empty[pc.i]);  // the compute warps are done with it
+            const uint32_t al = tmem + kColLo + 32u * lf.i;
+            const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_tf32_ta(tmem + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(&bb->lofree[lf.i]);
+            lr.next(kChunkRing);
+            lf.next(kLoBufs);
+            pc.next(NST);
+            ++qc;
+            did = true;
+          }
+          if (!did && qm < NC && qm < qc + 2 && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
+            tc_fence_after();
+            const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
+            const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_tf32(tmem + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
+            umma_commit(&bb->empty[pm.i]);  // first of the stage's two arrivals
+            pm.next(NST);
+            ++qm;
+            did = true;
+          }
+          if (did)
+            clk.progress();
+          else if (clk.idle(a.err))
+            break;
+        }
+        for (int i = 0; i < NC + 1; ++i) tp.next(NST);
+        umma_commit(&bb->accfull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- compute
+    const int qd = warp & 3, sub = warp >> 2;
+    const int row = 32 * qd + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    // C partial dots: thread = (sample quarter, state, column quad), 4 samples
+    const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_s0 = 4 * (tid >> 7);
+    const int sd_ns = min(4, S_max - sd_s0);
+    const int sd_box = a.off_S + sd_s0 * 128;
+    const float* sd_w = sW_Ct + sd_d * SH2 + 4 * sd_jq;
+    const int lo_off0 = row * 32 + (((2 * sub) ^ (row & 7)) << 2);
+    const int lo_off1 = row * 32 + (((2 * sub + 1) ^ (row & 7)) << 2);
+    RingPos ip, lr, lf;
+    int c = 0;
+    PROF_DECL;
+    for (int t = 0; t < T; ++t) {
+      const long long tb0 = tile_start(t);
+      const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      // ====================================================== pass 1 chunks
+      float4 wnext = lds4(sd_w);
+      RingPos lr_prev = lr;
+      for (int q = 0; q < NC; ++q, ++c) {
+        const float4 w = wnext;
+        if (q + 1 < NC) wnext = lds4(sd_w + (q + 1) * kChunk);
+        PROF_BEGIN();
+        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        PROF_END(0);
+        PROF_BEGIN();
+        const unsigned char* sp = stage_ptr(ip.i);
+        const float* Hc = reinterpret_cast<const float*>(sp);
+        float lo[8];
+        {
+          const float4 x0 = lds4(Hc + lo_off0), x1 = lds4(Hc + lo_off1);
+          const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) lo[i] = xv[i] - tf32_trunc(xv[i]);
+        }
+        PROF_END(1);
+        if (q > 0) {  // the previous chunk's remainder has landed: hand it over
+          PROF_BEGIN();
+          tmem_st_wait();
+          PROF_END(2);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
+          lr_prev = lr;
+        }
+        PROF_BEGIN();
+        if (c >= kLoBufs) bounded_wait(&bb->lofree[lf.i], lf.ph ^ 1u, a.err);
+        PROF_END(3);
+        PROF_BEGIN();
+        tc_fence_after();
+        tmem_st8(lane_base + kColLo + 32u * lf.i + 8u * sub, lo);
+        lr.next(kChunkRing);
+        lf.next(kLoBufs);
+        {
+          const float* bp = reinterpret_cast<const float*>(sp + sd_box);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < sd_ns) {
+              const int s = sd_s0 + i;
+              const float4 v = lds4(bp + i * 32 + ((sd_jq ^ (s & 7)) << 2));
+              float x = sacc[i];
+              x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
+              sacc[i] = x;
+            }
+        }
+        ip.next(NST);
+        PROF_END(4);
+      }
+      PROF_BEGIN();
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) sacc[i] += __shfl_xor_sync(0xffffffffu, sacc[i], m);
+      }
+      if (sd_jq == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (sd_s0 + i < S_t) sC[(sd_s0 + i) * D + sd_d] = sacc[i];
+      }
+      PROF_END(5);
+      // ==================================== projections: TMEM -> shared memory
+      PROF_BEGIN();
+      bounded_wait(&bb->accfull, t & 1, a.err);
+      PROF_END(6);
+      PROF_BEGIN();
+      tc_fence_after();
+      {
+        const int c0 = 8 * sub;  // columns c0 .. c0 + 7 of A|B
+        uint32_t r0[8], r1[8], r2[8], r3[8], r4[8];
+        tmem_ld8_nowait(lane_base + c0, r0);
+        tmem_ld8_nowait(lane_base + TD + c0, r1);
+        tmem_ld8_nowait(lane_base + 64u + c0, r2);
+        tmem_ld8_nowait(lane_base + 64u + TD + c0, r3);
+        tmem_ld8_nowait(lane_base + kColCorr + c0, r4);
+        tmem_ld_wait();
+        const bool odd = NC > 1;  // the odd-chunk sum exists
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float m1 = odd ? __uint_as_float(r2[i]) : 0.f;
+          const float c1 = odd ? __uint_as_float(r3[i]) : 0.f;
+          v[i] = (__uint_as_float(r0[i]) + m1) + ((__uint_as_float(r1[i]) + c1) + __uint_as_float(r4[i]));
+        }
+        sts4(sP + sw128_idx(row, c0), make_float4(v[0], v[1], v[2], v[3]));
+        sts4(sP + sw128_idx(row, c0 + 4), make_float4(v[4], v[5], v[6], v[7]));
+      }
+      tc_fence_before();
+      named_sync(1, kComputeThreads);
+      if (tid == 0) mbar_arrive(&bb->accempty);
+      PROF_END(7);
+      PROF_BEGIN();
+      // ============================== scan: one thread per (sample, state)
+      if (tid < S_t * D) {
+        const int s = tid >> 4, d = tid & 15, rb = s * K;
+        float x = 0.f;
+        for (int k0 = 0; k0 < K; k0 += 8) {
+          const int n = min(8, K - k0);
+          float av[8], bv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < n) {
+              av[u] = sP[sw128_idx(rb + k0 + u, d)];
+              bv[u] = sP[sw128_idx(rb + k0 + u, D + d)];
+            }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < n) av[u] = sigmoid_fast(av[u]);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < n) x = fmaf(av[u], x, bv[u]);
+        }
+        sCtx[s * D + d] = sC[s * D + d] * x;
+      }
+      named_sync(1, kComputeThreads);
+      PROF_END(8);
+      // ====== output: h_enriched = h_s2 + tw ctx . W_O, in place over h_s2
+      {
+        PROF_BEGIN();
+        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        PROF_END(9);
+        PROF_BEGIN();
+        float* hs = reinterpret_cast<float*>(stage_ptr(ip.i));
+        const int st = ip.i;
+        ip.next(NST);
+        const int s = warp;  // one sample per warp, 4 columns x 2 per thread
+        if (s < S_t) {
+          const float* cr = sCtx + s * D;
+          float cx[D];
+#pragma unroll
+          for (int q = 0; q < D / 4; ++q) {
+            const float4 v = lds4(cr + 4 * q);
+            cx[4 * q] = v.x; cx[4 * q + 1] = v.y; cx[4 * q + 2] = v.z; cx[4 * q + 3] = v.w;
+          }
+#pragma unroll
+          for (int hv = 0; hv < 2; ++hv) {
+            const int jq = lane + 32 * hv;
+            if (4 * jq < SH2) {
+              float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int d = 0; d < D; ++d) {
+                const float4 w = lds4(sW_O + d * SH2 + 4 * jq);
+                o.x = fmaf(cx[d], w.x, o.x);
+                o.y = fmaf(cx[d], w.y, o.y);
+                o.z = fmaf(cx[d], w.z, o.z);
+                o.w = fmaf(cx[d], w.w, o.w);
+              }
+              float* hp = hs + s * SH2 + 4 * jq;
+              float4 h = lds4(hp);
+              h.x = fmaf(a.tw, o.x, h.x);
+              h.y = fmaf(a.tw, o.y, h.y);
+              h.z = fmaf(a.tw, o.z, h.z);
+              h.w = fmaf(a.tw, o.w, h.w);
+              sts4(hp, h);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_sync(1, kComputeThreads);
+        if (tid == 0) mbar_arrive(&bb->empty[st], kEmptyArrivals);  // the producer stores it
+        PROF_END(10);
+      }
+    }
+    if (tid == 0) PROF_FLUSH(0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 256);
+}
+
+int round_up_f(int x, int m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a) {
+  if (!fast_path_ok(K, SH2, D) || D != 16) return false;
+  int S_max = kTileRows / K;
+  if (S_max > 16) S_max = 16;  // the dots cover four quarters of 4 samples, the output one sample per warp
+  const int hc = S_max * K * 128, sc = S_max * 128;
+  const int off_S = round_up_f(hc, 1024);
+  int stage = off_S + sc;
+  if (S_max * SH2 * 4 > stage) stage = S_max * SH2 * 4;
+  // the projection MMAs read 128 rows of 128 bytes from the start of a stage
+  if (kTileRows * 128 > stage) stage = kTileRows * 128;
+  stage = round_up_f(stage, 1024);
+  const int wbytes = SH2 * 4 * D * 4;
+  const int rest = wbytes + 2 * D * SH2 * 4 + kTileRows * 128 + 2 * S_max * D * 4 +
+                   static_cast<int>(sizeof(FwdBars)) + 16 + 1024;
+  int n_stages = kMaxStages;
+  while (n_stages > 2 && n_stages * stage + rest > 227 * 1024) --n_stages;
+  int off = n_stages * stage;
+  a->off_wt = off;  off += wbytes;
+  a->off_wct = off; off += D * SH2 * 4;
+  a->off_wo = off;  off += D * SH2 * 4;
+  a->off_p = off;   off += kTileRows * 128;
+  a->off_cs = off;  off += S_max * D * 4;
+  a->off_ctx = off; off += S_max * D * 4;
+  off = round_up_f(off, 16);
+  a->off_bar = off; off += static_cast<int>(sizeof(FwdBars));
+  a->smem_bytes = off + 1024;
+  a->S_max = S_max;
+  a->SG = S_max;
+  a->stage_bytes = stage;
+  a->hc_bytes = hc;
+  a->sc_bytes = sc;
+  a->off_S = off_S;
+  a->off_G = off_S;
+  a->K = K;
+  a->SH2 = SH2;
+  a->n_stages = n_stages;
+  a->tc = 2;
+  a->tmem_cols = 256;
+  return a->smem_bytes <= 227 * 1024;
+}
+
+cudaError_t launch_fwd_tc16(const FastArgs& a, int grid, cudaStream_t stream) {
+  fwd_tc16_kernel<<<grid, kFwdThreads, a.smem_bytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_fwd_tc16_kernels(int max_smem) {
+  return cudaFuncSetAttribute(fwd_tc16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+}
+
+}  // namespace m2scan

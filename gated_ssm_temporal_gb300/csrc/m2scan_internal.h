@@ -55,7 +55,7 @@ struct alignas(128) FastArgs {
   int off_mbar;   // tensor-core path: two MMA-completion barriers
   int off_tslot;  // tensor-core path: TMEM base address written by tcgen05.alloc
   int n_stages;   // depth of the copy ring
-  int tc;         // 1 when the projections run on the tensor cores
+  int tc;         // 0: FP32-FMA kernel, 1: tensor-core kernel, 2: 16-warp tensor-core forward
   int tmem_cols;  // TMEM columns allocated by each CTA (power of two)
   int smem_bytes;
   float tw;
@@ -91,6 +91,10 @@ cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream
 // Warp-specialised tensor-core forward (D in {8, 16}).
 bool fwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_fwd_tc(int D, const FastArgs& a, int grid, cudaStream_t stream);
+// Warp-specialised tensor-core forward for D = 16 with 16 compute warps
+// (plan->tc = 2).
+bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a);
+cudaError_t launch_fwd_tc16(const FastArgs& a, int grid, cudaStream_t stream);
 // Warp-specialised tensor-core backward (D = 16).
 bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_bwd_tc(const FastArgs& a, int grid, cudaStream_t stream);
