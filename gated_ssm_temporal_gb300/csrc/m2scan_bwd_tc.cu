@@ -502,7 +502,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     // role 0 sums h_s2 . W_C, role 1 dY . W_O^T, for 8 samples at once
     const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_sh = (tid >> 7) & 1, sd_role = tid >> 8;
     const int sd_s0 = 8 * sd_sh;
-    const int sd_ns = min(8, S_max - sd_s0);
     const int sd_box = (sd_role == 0 ? a.off_S : a.off_G) + sd_s0 * 128;  // bytes from the stage
     const float* sd_w = sd_role == 0 ? sW_Ct + sd_d * SH2 + 4 * sd_jq : a.W_O + sd_d * SH2 + 4 * sd_jq;
     // h of this thread in a chunk: its row, columns 8 sub .. 8 sub + 7
@@ -569,15 +568,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         lr.next(kChunkRing);
         lf.next(kLoBufs);
         {
+          // all 8 rows of this half even past S_max: the reads stay inside
+          // shared memory and the sums of missing samples are never stored
           const float* bp = reinterpret_cast<const float*>(sp + sd_box);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i < sd_ns) {
-              const float4 v = lds4(bp + i * 32 + ((sd_jq ^ i) << 2));  // row sd_s0 + i; (sd_s0 + i) & 7 == i
-              float x = sacc[i];
-              x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
-              sacc[i] = x;
-            }
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = lds4(bp + i * 32 + ((sd_jq ^ i) << 2));  // row sd_s0 + i; (sd_s0 + i) & 7 == i
+            float x = sacc[i];
+            x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
+            sacc[i] = x;
+          }
         }
         ip.next(NST);
         if (tid == 0) TRACE_AT(0, 13);
@@ -707,15 +707,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           if (cw_own) {
             const float* rowp = (cw_role == 0 ? hsb : gb) + 4 * cw_jq;
             const float* vecp = (cw_role == 0 ? sDC : sCtx) + s0 * D + 4 * cw_dq;
-            for (int s = 0; s < ns; ++s) {
-              const float4 hv = lds4(rowp + s * SH2);
-              const float4 vv = lds4(vecp + s * D);
-              const float hvv[4] = {hv.x, hv.y, hv.z, hv.w}, vvv[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
+            for (int s = 0; s < kBwdSampleItem; ++s)
+              if (s < ns) {
+                const float4 hv = lds4(rowp + s * SH2);
+                const float4 vv = lds4(vecp + s * D);
+                const float hvv[4] = {hv.x, hv.y, hv.z, hv.w}, vvv[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) cacc[i][e] = fmaf(hvv[i], vvv[e], cacc[i][e]);
-            }
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) cacc[i][e] = fmaf(hvv[i], vvv[e], cacc[i][e]);
+              }
           }
           named_sync(1, kComputeThreads);  // h_s2 rows no longer needed: d_h_s2 goes there
           {

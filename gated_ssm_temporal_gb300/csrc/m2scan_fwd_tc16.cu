@@ -284,7 +284,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     // C partial dots: thread = (sample quarter, state, column quad), 4 samples
     const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_s0 = 4 * (tid >> 7);
-    const int sd_ns = min(4, S_max - sd_s0);
     const int sd_box = a.off_S + sd_s0 * 128;
     const float* sd_w = sW_Ct + sd_d * SH2 + 4 * sd_jq;
     const int lo_off0 = row * 32 + (((2 * sub) ^ (row & 7)) << 2);
@@ -334,16 +333,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
         lr.next(kChunkRing);
         lf.next(kLoBufs);
         {
+          // all 4 rows even past S_max: the reads stay inside shared memory
+          // and the sums of missing samples are never stored
           const float* bp = reinterpret_cast<const float*>(sp + sd_box);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < sd_ns) {
-              const int s = sd_s0 + i;
-              const float4 v = lds4(bp + i * 32 + ((sd_jq ^ (s & 7)) << 2));
-              float x = sacc[i];
-              x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
-              sacc[i] = x;
-            }
+          for (int i = 0; i < 4; ++i) {
+            const float4 v = lds4(bp + i * 32 + ((sd_jq ^ (sd_s0 + i)) & 7) * 4);
+            float x = sacc[i];
+            x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
+            sacc[i] = x;
+          }
         }
         ip.next(NST);
         PROF_END(4);
