@@ -40,7 +40,7 @@
 namespace m2scan {
 namespace {
 
-constexpr int kComputeWarps = 16;
+constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kBwdThreads = kComputeThreads + 64;
 constexpr int kProducerWarp = kComputeWarps;
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   // rows into TMEM; every global load is issued before the first store
   constexpr int kWPer = (4096 + kBwdThreads - 1) / kBwdThreads;
   {
-    const int wsub = warp >> 2, wh = wsub & 1, wpart = wsub >> 1;
+    const int wh = warp >> 2;  // j-half of this compute warp's TMEM rows
     const int wj = 128 * wh + 32 * (warp & 3) + lane;
     float4 wr[8];
     if (warp < kComputeWarps) {
@@ -322,19 +322,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       for (int i = 0; i < NST && ptile < T; ++i) produce_one();
     if (warp < kComputeWarps) {
       // thread = TMEM lane = row j of [W_A|W_B] within its j-half
-      float v[32];
+      float hi[32], lo[32];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        v[4 * q] = wr[q].x; v[4 * q + 1] = wr[q].y; v[4 * q + 2] = wr[q].z; v[4 * q + 3] = wr[q].w;
-      }
+        const float v4[4] = {wr[q].x, wr[q].y, wr[q].z, wr[q].w};
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float hi = tf32_rn(v[k]);
-        v[k] = wpart == 0 ? hi : v[k] - hi;
+        for (int e = 0; e < 4; ++e) {
+          hi[4 * q + e] = tf32_rn(v4[e]);
+          lo[4 * q + e] = v4[e] - hi[4 * q + e];
+        }
       }
-      const uint32_t tw0 = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kColW + 64u * wh + 32u * wpart;
-      tmem_st16(tw0, v);
-      tmem_st16(tw0 + 16u, v + 16);
+      const uint32_t tw0 = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kColW + 64u * wh;
+      tmem_st16(tw0, hi);
+      tmem_st16(tw0 + 16u, hi + 16);
+      tmem_st16(tw0 + 32u, lo);
+      tmem_st16(tw0 + 48u, lo + 16);
     }
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
@@ -495,26 +497,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------- compute
+    // 8 warps, two per TMEM lane quadrant: sub = 0 / 1 selects the half of a
+    // row's columns (projections) or the j-half (transposed rows, d_h, dW).
     const int qd = warp & 3, sub = warp >> 2;
     const int row = 32 * qd + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-    // C / d_ctx partial dots: thread = (role, sample half, state, column quad);
-    // role 0 sums h_s2 . W_C, role 1 dY . W_O^T, for 8 samples at once
-    const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_sh = (tid >> 7) & 1, sd_role = tid >> 8;
-    const int sd_s0 = 8 * sd_sh;
-    const int sd_box = (sd_role == 0 ? a.off_S : a.off_G) + sd_s0 * 128;  // bytes from the stage
+    // C / d_ctx partial dots: thread = (role, state, column quad), all 16
+    // samples of a tile; role 0 sums h_s2 . W_C, role 1 dY . W_O^T
+    const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_role = tid >> 7;
+    const int sd_box = sd_role == 0 ? a.off_S : a.off_G;  // bytes from the stage
     const float* sd_w = sd_role == 0 ? sW_Ct + sd_d * SH2 + 4 * sd_jq : a.W_O + sd_d * SH2 + 4 * sd_jq;
-    // h of this thread in a chunk: its row, columns 8 sub .. 8 sub + 7
-    const int lo_off0 = row * 32 + (((2 * sub) ^ (row & 7)) << 2);
-    const int lo_off1 = row * 32 + (((2 * sub + 1) ^ (row & 7)) << 2);
-    // dW_C (role 0: h_s2 x dC) or dW_O (role 1: dY x ctx): 4 rows j x 4 states
-    const int cw_role = tid >> 8, cw_jq = tid & 63, cw_dq = (tid >> 6) & 3;
+    // h of this thread in a chunk: its row, columns 16 sub .. 16 sub + 15
+    int lo_off[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) lo_off[v] = row * 32 + (((4 * sub + v) ^ (row & 7)) << 2);
+    // dW_C (role 0: h_s2 x dC) or dW_O (role 1: dY x ctx): rows 4 jq .. 4 jq + 3
+    // x states 8 dh .. 8 dh + 7
+    const int cw_role = tid >> 7, cw_jq = tid & 63, cw_dh = (tid >> 6) & 1;
     const bool cw_own = 4 * cw_jq < SH2;
-    float cacc[4][4];
+    float cacc[4][8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) cacc[i][e] = 0.f;
+      for (int e = 0; e < 8; ++e) cacc[i][e] = 0.f;
+    // transposed rows and d_h: thread = row j of SH2 (TMEM lane), 16 rows
+    const int jrow = 128 * sub + row;
+    const bool jok = jrow < SH2;
     RingPos ip;  // stage of the next item
     RingPos lr;  // loready position of the next chunk
     RingPos lf;  // lofree position of the next chunk
@@ -524,36 +532,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
       const int R_t = S_t * K;
       const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
-      float sacc[8];
+      float sacc[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sacc[i] = 0.f;
+      for (int i = 0; i < 16; ++i) sacc[i] = 0.f;
       // the remainder buffers share TMEM with the previous tile's transposed
       // rows: wait until the dW MMAs of its last two row items are done
       if (ri >= 1) bounded_wait(&bb->htfree[(ri - 1) & 1], ((ri - 1) >> 1) & 1, a.err);
       if (ri >= 2) bounded_wait(&bb->htfree[ri & 1], ((ri - 2) >> 1) & 1, a.err);
       // ====================================================== pass 1 chunks
-      // Per chunk: h - trunc(h) (rounded to tf32) into its TMEM buffer, thread
-      // = row, 8 of the chunk's 32 columns per warp; the C / d_ctx dots run
-      // while that store lands, and the chunk is handed to the MMA warp at the
-      // top of the next iteration (or after the last chunk).
-      float4 wnext = sd_role == 0 ? lds4(sd_w) : __ldg(reinterpret_cast<const float4*>(sd_w));
+      // Per chunk: h - trunc(h) into its TMEM buffer; the C / d_ctx dots run
+      // while that store lands, and the chunk is handed to the MMA warp at
+      // the top of the next iteration (or after the last one).
       RingPos lr_prev = lr;
       for (int q = 0; q < NC; ++q, ++c) {
-        const float4 w = wnext;
-        if (q + 1 < NC)
-          wnext = sd_role == 0 ? lds4(sd_w + (q + 1) * kChunk)
-                               : __ldg(reinterpret_cast<const float4*>(sd_w + (q + 1) * kChunk));
+        const float4 w = sd_role == 0 ? lds4(sd_w + q * kChunk)
+                                      : __ldg(reinterpret_cast<const float4*>(sd_w + q * kChunk));
         if (tid == 0) TRACE_AT(0, 10);
         bounded_wait(&bb->full[ip.i], ip.ph, a.err);
         if (tid == 0) TRACE_AT(0, 11);
         const unsigned char* sp = stage_ptr(ip.i);
         const float* Hc = reinterpret_cast<const float*>(sp);
-        float lo[8];
-        {
-          const float4 x0 = lds4(Hc + lo_off0), x1 = lds4(Hc + lo_off1);
-          const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float lo[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) lo[i] = xv[i] - tf32_trunc(xv[i]);
+        for (int v = 0; v < 4; ++v) {
+          const float4 x = lds4(Hc + lo_off[v]);
+          lo[4 * v] = x.x - tf32_trunc(x.x);
+          lo[4 * v + 1] = x.y - tf32_trunc(x.y);
+          lo[4 * v + 2] = x.z - tf32_trunc(x.z);
+          lo[4 * v + 3] = x.w - tf32_trunc(x.w);
         }
         if (q > 0) {  // the previous chunk's remainder has landed: hand it over
           tmem_st_wait();
@@ -564,16 +570,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         }
         if (c >= kLoBufs) bounded_wait(&bb->lofree[lf.i], lf.ph ^ 1u, a.err);
         tc_fence_after();
-        tmem_st8(lane_base + kColLo + 32u * lf.i + 8u * sub, lo);
+        tmem_st16(lane_base + kColLo + 32u * lf.i + 16u * sub, lo);
         lr.next(kChunkRing);
         lf.next(kLoBufs);
         {
-          // all 8 rows of this half even past S_max: the reads stay inside
+          // all 16 rows of the box even past S_max: the reads stay inside
           // shared memory and the sums of missing samples are never stored
           const float* bp = reinterpret_cast<const float*>(sp + sd_box);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = lds4(bp + i * 32 + ((sd_jq ^ i) << 2));  // row sd_s0 + i; (sd_s0 + i) & 7 == i
+          for (int i = 0; i < 16; ++i) {
+            const float4 v = lds4(bp + i * 32 + ((sd_jq ^ (i & 7)) << 2));
             float x = sacc[i];
             x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
             sacc[i] = x;
@@ -587,7 +593,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 16; ++i) {
 #pragma unroll
         for (int m = 1; m < 8; m <<= 1) sacc[i] += __shfl_xor_sync(0xffffffffu, sacc[i], m);
       }
@@ -595,8 +601,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         float* dst = sd_role == 0 ? sC : sDctx;
         const float scale = sd_role == 0 ? 1.f : a.tw;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (sd_s0 + i < S_t) dst[(sd_s0 + i) * D + sd_d] = scale * sacc[i];
+        for (int i = 0; i < 16; ++i)
+          if (i < S_t) dst[i * D + sd_d] = scale * sacc[i];
       }
       // ==================================== projections: TMEM -> shared memory
       if (tid == 0) TRACE_AT(0, 20);
@@ -604,27 +610,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       if (tid == 0) TRACE_AT(0, 21);
       tc_fence_after();
       {
-        const int c0 = 8 * sub;  // columns c0 .. c0 + 7 of A|B
-        float v[8];
-        {
-          uint32_t r0[8], r1[8], r2[8], r3[8], r4[8];
-          tmem_ld8_nowait(lane_base + c0, r0);
-          tmem_ld8_nowait(lane_base + TD + c0, r1);
-          tmem_ld8_nowait(lane_base + 64u + c0, r2);
-          tmem_ld8_nowait(lane_base + 64u + TD + c0, r3);
-          tmem_ld8_nowait(lane_base + kColCorr + c0, r4);
-          tmem_ld_wait();
-          const bool odd = NC > 1;  // the odd-chunk sum exists
+        const int c0 = 16 * sub;  // columns c0 .. c0 + 15 of A|B
+        uint32_t r0[16], r1[16], r2[16], r3[16], r4[16];
+        tmem_ld16_nowait(lane_base + c0, r0);
+        tmem_ld16_nowait(lane_base + TD + c0, r1);
+        tmem_ld16_nowait(lane_base + 64u + c0, r2);
+        tmem_ld16_nowait(lane_base + 64u + TD + c0, r3);
+        tmem_ld16_nowait(lane_base + kColCorr + c0, r4);
+        tmem_ld_wait();
+        const bool odd = NC > 1;  // the odd-chunk sum exists
+        float v[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float m1 = odd ? __uint_as_float(r2[i]) : 0.f;
-            const float c1 = odd ? __uint_as_float(r3[i]) : 0.f;
-            v[i] = (__uint_as_float(r0[i]) + m1) +
-                   ((__uint_as_float(r1[i]) + c1) + __uint_as_float(r4[i]));
-          }
+        for (int i = 0; i < 16; ++i) {
+          const float m1 = odd ? __uint_as_float(r2[i]) : 0.f;
+          const float c1 = odd ? __uint_as_float(r3[i]) : 0.f;
+          v[i] = (__uint_as_float(r0[i]) + m1) + ((__uint_as_float(r1[i]) + c1) + __uint_as_float(r4[i]));
         }
-        sts4(sPh + sw128_idx(row, c0), make_float4(v[0], v[1], v[2], v[3]));
-        sts4(sPh + sw128_idx(row, c0 + 4), make_float4(v[4], v[5], v[6], v[7]));
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          sts4(sPh + sw128_idx(row, c0 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
       }
       tc_fence_before();
       named_sync(1, kComputeThreads);
@@ -689,9 +693,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       if (tid == 0) TRACE_AT(0, 24);
       // ======= sample items (dW_C, dW_O partial sums, d_h_s2) and 16-row items
       // (h^T into TMEM for dW, d_h_history rows out), in post_item order
-      const int hh = sub & 1, rg = sub >> 1;
-      const int jrow = 128 * hh + 32 * qd + lane;
-      const bool jok = jrow < SH2;
       for (int pi = 0; pi < NSI + NRI; ++pi) {
         int kind, k;
         post_item(pi, NSI, NRI, kind, k);
@@ -706,39 +707,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           const int s0 = k * kBwdSampleItem, ns = min(kBwdSampleItem, S_t - s0);
           if (cw_own) {
             const float* rowp = (cw_role == 0 ? hsb : gb) + 4 * cw_jq;
-            const float* vecp = (cw_role == 0 ? sDC : sCtx) + s0 * D + 4 * cw_dq;
+            const float* vecp = (cw_role == 0 ? sDC : sCtx) + s0 * D + 8 * cw_dh;
 #pragma unroll
             for (int s = 0; s < kBwdSampleItem; ++s)
               if (s < ns) {
                 const float4 hv = lds4(rowp + s * SH2);
-                const float4 vv = lds4(vecp + s * D);
-                const float hvv[4] = {hv.x, hv.y, hv.z, hv.w}, vvv[4] = {vv.x, vv.y, vv.z, vv.w};
+                const float4 v0 = lds4(vecp + s * D), v1 = lds4(vecp + s * D + 4);
+                const float hvv[4] = {hv.x, hv.y, hv.z, hv.w};
+                const float vvv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) cacc[i][e] = fmaf(hvv[i], vvv[e], cacc[i][e]);
+                  for (int e = 0; e < 8; ++e) cacc[i][e] = fmaf(hvv[i], vvv[e], cacc[i][e]);
               }
           }
           named_sync(1, kComputeThreads);  // h_s2 rows no longer needed: d_h_s2 goes there
           {
-            const int jq = tid & 63, s = tid >> 6;
-            if (s < ns && 4 * jq < SH2) {
-              float4 o = lds4(gb + s * SH2 + 4 * jq);
-              const float* dcr = sDC + (s0 + s) * D;
+            // two samples sq, sq + 4 per thread: each W_C^T element serves both
+            const int jq = tid & 63, sq = tid >> 6;
+            if (sq < ns && 4 * jq < SH2) {
+              const bool two = sq + 4 < ns;
+              float4 o0 = lds4(gb + sq * SH2 + 4 * jq);
+              float4 o1 = two ? lds4(gb + (sq + 4) * SH2 + 4 * jq) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float* dc0 = sDC + (s0 + sq) * D;
+              const float* dc1 = sDC + (s0 + (two ? sq + 4 : sq)) * D;
 #pragma unroll
               for (int dq = 0; dq < 4; ++dq) {
-                const float4 dcv = lds4(dcr + 4 * dq);
-                const float dv[4] = {dcv.x, dcv.y, dcv.z, dcv.w};
+                const float4 a0 = lds4(dc0 + 4 * dq), a1 = lds4(dc1 + 4 * dq);
+                const float d0[4] = {a0.x, a0.y, a0.z, a0.w}, d1[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  const float4 w = lds4(sW_Ct + (4 * dq + e) * SH2 + 4 * jq);
-                  o.x = fmaf(dv[e], w.x, o.x);
-                  o.y = fmaf(dv[e], w.y, o.y);
-                  o.z = fmaf(dv[e], w.z, o.z);
-                  o.w = fmaf(dv[e], w.w, o.w);
+                  const float4 wv = lds4(sW_Ct + (4 * dq + e) * SH2 + 4 * jq);
+                  o0.x = fmaf(d0[e], wv.x, o0.x); o0.y = fmaf(d0[e], wv.y, o0.y);
+                  o0.z = fmaf(d0[e], wv.z, o0.z); o0.w = fmaf(d0[e], wv.w, o0.w);
+                  o1.x = fmaf(d1[e], wv.x, o1.x); o1.y = fmaf(d1[e], wv.y, o1.y);
+                  o1.z = fmaf(d1[e], wv.z, o1.z); o1.w = fmaf(d1[e], wv.w, o1.w);
                 }
               }
-              sts4(hsb + s * SH2 + 4 * jq, o);
+              sts4(hsb + sq * SH2 + 4 * jq, o0);
+              if (two) sts4(hsb + (sq + 4) * SH2 + 4 * jq, o1);
             }
           }
           fence_proxy_async_smem();
@@ -751,27 +758,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           if (tid == 0) TRACE_AT(0, 41);
           float* hb = stg;
           const int r0 = k * kRowItem, nr = min(kRowItem, R_t - r0);
+          const bool full_item = nr == kRowItem && jok;
           if (ri >= 2) bounded_wait(&bb->htfree[ri & 1], ((ri - 2) >> 1) & 1, a.err);
           tc_fence_after();
           {
-            float raw[8], lo[8];
+            // this thread's column j of the 16 rows: h and h - trunc(h)
+            float raw[16], lo[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = 8 * rg + i;
-              const float x = (r < nr && jok) ? hb[r * SH2 + jrow] : 0.f;
-              raw[i] = x;
-              lo[i] = x - tf32_trunc(x);
+            for (int r = 0; r < 16; ++r) {
+              const float x = (full_item || (r < nr && jok)) ? hb[r * SH2 + jrow] : 0.f;
+              raw[r] = x;
+              lo[r] = x - tf32_trunc(x);
             }
-            const uint32_t tb = lane_base + kColHT + 64u * (ri & 1) + 32u * hh + 8u * rg;
-            tmem_st8(tb, raw);
-            tmem_st8(tb + 16u, lo);
+            const uint32_t tb = lane_base + kColHT + 64u * (ri & 1) + 32u * sub;
+            tmem_st16(tb, raw);
+            tmem_st16(tb + 16u, lo);
           }
           {  // dA|dB of these rows, transposed: [hi 32 | lo 32] x 16 rows; zero past the tile
-            const int m = tid >> 3, rr = 2 * (tid & 7);
+            const int m = tid >> 2, rr = 4 * (tid & 3);
             const float* src = m < TD ? sPh : sPl;
             const int col = m & (TD - 1);
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
+            for (int v = 0; v < 4; ++v) {
               const int r = rr + v;
               sDT[sw128_idx(m, 16 * (ri & 1) + r)] = r < nr ? src[sw128_idx(r0 + r, col)] : 0.f;
             }
@@ -790,12 +798,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           tc_fence_after();
           named_sync(1, kComputeThreads);  // every read of the h rows done
           {
-            float v[8];
-            tmem_ld<8>(lane_base + 64u * hh + 16u * (k & 3) + 8u * rg, v);
+            float v[16];
+            tmem_ld<16>(lane_base + 64u * sub + 16u * (k & 3), v);
+            if (full_item) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = 8 * rg + i;
-              if (r < nr && jok) hb[r * SH2 + jrow] = v[i];
+              for (int r = 0; r < 16; ++r) hb[r * SH2 + jrow] = v[r];
+            } else {
+#pragma unroll
+              for (int r = 0; r < 16; ++r)
+                if (r < nr && jok) hb[r * SH2 + jrow] = v[r];
             }
           }
           const bool last_of_half = (k & 3) == 3 || k == NRI - 1;
@@ -819,17 +830,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     bounded_wait(&bb->dwdone, 0, a.err);
     tc_fence_after();
     {
-      const int h = sub & 1, cp = sub >> 1;  // cp 0: dW_A row, 1: dW_B row
-      const int j = 128 * h + 32 * qd + lane;
+      // row j of dW_A and dW_B: main sums (columns k) plus corrections (32 + k)
       float m[16], r[16];
-      tmem_ld<16>(lane_base + kColDW + 64u * h + 16u * cp, m);
-      tmem_ld<16>(lane_base + kColDW + 64u * h + TD + 16u * cp, r);
-      if (j < SH2) {
-        float4* dst = reinterpret_cast<float4*>(slot + cp * n + j * D);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_float4(m[4 * i] + r[4 * i], m[4 * i + 1] + r[4 * i + 1], m[4 * i + 2] + r[4 * i + 2],
-                               m[4 * i + 3] + r[4 * i + 3]);
+      for (int cp = 0; cp < 2; ++cp) {
+        tmem_ld<16>(lane_base + kColDW + 64u * sub + 16u * cp, m);
+        tmem_ld<16>(lane_base + kColDW + 64u * sub + TD + 16u * cp, r);
+        if (jok) {
+          float4* dst = reinterpret_cast<float4*>(slot + cp * n + jrow * D);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(m[4 * i] + r[4 * i], m[4 * i + 1] + r[4 * i + 1], m[4 * i + 2] + r[4 * i + 2],
+                                 m[4 * i + 3] + r[4 * i + 3]);
+        }
       }
     }
     if (cw_own) {
@@ -837,11 +850,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       for (int i = 0; i < 4; ++i) {
         const int j = 4 * cw_jq + i;
         if (cw_role == 0) {
-          *reinterpret_cast<float4*>(slot + 2 * n + j * D + 4 * cw_dq) =
-              make_float4(cacc[i][0], cacc[i][1], cacc[i][2], cacc[i][3]);
+          float4* dst = reinterpret_cast<float4*>(slot + 2 * n + j * D + 8 * cw_dh);
+          dst[0] = make_float4(cacc[i][0], cacc[i][1], cacc[i][2], cacc[i][3]);
+          dst[1] = make_float4(cacc[i][4], cacc[i][5], cacc[i][6], cacc[i][7]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) slot[3 * n + (4 * cw_dq + e) * SH2 + j] = a.tw * cacc[i][e];
+          for (int e = 0; e < 8; ++e) slot[3 * n + (8 * cw_dh + e) * SH2 + j] = a.tw * cacc[i][e];
         }
       }
     }
