@@ -25,7 +25,7 @@
 namespace m2scan {
 namespace {
 
-constexpr int kComputeWarps = 16;
+constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kFwdThreads = kComputeThreads + 64;
 constexpr int kProducerWarp = kComputeWarps;
@@ -279,40 +279,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     }
   } else {
     // ------------------------------------------------------------- compute
+    // 8 warps, two per TMEM lane quadrant: sub = 0 / 1 selects the half of a
+    // row's columns
     const int qd = warp & 3, sub = warp >> 2;
     const int row = 32 * qd + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-    // C partial dots: thread = (sample quarter, state, column quad), 4 samples
-    const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_s0 = 4 * (tid >> 7);
+    // C partial dots: thread = (sample half, state, column quad), 8 samples
+    const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_s0 = 8 * (tid >> 7);
     const int sd_box = a.off_S + sd_s0 * 128;
     const float* sd_w = sW_Ct + sd_d * SH2 + 4 * sd_jq;
-    const int lo_off0 = row * 32 + (((2 * sub) ^ (row & 7)) << 2);
-    const int lo_off1 = row * 32 + (((2 * sub + 1) ^ (row & 7)) << 2);
+    int lo_off[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) lo_off[v] = row * 32 + (((4 * sub + v) ^ (row & 7)) << 2);
     RingPos ip, lr, lf;
     int c = 0;
     PROF_DECL;
     for (int t = 0; t < T; ++t) {
       const long long tb0 = tile_start(t);
       const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sacc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sacc[i] = 0.f;
       // ====================================================== pass 1 chunks
-      float4 wnext = lds4(sd_w);
       RingPos lr_prev = lr;
       for (int q = 0; q < NC; ++q, ++c) {
-        const float4 w = wnext;
-        if (q + 1 < NC) wnext = lds4(sd_w + (q + 1) * kChunk);
+        const float4 w = lds4(sd_w + q * kChunk);
         PROF_BEGIN();
         bounded_wait(&bb->full[ip.i], ip.ph, a.err);
         PROF_END(0);
         PROF_BEGIN();
         const unsigned char* sp = stage_ptr(ip.i);
         const float* Hc = reinterpret_cast<const float*>(sp);
-        float lo[8];
-        {
-          const float4 x0 = lds4(Hc + lo_off0), x1 = lds4(Hc + lo_off1);
-          const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float lo[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) lo[i] = xv[i] - tf32_trunc(xv[i]);
+        for (int v = 0; v < 4; ++v) {
+          const float4 x = lds4(Hc + lo_off[v]);
+          lo[4 * v] = x.x - tf32_trunc(x.x);
+          lo[4 * v + 1] = x.y - tf32_trunc(x.y);
+          lo[4 * v + 2] = x.z - tf32_trunc(x.z);
+          lo[4 * v + 3] = x.w - tf32_trunc(x.w);
         }
         PROF_END(1);
         if (q > 0) {  // the previous chunk's remainder has landed: hand it over
@@ -329,16 +334,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
         PROF_END(3);
         PROF_BEGIN();
         tc_fence_after();
-        tmem_st8(lane_base + kColLo + 32u * lf.i + 8u * sub, lo);
+        tmem_st16(lane_base + kColLo + 32u * lf.i + 16u * sub, lo);
         lr.next(kChunkRing);
         lf.next(kLoBufs);
         {
-          // all 4 rows even past S_max: the reads stay inside shared memory
-          // and the sums of missing samples are never stored
+          // all 8 rows of this half even past S_max: the reads stay inside
+          // shared memory and the sums of missing samples are never stored
           const float* bp = reinterpret_cast<const float*>(sp + sd_box);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 v = lds4(bp + i * 32 + ((sd_jq ^ (sd_s0 + i)) & 7) * 4);
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = lds4(bp + i * 32 + ((sd_jq ^ i) << 2));  // row sd_s0 + i; (sd_s0 + i) & 7 == i
             float x = sacc[i];
             x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
             sacc[i] = x;
@@ -353,13 +358,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
 #pragma unroll
         for (int m = 1; m < 8; m <<= 1) sacc[i] += __shfl_xor_sync(0xffffffffu, sacc[i], m);
       }
       if (sd_jq == 0) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
           if (sd_s0 + i < S_t) sC[(sd_s0 + i) * D + sd_d] = sacc[i];
       }
       PROF_END(5);
@@ -370,24 +375,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       PROF_BEGIN();
       tc_fence_after();
       {
-        const int c0 = 8 * sub;  // columns c0 .. c0 + 7 of A|B
-        uint32_t r0[8], r1[8], r2[8], r3[8], r4[8];
-        tmem_ld8_nowait(lane_base + c0, r0);
-        tmem_ld8_nowait(lane_base + TD + c0, r1);
-        tmem_ld8_nowait(lane_base + 64u + c0, r2);
-        tmem_ld8_nowait(lane_base + 64u + TD + c0, r3);
-        tmem_ld8_nowait(lane_base + kColCorr + c0, r4);
+        const int c0 = 16 * sub;  // columns c0 .. c0 + 15 of A|B
+        uint32_t r0[16], r1[16], r2[16], r3[16], r4[16];
+        tmem_ld16_nowait(lane_base + c0, r0);
+        tmem_ld16_nowait(lane_base + TD + c0, r1);
+        tmem_ld16_nowait(lane_base + 64u + c0, r2);
+        tmem_ld16_nowait(lane_base + 64u + TD + c0, r3);
+        tmem_ld16_nowait(lane_base + kColCorr + c0, r4);
         tmem_ld_wait();
         const bool odd = NC > 1;  // the odd-chunk sum exists
-        float v[8];
+        float v[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const float m1 = odd ? __uint_as_float(r2[i]) : 0.f;
           const float c1 = odd ? __uint_as_float(r3[i]) : 0.f;
           v[i] = (__uint_as_float(r0[i]) + m1) + ((__uint_as_float(r1[i]) + c1) + __uint_as_float(r4[i]));
         }
-        sts4(sP + sw128_idx(row, c0), make_float4(v[0], v[1], v[2], v[3]));
-        sts4(sP + sw128_idx(row, c0 + 4), make_float4(v[4], v[5], v[6], v[7]));
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          sts4(sP + sw128_idx(row, c0 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
       }
       tc_fence_before();
       named_sync(1, kComputeThreads);
@@ -427,34 +433,44 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
         float* hs = reinterpret_cast<float*>(stage_ptr(ip.i));
         const int st = ip.i;
         ip.next(NST);
-        const int s = warp;  // one sample per warp, 4 columns x 2 per thread
-        if (s < S_t) {
-          const float* cr = sCtx + s * D;
-          float cx[D];
+        // thread = 4 columns x samples sq, sq + 4, sq + 8, sq + 12: each W_O
+        // element serves four samples
+        const int jq = tid & 63, sq = tid >> 6;
+        if (4 * jq < SH2) {
+          float4 o[4];
 #pragma unroll
-          for (int q = 0; q < D / 4; ++q) {
-            const float4 v = lds4(cr + 4 * q);
-            cx[4 * q] = v.x; cx[4 * q + 1] = v.y; cx[4 * q + 2] = v.z; cx[4 * q + 3] = v.w;
+          for (int u = 0; u < 4; ++u) o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int dq = 0; dq < D / 4; ++dq) {
+            float cx[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int s = min(sq + 4 * u, S_max - 1);
+              const float4 cv = lds4(sCtx + s * D + 4 * dq);
+              cx[u][0] = cv.x; cx[u][1] = cv.y; cx[u][2] = cv.z; cx[u][3] = cv.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float4 wv = lds4(sW_O + (4 * dq + e) * SH2 + 4 * jq);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                o[u].x = fmaf(cx[u][e], wv.x, o[u].x);
+                o[u].y = fmaf(cx[u][e], wv.y, o[u].y);
+                o[u].z = fmaf(cx[u][e], wv.z, o[u].z);
+                o[u].w = fmaf(cx[u][e], wv.w, o[u].w);
+              }
+            }
           }
 #pragma unroll
-          for (int hv = 0; hv < 2; ++hv) {
-            const int jq = lane + 32 * hv;
-            if (4 * jq < SH2) {
-              float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-              for (int d = 0; d < D; ++d) {
-                const float4 w = lds4(sW_O + d * SH2 + 4 * jq);
-                o.x = fmaf(cx[d], w.x, o.x);
-                o.y = fmaf(cx[d], w.y, o.y);
-                o.z = fmaf(cx[d], w.z, o.z);
-                o.w = fmaf(cx[d], w.w, o.w);
-              }
+          for (int u = 0; u < 4; ++u) {
+            const int s = sq + 4 * u;
+            if (s < S_t) {
               float* hp = hs + s * SH2 + 4 * jq;
               float4 h = lds4(hp);
-              h.x = fmaf(a.tw, o.x, h.x);
-              h.y = fmaf(a.tw, o.y, h.y);
-              h.z = fmaf(a.tw, o.z, h.z);
-              h.w = fmaf(a.tw, o.w, h.w);
+              h.x = fmaf(a.tw, o[u].x, h.x);
+              h.y = fmaf(a.tw, o[u].y, h.y);
+              h.z = fmaf(a.tw, o[u].z, h.z);
+              h.w = fmaf(a.tw, o[u].w, h.w);
               sts4(hp, h);
             }
           }
@@ -479,7 +495,7 @@ int round_up_f(int x, int m) { return (x + m - 1) / m * m; }
 bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a) {
   if (!fast_path_ok(K, SH2, D) || D != 16) return false;
   int S_max = kTileRows / K;
-  if (S_max > 16) S_max = 16;  // the dots cover four quarters of 4 samples, the output one sample per warp
+  if (S_max > 16) S_max = 16;  // the dots cover two halves of 8 samples, the output four groups of 4
   const int hc = S_max * K * 128, sc = S_max * 128;
   const int off_S = round_up_f(hc, 1024);
   int stage = off_S + sc;
