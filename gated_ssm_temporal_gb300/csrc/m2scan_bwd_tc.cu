@@ -634,58 +634,112 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       named_sync(1, kComputeThreads);
       if (tid == 0) TRACE_AT(0, 22);
       // ================================ scan and reverse scan per (sample, state)
-      if (tid < S_t * D) {
+      if (tid < S_t * D && (K & 7) == 0) {
+        // K a multiple of 8: every group of 8 rows starts at a swizzle phase
+        // of 0, so the offsets of this thread's two columns within a group
+        // are the same for every group
         const int s = tid >> 4, d = tid & 15, rb = s * K;
+        int oa[8], ob[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          oa[u] = u * 32 + ((((d >> 2)) ^ u) << 2) + (d & 3);
+          ob[u] = u * 32 + (((4 + (d >> 2)) ^ u) << 2) + (d & 3);
+        }
         float x = 0.f;
-        for (int k0 = 0; k0 < K; k0 += 8) {  // replay: B_t is replaced by x_t
-          const int n = min(8, K - k0);
+        for (int g = 0; g < K; g += 8) {  // replay: B_t is replaced by x_t
+          float* pg = sPh + (rb + g) * 32;
           float av[8], bv[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (u < n) {
-              av[u] = sPh[sw128_idx(rb + k0 + u, d)];
-              bv[u] = sPh[sw128_idx(rb + k0 + u, D + d)];
-            }
+          for (int u = 0; u < 8; ++u) {
+            av[u] = pg[oa[u]];
+            bv[u] = pg[ob[u]];
+          }
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (u < n) av[u] = sigmoid_fast(av[u]);
+          for (int u = 0; u < 8; ++u) av[u] = sigmoid_fast(av[u]);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (u < n) {
-              x = fmaf(av[u], x, bv[u]);
-              sPh[sw128_idx(rb + k0 + u, D + d)] = x;
-            }
+          for (int u = 0; u < 8; ++u) {
+            x = fmaf(av[u], x, bv[u]);
+            pg[ob[u]] = x;
+          }
         }
         const float Cv = sC[s * D + d], dctx = sDctx[s * D + d];
         sCtx[s * D + d] = Cv * x;
         sDC[s * D + d] = dctx * x;
         float dx = dctx * Cv;
-        for (int k1 = K; k1 > 0; k1 -= 8) {
-          const int k0 = k1 > 8 ? k1 - 8 : 0, n = k1 - k0;
+        for (int g = K - 8; g >= 0; g -= 8) {
+          float* pg = sPh + (rb + g) * 32;
+          float* lg = sPl + (rb + g) * 32;
           float av[8], xp[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (u < n) {
-              const int r = rb + k0 + u;
-              av[u] = sPh[sw128_idx(r, d)];
-              xp[u] = (k0 + u > 0) ? sPh[sw128_idx(r - 1, D + d)] : 0.f;
-            }
+          for (int u = 0; u < 8; ++u) av[u] = pg[oa[u]];
+          xp[0] = g > 0 ? pg[ob[7] - 256] : 0.f;  // x of the last row of the previous group
 #pragma unroll
-          for (int u = 7; u >= 0; --u)
-            if (u < n) {
-              const int r = rb + k0 + u;
-              float sg, dsg;
-              sigmoid_and_slope(av[u], sg, dsg);
-              const float dB = dx, dA = dx * xp[u] * dsg;
-              dx *= sg;
-              const float ah = tf32_rn(dA), bh = tf32_rn(dB);
-              const float al = dA - ah, bl = dB - bh;
-              sPh[sw128_idx(r, d)] = ah;
-              sPh[sw128_idx(r, D + d)] = bh;
-              sPl[sw128_idx(r, d)] = al;
-              sPl[sw128_idx(r, D + d)] = bl;
-            }
+          for (int u = 1; u < 8; ++u) xp[u] = pg[ob[u - 1]];
+#pragma unroll
+          for (int u = 7; u >= 0; --u) {
+            float sg, dsg;
+            sigmoid_and_slope(av[u], sg, dsg);
+            const float dB = dx, dA = dx * xp[u] * dsg;
+            dx *= sg;
+            const float ah = tf32_rn(dA), bh = tf32_rn(dB);
+            pg[oa[u]] = ah;
+            pg[ob[u]] = bh;
+            lg[oa[u]] = dA - ah;
+            lg[ob[u]] = dB - bh;
+          }
         }
+      } else if (tid < S_t * D) {
+          const int s = tid >> 4, d = tid & 15, rb = s * K;
+          float x = 0.f;
+          for (int k0 = 0; k0 < K; k0 += 8) {  // replay: B_t is replaced by x_t
+            const int n = min(8, K - k0);
+            float av[8], bv[8];
+  #pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (u < n) {
+                av[u] = sPh[sw128_idx(rb + k0 + u, d)];
+                bv[u] = sPh[sw128_idx(rb + k0 + u, D + d)];
+              }
+  #pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (u < n) av[u] = sigmoid_fast(av[u]);
+  #pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (u < n) {
+                x = fmaf(av[u], x, bv[u]);
+                sPh[sw128_idx(rb + k0 + u, D + d)] = x;
+              }
+          }
+          const float Cv = sC[s * D + d], dctx = sDctx[s * D + d];
+          sCtx[s * D + d] = Cv * x;
+          sDC[s * D + d] = dctx * x;
+          float dx = dctx * Cv;
+          for (int k1 = K; k1 > 0; k1 -= 8) {
+            const int k0 = k1 > 8 ? k1 - 8 : 0, n = k1 - k0;
+            float av[8], xp[8];
+  #pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (u < n) {
+                const int r = rb + k0 + u;
+                av[u] = sPh[sw128_idx(r, d)];
+                xp[u] = (k0 + u > 0) ? sPh[sw128_idx(r - 1, D + d)] : 0.f;
+              }
+  #pragma unroll
+            for (int u = 7; u >= 0; --u)
+              if (u < n) {
+                const int r = rb + k0 + u;
+                float sg, dsg;
+                sigmoid_and_slope(av[u], sg, dsg);
+                const float dB = dx, dA = dx * xp[u] * dsg;
+                dx *= sg;
+                const float ah = tf32_rn(dA), bh = tf32_rn(dB);
+                const float al = dA - ah, bl = dB - bh;
+                sPh[sw128_idx(r, d)] = ah;
+                sPh[sw128_idx(r, D + d)] = bh;
+                sPl[sw128_idx(r, d)] = al;
+                sPl[sw128_idx(r, D + d)] = bl;
+              }
+          }
       }
       fence_proxy_async_smem();
       named_sync(1, kComputeThreads);
