@@ -40,16 +40,20 @@ struct FwdBars {
   uint64_t loready[kChunkRing];  // compute -> MMA: chunk read, h - trunc(h) in TMEM
   uint64_t lofree[kLoBufs];      // MMA -> compute: remainder buffer consumed
   uint64_t accfull;              // MMA -> compute: projections of the tile done
-  uint64_t accempty;             // compute -> MMA: projections read back
+  uint64_t accempty[2];          // compute -> MMA: projections of accumulator set s read back
   uint32_t tslot;
   uint32_t pad;
 };
 
-// TMEM columns: [0, 128) trunc(h) . [W_hi | W_lo] of the even and of the odd
-// chunks; [128, 224) three buffers of h - trunc(h); [224, 256)
-// (h - trunc h) . W_hi.
+// TMEM columns: two accumulator sets, tile t using set t & 1 at 256 (t & 1),
+// so that the MMA warp starts the next tile's products while the compute
+// warps still read back, scan and write out this one. Within a set: [0, 128)
+// trunc(h) . [W_hi | W_lo] of the even and of the odd chunks, [224, 256)
+// (h - trunc h) . W_hi. [128, 224): three buffers of h - trunc(h), shared
+// by both sets.
 constexpr uint32_t kColLo = 128;
 constexpr uint32_t kColCorr = 224;
+constexpr uint32_t kSetCols = 256;
 
 struct RingPos {
   int i = 0;
@@ -123,10 +127,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
     for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
     mbar_init(&bb->accfull, 1);
-    mbar_init(&bb->accempty, 1);
+    mbar_init(&bb->accempty[0], 1);
+    mbar_init(&bb->accempty[1], 1);
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(&bb->tslot, 256);
+  if (warp == kMmaWarp) tmem_alloc(&bb->tslot, 2 * kSetCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -231,11 +236,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       const uint32_t w0 = smem_addr(sW);
       RingPos tp, lr, lf;
       for (int t = 0; t < T; ++t) {
-        if (t > 0) bounded_wait(&bb->accempty, (t - 1) & 1, a.err);
+        // the set's previous tile (t - 2) has been read back
+        if (t >= 2) bounded_wait(&bb->accempty[t & 1], ((t - 2) >> 1) & 1, a.err);
         tc_fence_after();
+        const uint32_t acc = tmem + kSetCols * static_cast<uint32_t>(t & 1);
         // remainder products of a chunk as soon as it is written, else main
-        // products of the next landed chunk (at most two ahead); each kind in
-        // chunk order into its own accumulator. descriptor + 2 u = 32 u bytes on.
+        // products of the next landed chunk; each kind in chunk order into its
+        // own accumulator. descriptor + 2 u = 32 u bytes on.
         RingPos pm = tp, pc = tp;
         int qm = 0, qc = 0;
         IdleClock clk;
@@ -248,7 +255,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
             const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_tf32_ta(tmem + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
+              umma_tf32_ta(acc + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
             umma_commit(&bb->lofree[lf.i]);
             lr.next(kChunkRing);
             lf.next(kLoBufs);
@@ -256,13 +263,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
             ++qc;
             did = true;
           }
-          if (!did && qm < NC && qm < qc + 2 && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
+          if (!did && qm < NC && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
             tc_fence_after();
             const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
             const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_tf32(tmem + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
+              umma_tf32(acc + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
             umma_commit(&bb->empty[pm.i]);  // first of the stage's two arrivals
             pm.next(NST);
             ++qm;
@@ -376,12 +383,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       tc_fence_after();
       {
         const int c0 = 16 * sub;  // columns c0 .. c0 + 15 of A|B
+        const uint32_t tc0 = lane_base + kSetCols * static_cast<uint32_t>(t & 1) + c0;
         uint32_t r0[16], r1[16], r2[16], r3[16], r4[16];
-        tmem_ld16_nowait(lane_base + c0, r0);
-        tmem_ld16_nowait(lane_base + TD + c0, r1);
-        tmem_ld16_nowait(lane_base + 64u + c0, r2);
-        tmem_ld16_nowait(lane_base + 64u + TD + c0, r3);
-        tmem_ld16_nowait(lane_base + kColCorr + c0, r4);
+        tmem_ld16_nowait(tc0, r0);
+        tmem_ld16_nowait(tc0 + TD, r1);
+        tmem_ld16_nowait(tc0 + 64u, r2);
+        tmem_ld16_nowait(tc0 + 64u + TD, r3);
+        tmem_ld16_nowait(tc0 + kColCorr, r4);
         tmem_ld_wait();
         const bool odd = NC > 1;  // the odd-chunk sum exists
         float v[16];
@@ -397,7 +405,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       }
       tc_fence_before();
       named_sync(1, kComputeThreads);
-      if (tid == 0) mbar_arrive(&bb->accempty);
+      if (tid == 0) mbar_arrive(&bb->accempty[t & 1]);
       PROF_END(7);
       PROF_BEGIN();
       // ============================== scan: one thread per (sample, state)
@@ -510,7 +518,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, 256);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 2 * kSetCols);
 }
 
 int round_up_f(int x, int m) { return (x + m - 1) / m * m; }
@@ -554,7 +562,7 @@ bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a) {
   a->SH2 = SH2;
   a->n_stages = n_stages;
   a->tc = 2;
-  a->tmem_cols = 256;
+  a->tmem_cols = 512;
   return a->smem_bytes <= 227 * 1024;
 }
 
