@@ -31,15 +31,13 @@ constexpr int kFwdThreads = kComputeThreads + 64;
 constexpr int kProducerWarp = kComputeWarps;
 constexpr int kMmaWarp = kComputeWarps + 1;
 constexpr int kChunkRing = 6;
-constexpr uint32_t kEmptyArrivals = 2;
 constexpr int kLoBufs = 3;
 
 struct FwdBars {
   uint64_t full[kMaxStages];     // producer -> all: stage loaded
-  uint64_t empty[kMaxStages];    // stage free: two arrivals
-  uint64_t loready[kChunkRing];  // compute -> MMA: chunk read, h - trunc(h) in TMEM
-  uint64_t lofree[kLoBufs];      // MMA -> compute: remainder buffer consumed
-  uint64_t accfull;              // MMA -> compute: projections of the tile done
+  uint64_t outdone[kMaxStages];  // compute -> producer: output written over the h_s2 item in stage s
+  uint64_t loready[kChunkRing];  // compute -> MMA: chunk c read, h - trunc(h) in TMEM
+  uint64_t cdone[kChunkRing];    // MMA -> all: every product of chunk c (and before) done
   uint64_t accempty[2];          // compute -> MMA: projections of accumulator set s read back
   uint32_t tslot;
   uint32_t pad;
@@ -104,6 +102,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, SH2 = a.SH2, S_max = a.S_max, NST = a.n_stages;
+  int trace_n = 0;
+  (void)trace_n;
   const uint32_t stage_bytes = static_cast<uint32_t>(a.stage_bytes);
   const int NC = SH2 / kChunk;
   const long long B = a.B;
@@ -122,11 +122,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_hs)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
-      mbar_init(&bb->empty[s], kEmptyArrivals);
     }
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
-    for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
-    mbar_init(&bb->accfull, 1);
+    for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->cdone[s], 1);
+    for (int s = 0; s < NST; ++s) mbar_init(&bb->outdone[s], 1);
     mbar_init(&bb->accempty[0], 1);
     mbar_init(&bb->accempty[1], 1);
     fence_barrier_init();
@@ -137,48 +136,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = bb->tslot;
 
-  // ---- producer: per tile NC chunks, then one item of the tile's h_s2 rows
-  // (h_enriched is written over them; the producer stores it before it reuses
-  // the stage)
-  RingPos lp, rp;
-  int pn = 0, ptile = 0, pit = 0;
-  int rn = 0, rtile = 0, rit = 0;
+  // ---- producer: in round u = 0 .. T the NC chunks of tile u (u < T), then
+  // the item of tile u - 1's h_s2 rows (u >= 1): the compute warps write the
+  // output of a tile over its h_s2 rows after the next tile's chunks, and the
+  // producer stores it before it reuses the stage
+  RingPos lp, rp, rcd;  // rcd: cdone position of the next chunk to release
+  uint32_t rout = 0;    // bit s: parity of the next outdone[s] phase (h_s2 items only)
+  int pn = 0, pround = 0, pit = 0;
+  int rn = 0, rround = 0, rit = 0;
+  auto round_items = [&](int u) { return (u < T ? NC : 0) + (u >= 1 ? 1 : 0); };
   auto release_one = [&]() {
-    bounded_wait(&bb->empty[rp.i], rp.ph, a.err);
-    if (rit == NC) {
-      const long long tb0 = tile_start(rtile);
-      const int S_t = static_cast<int>(tile_start(rtile + 1) - tb0);
+    if (rit < (rround < T ? NC : 0)) {
+      // a chunk: free once its products are done (they follow the compute
+      // warps' read of it)
+      bounded_wait(&bb->cdone[rcd.i], rcd.ph, a.err);
+      rcd.next(kChunkRing);
+    } else {
+      bounded_wait(&bb->outdone[rp.i], (rout >> rp.i) & 1u, a.err);
+      rout ^= 1u << rp.i;
+      const long long tb0 = tile_start(rround - 1);
+      const int S_t = static_cast<int>(tile_start(rround) - tb0);
       bulk_store(a.out0 + tb0 * SH2, stage_ptr(rp.i), static_cast<uint32_t>(S_t) * SH2 * 4u);
       bulk_commit();
       bulk_wait_read_all();
     }
     rp.next(NST);
     ++rn;
-    if (++rit == NC + 1) {
+    if (++rit == round_items(rround)) {
       rit = 0;
-      ++rtile;
+      ++rround;
     }
   };
   auto produce_one = [&]() {
-    const long long tb0 = tile_start(ptile);
-    const int S_t = static_cast<int>(tile_start(ptile + 1) - tb0);
     if (pn >= NST) release_one();
     unsigned char* sp = stage_ptr(lp.i);
     uint64_t* bar = &bb->full[lp.i];
-    if (pit < NC) {
+    if (pit < (pround < T ? NC : 0)) {
+      const long long tb0 = tile_start(pround);
       mbar_arrive_expect_tx(bar, a.hc_bytes + a.sc_bytes);
       tma_load_3d(sp, &a.tm_h, pit * kChunk, 0, static_cast<int>(tb0), bar);
       tma_load_2d(sp + a.off_S, &a.tm_hs, pit * kChunk, static_cast<int>(tb0), bar);
     } else {
+      const long long tb0 = tile_start(pround - 1);
+      const int S_t = static_cast<int>(tile_start(pround) - tb0);
       const uint32_t rb = static_cast<uint32_t>(S_t) * SH2 * 4u;
       mbar_arrive_expect_tx(bar, rb);
       bulk_load(sp, a.h_s2 + tb0 * SH2, rb, bar);
     }
     lp.next(NST);
     ++pn;
-    if (++pit == NC + 1) {
+    if (++pit == round_items(pround)) {
       pit = 0;
-      ++ptile;
+      ++pround;
     }
   };
 
@@ -198,7 +207,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     // the first stages are requested after the weights, so that the weight
     // loads are not queued behind them
     if (warp == kProducerWarp && lane == 0)
-      for (int i = 0; i < NST && ptile < T; ++i) produce_one();
+      for (int i = 0; i < NST && pround <= T; ++i) produce_one();
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
       const int i = tid + u * kFwdThreads;
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      while (ptile < T) produce_one();
+      while (pround <= T) produce_one();
       while (rn < pn) release_one();
       bulk_wait_all();
     }
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       constexpr uint32_t idesc32 = umma_idesc_tf32(128, 32);
       const uint32_t ring = smem_addr(base);
       const uint32_t w0 = smem_addr(sW);
-      RingPos tp, lr, lf;
+      RingPos tp, lr, lf;  // lr: loready / cdone position of the next remainder product
       for (int t = 0; t < T; ++t) {
         // the set's previous tile (t - 2) has been read back
         if (t >= 2) bounded_wait(&bb->accempty[t & 1], ((t - 2) >> 1) & 1, a.err);
@@ -243,34 +252,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
         // remainder products of a chunk as soon as it is written, else main
         // products of the next landed chunk; each kind in chunk order into its
         // own accumulator. descriptor + 2 u = 32 u bytes on.
-        RingPos pm = tp, pc = tp;
+        RingPos pm = tp;
         int qm = 0, qc = 0;
         IdleClock clk;
         while (qc < NC) {
           bool did = false;
           if (qc < qm && mbar_test_wait(&bb->loready[lr.i], lr.ph)) {
+            TRACE_AT(2, 700 + qc);
             tc_fence_after();
-            mbar_arrive(&bb->empty[pc.i]);  // the compute warps are done with it
             const uint32_t al = tmem + kColLo + 32u * lf.i;
             const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               umma_tf32_ta(acc + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
-            umma_commit(&bb->lofree[lf.i]);
+            // one commit per chunk: it frees the remainder buffer and the
+            // chunk's stage, and after the last chunk it hands the
+            // projections to the compute warps
+            umma_commit(&bb->cdone[lr.i]);
+            TRACE_AT(2, 400 + qc);
             lr.next(kChunkRing);
             lf.next(kLoBufs);
-            pc.next(NST);
             ++qc;
             did = true;
           }
           if (!did && qm < NC && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
+            TRACE_AT(2, 600 + qm);
             tc_fence_after();
             const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
             const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               umma_tf32(acc + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
-            umma_commit(&bb->empty[pm.i]);  // first of the stage's two arrivals
+            TRACE_AT(2, 300 + qm);
             pm.next(NST);
             ++qm;
             did = true;
@@ -280,8 +293,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
           else if (clk.idle(a.err))
             break;
         }
-        for (int i = 0; i < NC + 1; ++i) tp.next(NST);
-        umma_commit(&bb->accfull);
+        for (int i = 0; i < round_items(t); ++i) tp.next(NST);  // this tile's chunks, the previous tile's rows
+        TRACE_AT(2, 500);
       }
     }
   } else {
@@ -291,28 +304,96 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     const int qd = warp & 3, sub = warp >> 2;
     const int row = 32 * qd + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-    // C partial dots: thread = (sample half, state, column quad), 8 samples
-    const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_s0 = 8 * (tid >> 7);
-    const int sd_box = a.off_S + sd_s0 * 128;
-    const float* sd_w = sW_Ct + sd_d * SH2 + 4 * sd_jq;
+    // C partial dots: thread = (state quad sd_dq, sample pair sd_sp, column
+    // quad sd_jq): samples 2 sd_sp, 2 sd_sp + 1 x states 4 sd_dq .. + 3 over 4
+    // columns of each chunk
+    const int sd_jq = tid & 7, sd_sp = (tid >> 3) & 7, sd_dq = tid >> 6;
+    const float* sd_w = sW_Ct + 4 * sd_dq * SH2 + 4 * sd_jq;
     int lo_off[4];
 #pragma unroll
     for (int v = 0; v < 4; ++v) lo_off[v] = row * 32 + (((4 * sub + v) ^ (row & 7)) << 2);
     RingPos ip, lr, lf;
     int c = 0;
     PROF_DECL;
+    // ====== output of tile tt: h_enriched = h_s2 + tw ctx . W_O, in place over
+    // its h_s2 rows; runs after the next tile's chunks, while the MMA warp
+    // finishes that tile's projections
+    auto output_tile = [&](int tt) {
+      const int S_t = static_cast<int>(tile_start(tt + 1) - tile_start(tt));
+      {
+        PROF_BEGIN();
+        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        PROF_END(9);
+        PROF_BEGIN();
+        float* hs = reinterpret_cast<float*>(stage_ptr(ip.i));
+        const int st = ip.i;
+        ip.next(NST);
+        // thread = 4 columns x samples sq, sq + 4, sq + 8, sq + 12: each W_O
+        // element serves four samples
+        const int jq = tid & 63, sq = tid >> 6;
+        if (4 * jq < SH2) {
+          float4 o[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int dq = 0; dq < D / 4; ++dq) {
+            float cx[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int s = min(sq + 4 * u, S_max - 1);
+              const float4 cv = lds4(sCtx + s * D + 4 * dq);
+              cx[u][0] = cv.x; cx[u][1] = cv.y; cx[u][2] = cv.z; cx[u][3] = cv.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float4 wv = lds4(sW_O + (4 * dq + e) * SH2 + 4 * jq);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                o[u].x = fmaf(cx[u][e], wv.x, o[u].x);
+                o[u].y = fmaf(cx[u][e], wv.y, o[u].y);
+                o[u].z = fmaf(cx[u][e], wv.z, o[u].z);
+                o[u].w = fmaf(cx[u][e], wv.w, o[u].w);
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int s = sq + 4 * u;
+            if (s < S_t) {
+              float* hp = hs + s * SH2 + 4 * jq;
+              float4 h = lds4(hp);
+              h.x = fmaf(a.tw, o[u].x, h.x);
+              h.y = fmaf(a.tw, o[u].y, h.y);
+              h.z = fmaf(a.tw, o[u].z, h.z);
+              h.w = fmaf(a.tw, o[u].w, h.w);
+              sts4(hp, h);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_sync(1, kComputeThreads);
+        if (tid == 0) mbar_arrive(&bb->outdone[st]);  // the producer stores it
+        PROF_END(10);
+      }
+    };
     for (int t = 0; t < T; ++t) {
       const long long tb0 = tile_start(t);
       const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
-      float sacc[8];
+      float sacc[2][4];  // [sample 2 sd_sp + i][state 4 sd_dq + e]
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sacc[i] = 0.f;
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[i][e] = 0.f;
       // ====================================================== pass 1 chunks
       RingPos lr_prev = lr;
       for (int q = 0; q < NC; ++q, ++c) {
-        const float4 w = lds4(sd_w + q * kChunk);
+        float4 w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = lds4(sd_w + e * SH2 + q * kChunk);
         PROF_BEGIN();
+        if (tid == 0) TRACE_AT(0, 10);
         bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        if (tid == 0) TRACE_AT(0, 11);
         PROF_END(0);
         PROF_BEGIN();
         const unsigned char* sp = stage_ptr(ip.i);
@@ -337,7 +418,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
           lr_prev = lr;
         }
         PROF_BEGIN();
-        if (c >= kLoBufs) bounded_wait(&bb->lofree[lf.i], lf.ph ^ 1u, a.err);
+        // the buffer's previous chunk c - 3 is done
+        if (c >= kLoBufs) bounded_wait(&bb->cdone[(c - kLoBufs) % kChunkRing], ((c - kLoBufs) / kChunkRing) & 1, a.err);
         PROF_END(3);
         PROF_BEGIN();
         tc_fence_after();
@@ -345,18 +427,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
         lr.next(kChunkRing);
         lf.next(kLoBufs);
         {
-          // all 8 rows of this half even past S_max: the reads stay inside
+          // all 16 rows of the box even past S_max: the reads stay inside
           // shared memory and the sums of missing samples are never stored
-          const float* bp = reinterpret_cast<const float*>(sp + sd_box);
+          const float* bp = reinterpret_cast<const float*>(sp + a.off_S);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = lds4(bp + i * 32 + ((sd_jq ^ i) << 2));  // row sd_s0 + i; (sd_s0 + i) & 7 == i
-            float x = sacc[i];
-            x = fmaf(v.x, w.x, x); x = fmaf(v.y, w.y, x); x = fmaf(v.z, w.z, x); x = fmaf(v.w, w.w, x);
-            sacc[i] = x;
+          for (int i = 0; i < 2; ++i) {
+            const int r = 2 * sd_sp + i;
+            const float4 v = lds4(bp + r * 32 + ((sd_jq ^ (r & 7)) << 2));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float x = sacc[i][e];
+              x = fmaf(v.x, w[e].x, x); x = fmaf(v.y, w[e].y, x); x = fmaf(v.z, w[e].z, x); x = fmaf(v.w, w[e].w, x);
+              sacc[i][e] = x;
+            }
           }
         }
         ip.next(NST);
+        if (tid == 0) TRACE_AT(0, 13);
         PROF_END(4);
       }
       PROF_BEGIN();
@@ -365,19 +452,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int m = 1; m < 8; m <<= 1) sacc[i] += __shfl_xor_sync(0xffffffffu, sacc[i], m);
-      }
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int m = 1; m < 8; m <<= 1) sacc[i][e] += __shfl_xor_sync(0xffffffffu, sacc[i][e], m);
       if (sd_jq == 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (sd_s0 + i < S_t) sC[(sd_s0 + i) * D + sd_d] = sacc[i];
+        for (int i = 0; i < 2; ++i) {
+          const int s = 2 * sd_sp + i;
+          if (s < S_t) sts4(sC + s * D + 4 * sd_dq, make_float4(sacc[i][0], sacc[i][1], sacc[i][2], sacc[i][3]));
+        }
       }
       PROF_END(5);
+      if (t >= 1) output_tile(t - 1);
       // ==================================== projections: TMEM -> shared memory
       PROF_BEGIN();
-      bounded_wait(&bb->accfull, t & 1, a.err);
+      if (tid == 0) TRACE_AT(0, 20);
+      bounded_wait(&bb->cdone[(c - 1) % kChunkRing], ((c - 1) / kChunkRing) & 1, a.err);  // the tile's last chunk
+      if (tid == 0) TRACE_AT(0, 21);
       PROF_END(6);
       PROF_BEGIN();
       tc_fence_after();
@@ -457,63 +550,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       }
       named_sync(1, kComputeThreads);
       PROF_END(8);
-      // ====== output: h_enriched = h_s2 + tw ctx . W_O, in place over h_s2
-      {
-        PROF_BEGIN();
-        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
-        PROF_END(9);
-        PROF_BEGIN();
-        float* hs = reinterpret_cast<float*>(stage_ptr(ip.i));
-        const int st = ip.i;
-        ip.next(NST);
-        // thread = 4 columns x samples sq, sq + 4, sq + 8, sq + 12: each W_O
-        // element serves four samples
-        const int jq = tid & 63, sq = tid >> 6;
-        if (4 * jq < SH2) {
-          float4 o[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int dq = 0; dq < D / 4; ++dq) {
-            float cx[4][4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int s = min(sq + 4 * u, S_max - 1);
-              const float4 cv = lds4(sCtx + s * D + 4 * dq);
-              cx[u][0] = cv.x; cx[u][1] = cv.y; cx[u][2] = cv.z; cx[u][3] = cv.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float4 wv = lds4(sW_O + (4 * dq + e) * SH2 + 4 * jq);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                o[u].x = fmaf(cx[u][e], wv.x, o[u].x);
-                o[u].y = fmaf(cx[u][e], wv.y, o[u].y);
-                o[u].z = fmaf(cx[u][e], wv.z, o[u].z);
-                o[u].w = fmaf(cx[u][e], wv.w, o[u].w);
-              }
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int s = sq + 4 * u;
-            if (s < S_t) {
-              float* hp = hs + s * SH2 + 4 * jq;
-              float4 h = lds4(hp);
-              h.x = fmaf(a.tw, o[u].x, h.x);
-              h.y = fmaf(a.tw, o[u].y, h.y);
-              h.z = fmaf(a.tw, o[u].z, h.z);
-              h.w = fmaf(a.tw, o[u].w, h.w);
-              sts4(hp, h);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        named_sync(1, kComputeThreads);
-        if (tid == 0) mbar_arrive(&bb->empty[st], kEmptyArrivals);  // the producer stores it
-        PROF_END(10);
-      }
     }
+    if (T > 0) output_tile(T - 1);
     if (tid == 0) PROF_FLUSH(0);
   }
   tc_fence_before();

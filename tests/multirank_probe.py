@@ -12,6 +12,8 @@ times = [1.0 + rank, 10.0 * (rank + 1), 0.5]
 mx = bench.max_over_ranks(dist, times)
 bench.barrier(dist)
 value = bench.whole_job_throughput(8192, world, mx[0])
-print(json.dumps({"rank": rank, "world": world, "local": local, "max": mx, "value": value}),
-      flush=True)
+# one write per line: both ranks share the pipe, and print() may issue the text
+# and its newline as two writes when stdout is unbuffered
+sys.stdout.write(json.dumps({"rank": rank, "world": world, "local": local, "max": mx, "value": value}) + "\n")
+sys.stdout.flush()
 dist.destroy_process_group()
