@@ -48,18 +48,16 @@ constexpr int kMmaWarp = kComputeWarps + 1;
 constexpr int kRowItem = 16;       // h_history rows per dW item
 constexpr int kBwdSampleItem = 8;  // samples per dW_C/dW_O/d_h_s2 item
 constexpr int kChunkRing = 6;      // chunk hand-off barriers (>= the copy ring's depth)
-// A chunk stage is free once its main MMAs are done (commit) and the compute
-// warps have read it (the MMA warp arrives when it sees loready); other stages
-// are released by the compute warps with both arrivals at once.
-constexpr uint32_t kEmptyArrivals = 2;
+// A chunk's stage is free once its products are done (the commit on cdone,
+// which follows the compute warps' read of the chunk); a sample or row item's
+// stage once the compute warps arrive on empty.
 constexpr int kLoBufs = 3;  // TMEM buffers of h - trunc(h) for the projections
 
 struct BwdBars {
   uint64_t full[kMaxStages];          // producer -> all: stage loaded
-  uint64_t empty[kMaxStages];         // stage free: two arrivals (see kEmptyArrivals)
-  uint64_t loready[kChunkRing];       // compute -> MMA: chunk read, h - trunc(h) in TMEM
-  uint64_t lofree[3];                 // MMA -> compute: remainder buffer consumed
-  uint64_t accfull;            // MMA -> compute: projections of the tile done
+  uint64_t empty[kMaxStages];         // compute -> producer: sample / row item in stage s released
+  uint64_t loready[kChunkRing];       // compute -> MMA: chunk c read, h - trunc(h) in TMEM
+  uint64_t cdone[kChunkRing];         // MMA -> all: every product of chunk c (and before) done
   uint64_t bready;             // compute -> MMA: dA|dB operands written
   uint64_t dhready[2];         // MMA -> compute: d_h of a 64-row half done
   uint64_t dhfree[2];          // compute -> MMA: that d_h read back
@@ -201,17 +199,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_g)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
-      mbar_init(&bb->empty[s], kEmptyArrivals);
+      mbar_init(&bb->empty[s], 1);
     }
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
-    for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
+    for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->cdone[s], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bb->dhready[s], 1);
       mbar_init(&bb->dhfree[s], 1);
       mbar_init(&bb->htready[s], kComputeWarps);
       mbar_init(&bb->htfree[s], 1);
     }
-    mbar_init(&bb->accfull, 1);
     mbar_init(&bb->bready, 1);
     mbar_init(&bb->dwdone, 1);
     fence_barrier_init();
@@ -227,10 +224,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   // A stage that held a sample or row item holds that item's output once the
   // compute warps release it: the producer stores it before reusing the stage.
   RingPos lp, rp;                  // next stage to load, oldest stage not yet released
+  RingPos rcd;                     // cdone position of the next chunk to release
+  uint32_t eph = 0;                // bit s: parity of the next empty[s] phase
   int pn = 0, ptile = 0, pit = 0;  // items loaded; tile and item of the next load
   int rn = 0, rtile = 0, rit = 0;  // items released; tile and item of the next release
   auto release_one = [&]() {
-    bounded_wait(&bb->empty[rp.i], rp.ph, a.err);
+    if (rit < NC) {
+      bounded_wait(&bb->cdone[rcd.i], rcd.ph, a.err);
+      rcd.next(kChunkRing);
+    } else {
+      bounded_wait(&bb->empty[rp.i], (eph >> rp.i) & 1u, a.err);
+      eph ^= 1u << rp.i;
+    }
     const long long tb0 = tile_start(rtile);
     const int S_t = static_cast<int>(tile_start(rtile + 1) - tb0);
     const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
@@ -394,8 +399,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         }
       };
       RingPos tp;  // stage of the tile's first item
-      RingPos lr;  // loready position of the next remainder
-      RingPos lf;  // lofree position of the next remainder
+      RingPos lr;  // loready / cdone position of the next remainder
+      RingPos lf;  // remainder buffer of the next remainder
       int ri = 0;
       bool dw_first = true;
       for (int t = 0; t < T; ++t) {
@@ -411,10 +416,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         tc_fence_after();
         // pass 1: the remainder products of a chunk as soon as the compute
         // warps have written it, else the main products of the next chunk that
-        // has landed (at most two chunks ahead, so that the remainders do not
-        // queue behind them); each kind in chunk order into its own accumulator
+        // has landed; each kind in chunk order into its own accumulator. One
+        // commit per chunk, after its remainder products: it frees the chunk's
+        // stage and remainder buffer, and after the last chunk it hands the
+        // projections to the compute warps.
         {
-          RingPos pm = tp, pc = tp;  // stages of the next main / remainder chunk
+          RingPos pm = tp;  // stage of the next main chunk
           int qm = 0, qc = 0;
           IdleClock clk;
           while (qc < NC) {
@@ -422,27 +429,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
             if (qc < qm && mbar_test_wait(&bb->loready[lr.i], lr.ph)) {
               TRACE_AT(2, 400 + qc);
               tc_fence_after();
-              mbar_arrive(&bb->empty[pc.i]);  // the compute warps are done with it
               const uint32_t al = tmem + kColLo + 32u * lf.i;
               const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
                 umma_tf32_ta(tmem + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
-              umma_commit(&bb->lofree[lf.i]);
+              umma_commit(&bb->cdone[lr.i]);
               lr.next(kChunkRing);
               lf.next(kLoBufs);
-              pc.next(NST);
               ++qc;
               did = true;
             }
-            if (!did && qm < NC && qm < qc + 2 && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
+            if (!did && qm < NC && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
               tc_fence_after();
               const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
               const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
                 umma_tf32(tmem + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
-              umma_commit(&bb->empty[pm.i]);  // first of the stage's two arrivals
               pm.next(NST);
               ++qm;
               did = true;
@@ -454,7 +458,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           }
         }
         for (int i = 0; i < NC + NSI + NRI; ++i) tp.next(NST);
-        umma_commit(&bb->accfull);
         TRACE_AT(2, 500);
         // d_h of rows [0, 64), then per 16 rows the dW MMAs; rows [64, 128)
         // once the first half has been read back
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     const bool jok = jrow < SH2;
     RingPos ip;  // stage of the next item
     RingPos lr;  // loready position of the next chunk
-    RingPos lf;  // lofree position of the next chunk
+    RingPos lf;  // remainder buffer of the next chunk
     int c = 0, ri = 0;
     for (int t = 0; t < T; ++t) {
       const long long tb0 = tile_start(t);
@@ -568,7 +571,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           if (lane == 0) mbar_arrive(&bb->loready[lr_prev.i]);
           lr_prev = lr;
         }
-        if (c >= kLoBufs) bounded_wait(&bb->lofree[lf.i], lf.ph ^ 1u, a.err);
+        // the buffer's previous chunk c - 3 is done
+        if (c >= kLoBufs) bounded_wait(&bb->cdone[(c - kLoBufs) % kChunkRing], ((c - kLoBufs) / kChunkRing) & 1, a.err);
         tc_fence_after();
         tmem_st16(lane_base + kColLo + 32u * lf.i + 16u * sub, lo);
         lr.next(kChunkRing);
@@ -606,7 +610,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       }
       // ==================================== projections: TMEM -> shared memory
       if (tid == 0) TRACE_AT(0, 20);
-      bounded_wait(&bb->accfull, t & 1, a.err);
+      bounded_wait(&bb->cdone[(c - 1) % kChunkRing], ((c - 1) / kChunkRing) & 1, a.err);  // the tile's last chunk
       if (tid == 0) TRACE_AT(0, 21);
       tc_fence_after();
       {
@@ -805,7 +809,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           fence_proxy_async_smem();
           named_sync(1, kComputeThreads);
           if (tid == 0) {
-            mbar_arrive(&bb->empty[st], kEmptyArrivals);  // the producer stores d_h_s2 from the stage
+            mbar_arrive(&bb->empty[st]);  // the producer stores d_h_s2 from the stage
             TRACE_AT(0, 33);
           }
         } else {
@@ -869,7 +873,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           named_sync(1, kComputeThreads);
           if (tid == 0) {
             if (last_of_half) mbar_arrive(&bb->dhfree[rh]);
-            mbar_arrive(&bb->empty[st], kEmptyArrivals);  // the producer stores the d_h rows from the stage
+            mbar_arrive(&bb->empty[st]);  // the producer stores the d_h rows from the stage
             TRACE_AT(0, 42);
           }
           ++ri;
