@@ -111,6 +111,18 @@ class ClockSampler:
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # nvidia-smi's start-up (driver and NVML initialisation) can hold up
+        # the GPU for seconds: let it finish, i.e. wait for its first sample,
+        # before the timed region begins
+        t0 = time.time()
+        while time.time() - t0 < 15.0 and self.proc.poll() is None:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                pass
+            time.sleep(0.05)
 
     def stop(self, gpus):
         if self.proc is None:
