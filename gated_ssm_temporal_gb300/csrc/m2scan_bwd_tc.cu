@@ -55,7 +55,7 @@ constexpr int kLoBufs = 3;  // TMEM buffers of h - trunc(h) for the projections
 
 struct BwdBars {
   uint64_t full[kMaxStages];          // producer -> all: stage loaded
-  uint64_t empty[kMaxStages];         // compute -> producer: sample / row item in stage s released
+  uint64_t empty[kMaxStages];         // compute -> producer: sample / row item in stage s released (one arrival per warp)
   uint64_t loready[kChunkRing];       // compute -> MMA: chunk c read, h - trunc(h) in TMEM
   uint64_t cdone[kChunkRing];         // MMA -> all: every product of chunk c (and before) done
   uint64_t bready;             // compute -> MMA: dA|dB operands written
@@ -199,13 +199,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_g)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
-      mbar_init(&bb->empty[s], 1);
+      mbar_init(&bb->empty[s], kComputeWarps);
     }
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->cdone[s], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bb->dhready[s], 1);
-      mbar_init(&bb->dhfree[s], 1);
+      mbar_init(&bb->dhfree[s], kComputeWarps);
       mbar_init(&bb->htready[s], kComputeWarps);
       mbar_init(&bb->htfree[s], 1);
     }
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           fence_proxy_async_smem();
           named_sync(1, kComputeThreads);
           if (tid == 0) {
-            mbar_arrive(&bb->empty[st]);  // the producer stores d_h_s2 from the stage
+            mbar_arrive(&bb->empty[st], kComputeWarps);  // the producer stores d_h_s2 from the stage
             TRACE_AT(0, 33);
           }
         } else {
@@ -854,8 +854,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
             if (tid == 0) TRACE_AT(0, 45);
           }
           tc_fence_after();
-          named_sync(1, kComputeThreads);  // every read of the h rows done
           {
+            // each thread overwrites exactly the elements it read (column j
+            // of the 16 rows), so no other thread's read is in the way
             float v[16];
             tmem_ld<16>(lane_base + 64u * sub + 16u * (k & 3), v);
             if (full_item) {
@@ -870,16 +871,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           const bool last_of_half = (k & 3) == 3 || k == NRI - 1;
           tc_fence_before();
           fence_proxy_async_smem();
-          named_sync(1, kComputeThreads);
-          if (tid == 0) {
+          __syncwarp();
+          if (lane == 0) {  // per warp: its part of d_h read, its rows written
             if (last_of_half) mbar_arrive(&bb->dhfree[rh]);
             mbar_arrive(&bb->empty[st]);  // the producer stores the d_h rows from the stage
-            TRACE_AT(0, 42);
           }
+          if (tid == 0) TRACE_AT(0, 42);
           ++ri;
         }
       }
-      if (NRI <= 4 && tid == 0) mbar_arrive(&bb->dhfree[1]);
+      if (NRI <= 4 && lane == 0) mbar_arrive(&bb->dhfree[1]);
       if (tid == 0) TRACE_AT(0, 46);
     }
     // ===================================== partial sums into the CTA's slot
