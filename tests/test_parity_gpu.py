@@ -45,6 +45,15 @@ def test_fast_path_shapes(K, SH2, D):
     check(custom(37, K, SH2, D, seed=K * 1000 + SH2 + D, wa_scale=2.0))
 
 
+@pytest.mark.parametrize("B,K,SH2", [
+    (3503, 1, 256), (2999, 3, 96), (4000, 5, 160), (2000, 12, 32), (1217, 33, 256), (900, 128, 64)])
+def test_tensor_core_multi_tile_shapes(B, K, SH2):
+    # D = 16 runs the tensor-core kernels; B > 152 gives every CTA several
+    # tiles of unequal size (S_t from 16 down to 1 sample, 1 or 2 sample
+    # items, 1 to 8 row items) and SH2 / 32 chunks per tile
+    check(custom(B, K, SH2, 16, seed=B + K + SH2, wa_scale=2.0))
+
+
 @pytest.mark.parametrize("K,SH2,D", [
     (8, 36, 16), (129, 64, 4), (4, 4, 1), (6, 20, 3), (8, 256, 16), (16, 512, 64), (3, 64, 24)])
 def test_generic_path_shapes(K, SH2, D):
