@@ -71,6 +71,7 @@ m2scan_status prepare_device(int* dev_out) {
   if ((e = prepare_fwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_bwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_fwd_tc16_kernels(smem)) != cudaSuccess) return cuda_fail(e);
+  if ((e = prepare_wide_kernels()) != cudaSuccess) return cuda_fail(e);
   void* p = nullptr;
   if ((e = cudaGetSymbolAddress(&p, g_m2scan_err_word)) != cudaSuccess) return cuda_fail(e);
   if (!g_encode) {
@@ -128,7 +129,7 @@ m2scan_status check_shape(int64_t B, int32_t K, int32_t SH2, int32_t D) {
 int slots_for(int64_t B) { return B < kMaxSlots ? static_cast<int>(B) : kMaxSlots; }
 
 // 1 = fast path (plan->tc set when the tensor-core kernel is used), 2 = generic,
-// 0 = unsupported.
+// 3 = wide-state FP32 kernels, 0 = unsupported.
 int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_smem,
                 FastArgs* plan) {
   if (!g_force_generic.load() && B <= 0x7fffffffll) {
@@ -136,6 +137,7 @@ int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_
     if (!bwd && fwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (bwd && bwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (fast_plan(bwd, K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
+    if (wide_path_ok(K, SH2, D)) return 3;
   }
   if (generic_smem_bytes(bwd, K, SH2, D) <= static_cast<size_t>(max_smem)) return 2;
   return 0;
@@ -205,7 +207,12 @@ int m2scan_path_for(int32_t K, int32_t SH2, int32_t D) {
 
 size_t m2scan_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D) {
   if (check_shape(B, K, SH2, D) != M2SCAN_OK || B == 0) return 0;
-  return static_cast<size_t>(slots_for(B)) * 4 * static_cast<size_t>(SH2) * D * sizeof(float);
+  const size_t slots = static_cast<size_t>(slots_for(B)) * 4 * static_cast<size_t>(SH2) * D * sizeof(float);
+  if (!wide_path_ok(K, SH2, D)) return slots;
+  // the wide-state kernels also keep dA|dB and [dC | ctx] there; the generic
+  // kernels (forced for tests) use the slots alone
+  const size_t wide = wide_bwd_workspace_bytes(B, K, SH2);
+  return wide > slots ? wide : slots;
 }
 
 m2scan_status m2scan_read_device_flags(uint32_t* flags) {
@@ -257,6 +264,8 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
     e = fa.tc == 2 ? launch_fwd_tc16(fa, grid, stream)
         : fa.tc    ? launch_fwd_tc(D, fa, grid, stream)
                    : launch_fast(false, D, fa, grid, stream);
+  } else if (path == 3) {
+    e = launch_wide_fwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, B, K, SH2, h_enriched, stream);
   } else {
     GenericArgs ga{h_history, h_s2, nullptr, W_A, W_B, W_C, W_O, h_enriched, nullptr, nullptr,
                    B, K, SH2, D, tw};
@@ -320,6 +329,13 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
     fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, d_h_enriched, B)) return M2SCAN_ERR_UNSUPPORTED;
     e = fa.tc ? launch_bwd_tc(fa, grid, stream) : launch_fast(true, D, fa, grid, stream);
+  } else if (path == 3) {
+    int n = 0;
+    e = launch_wide_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2, d_h_history,
+                        d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, stream, &n);
+    t_last_launches = n;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return M2SCAN_OK;
   } else {
     GenericArgs ga{h_history, h_s2, d_h_enriched, W_A, W_B, W_C, W_O, d_h_history, d_h_s2, ws,
                    B, K, SH2, D, tw};

@@ -88,6 +88,18 @@ bool tc_path_ok(bool bwd, int D);
 size_t generic_smem_bytes(bool bwd, int K, int SH2, int D);
 
 cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream);
+// FP32 kernels for wide states (D = 64, SH2 % 128 == 0, K <= 128).
+bool wide_path_ok(int K, int SH2, int D);
+size_t wide_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2);
+cudaError_t launch_wide_fwd(const float* h_history, const float* h_s2, const float* W_A,
+                            const float* W_B, const float* W_C, const float* W_O, float tw, int64_t B,
+                            int K, int SH2, float* h_enriched, cudaStream_t stream);
+cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const float* W_A,
+                            const float* W_B, const float* W_C, const float* W_O, float tw,
+                            const float* g, int64_t B, int K, int SH2, float* d_h_history,
+                            float* d_h_s2, float* dW_A, float* dW_B, float* dW_C, float* dW_O,
+                            void* workspace, cudaStream_t stream, int* n_launches);
+cudaError_t prepare_wide_kernels();
 // Warp-specialised tensor-core forward (D in {8, 16}).
 bool fwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_fwd_tc(int D, const FastArgs& a, int grid, cudaStream_t stream);

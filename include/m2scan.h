@@ -86,7 +86,10 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
 /*
  * Bytes of device workspace m2scan_bwd needs for these shapes: the per-slot
  * partial sums of the four weight gradients (min(B,152) slots of 4*SH2*D
- * floats). Depends on the shapes only. Returns 0 for invalid shapes.
+ * floats); for the wide-state shapes (D = 64, SH2 % 128 == 0, K <= 128) the
+ * larger of that and min(B,38) slots plus dA|dB (B*K*2D floats) and
+ * [dC | ctx] (B*2D floats). Depends on the shapes only. Returns 0 for invalid
+ * shapes.
  */
 size_t m2scan_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D);
 
@@ -152,7 +155,8 @@ int m2scan_last_cuda_error(void);
 int m2scan_set_force_generic(int force);
 
 /* Which kernel family m2scan_fwd/m2scan_bwd would launch for these shapes:
- * 1 = fused fast path, 2 = generic fallback, 0 = unsupported shape. */
+ * 1 = fused fast path, 2 = generic fallback, 3 = wide-state FP32 kernels
+ * (D = 64, SH2 % 128 == 0, K <= 128), 0 = unsupported shape. */
 int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
 
 /*

@@ -61,6 +61,7 @@ res["bwd_alias_dh_g"] = bwd(d_h_history=W[7])
 res["ws_bytes_pages"] = g.m2scan_bwd_workspace_bytes(8192, 8, 256, 16)
 res["ws_bytes_small_B"] = g.m2scan_bwd_workspace_bytes(3, 8, 256, 16)
 res["ws_bytes_B0"] = g.m2scan_bwd_workspace_bytes(0, 8, 256, 16)
+res["ws_bytes_wide"] = g.m2scan_bwd_workspace_bytes(16384, 16, 512, 64)
 res["ws_bytes_bad"] = g.m2scan_bwd_workspace_bytes(5, 0, 256, 16)
 res["path_pages"] = g.m2scan_path_for(8, 256, 16)
 res["path_long"] = g.m2scan_path_for(64, 256, 16)

@@ -63,13 +63,15 @@ def test_workspace_query(probe):
     assert probe["ws_bytes_small_B"] == 3 * 4 * 256 * 16 * 4
     assert probe["ws_bytes_B0"] == 0
     assert probe["ws_bytes_bad"] == 0
+    # wide states: 38 slots plus dA|dB [B*K][128] and [dC | ctx] [B][128]
+    assert probe["ws_bytes_wide"] == (38 * 4 * 512 * 64 + 16384 * 16 * 128 + 16384 * 128) * 4
 
 
 def test_path_choice(probe):
     assert probe["path_pages"] == 1
     assert probe["path_long"] == 1
     assert probe["path_tiny"] == 1
-    assert probe["path_wide"] == 2
+    assert probe["path_wide"] == 3
     assert probe["path_K129"] == 2
     assert probe["path_huge"] == 0
     assert probe["status_str_ok"] == "ok"

@@ -54,6 +54,18 @@ def test_tensor_core_multi_tile_shapes(B, K, SH2):
     check(custom(B, K, SH2, 16, seed=B + K + SH2, wa_scale=2.0))
 
 
+@pytest.mark.parametrize("B,K,SH2", [
+    (1, 1, 128), (5, 16, 512), (37, 3, 128), (1000, 7, 384), (300, 128, 256), (2047, 16, 512)])
+def test_wide_state_shapes(B, K, SH2):
+    # D = 64 runs the wide-state FP32 kernels: 128-row tiles of up to 16
+    # samples, a partial last tile, and up to 38 sample ranges for the dW
+    # products (fewer when B < 38)
+    import gated_ssm_temporal_gb300 as g
+    ensure_built()
+    assert g.m2scan_path_for(K, SH2, 64) == 3
+    check(custom(B, K, SH2, 64, seed=B * 7 + K + SH2, wa_scale=2.0))
+
+
 @pytest.mark.parametrize("K,SH2,D", [
     (8, 36, 16), (129, 64, 4), (4, 4, 1), (6, 20, 3), (8, 256, 16), (16, 512, 64), (3, 64, 24)])
 def test_generic_path_shapes(K, SH2, D):

@@ -52,7 +52,7 @@ def test_noalloc_matches_bwd_on_two_calls(name):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    """The wide-state shapes need 80 MB of slots, above the 16 MiB array: the call
+    """The wide-state shapes need 182 MB of workspace, above the 16 MiB array: the call
     returns M2SCAN_ERR_WORKSPACE before anything is launched."""
     import torch
     ensure_built()
