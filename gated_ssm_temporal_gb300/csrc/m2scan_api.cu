@@ -57,6 +57,10 @@ m2scan_status prepare_device(int* dev_out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return M2SCAN_ERR_DEVICE;
+  // A host thread that has made no runtime call yet has no current context,
+  // and the tensor-map encoder (a driver entry point) needs one: make the
+  // device's primary context current on this thread.
+  if ((e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail(e);
   *dev_out = dev;
   std::lock_guard<std::mutex> lock(g_prep_mutex);
   if (g_prepared[dev]) return M2SCAN_OK;

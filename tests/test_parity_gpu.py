@@ -215,3 +215,25 @@ def test_no_device_wait_timeouts():
     ensure_built()
     run_all(custom(64, 8, 256, 16, seed=4))
     assert g.m2scan_read_device_flags() == 0
+
+
+def test_calls_from_a_new_host_thread():
+    # a host thread that has made no CUDA runtime call yet (autograd's backward
+    # runs on one): the library makes the device's context current itself
+    import threading
+    x = custom(300, 8, 256, 16, seed=21)
+    ref = oracle_all(x)
+    res = {}
+
+    def work():
+        try:
+            res["got"] = run_all(x)
+        except Exception as e:  # reported below, on the test's thread
+            res["err"] = e
+
+    th = threading.Thread(target=work)
+    th.start()
+    th.join()
+    assert "err" not in res, res.get("err")
+    for n in NAMES:
+        assert_parity(n, res["got"][n], ref[n])
