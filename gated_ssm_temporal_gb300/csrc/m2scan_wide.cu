@@ -66,7 +66,7 @@ __device__ __forceinline__ int blk_row(int ty, int i) { return i < 4 ? 4 * ty + 
 // acc += At^T . Bs over one chunk: At[k][m] (k < 32, m < 128), Bs[k][n].
 __device__ __forceinline__ void chunk_mma(const float* At, const float* Bs, int ty, int tx,
                                           float (&acc)[8][8]) {
-#pragma unroll 4
+#pragma unroll 8
   for (int k = 0; k < kWKc; ++k) {
     const float4 a0 = lds4(At + k * kLd + 4 * ty), a1 = lds4(At + k * kLd + 64 + 4 * ty);
     const float4 b0 = lds4(Bs + k * kLd + 4 * tx), b1 = lds4(Bs + k * kLd + 64 + 4 * tx);
