@@ -161,6 +161,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ helpers
 
+def metric_for(w) -> str:
+    """The headline metric's name, with the workload's own dimensions."""
+    return "fwd+bwd samples/s (B=%d, K=%d, SH2=%d, D=%d)" % (w.B, w.K, w.SH2, w.D)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -348,7 +353,7 @@ def run_native(args, rank, world, local):
     achieved = ab["bwd"] / (bwd_ms / 1e3) / 1e9
     traffic = recorded_traffic("m2scan_bwd")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
+        "metric": metric_for(w), "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g per rank" % (w.name, B, K, SH2, D,
