@@ -9,11 +9,11 @@
 //            recomputes A|B = h . [W_A|W_B] with the chunk as the A operand
 //            straight from shared memory (the tensor core reads the top 19 bits
 //            of each fp32, i.e. trunc(h)); meanwhile the compute warps write
-//            h - trunc(h) (rounded to tf32) into tensor memory and the MMA warp
-//            adds that remainder's product. A stage is free as soon as its
-//            main MMAs are done and the compute warps have read it. The
-//            compute warps also form
-//            C = h_s2 . W_C and d_ctx = tw dY . W_O^T on the FMA pipe.
+//            h - trunc(h) into tensor memory and the MMA warp adds that
+//            remainder's product. One commit per chunk, after its remainder
+//            products, frees the chunk's stage and remainder buffer. The
+//            compute warps also form C = h_s2 . W_C and d_ctx = tw dY . W_O^T
+//            on the FMA pipe.
 //   scan     replay of the forward scan and the reverse scan of the
 //            implementation plan's Task 2 ("Custom Kernel Optimization
 //            Implementation Plan"): dB_t = dx, dA_t = dx x_{t-1} sigmoid'(A_t),

@@ -55,7 +55,7 @@ struct alignas(128) FastArgs {
   int off_mbar;   // tensor-core path: two MMA-completion barriers
   int off_tslot;  // tensor-core path: TMEM base address written by tcgen05.alloc
   int n_stages;   // depth of the copy ring
-  int tc;         // 0: FP32-FMA kernel, 1: tensor-core kernel, 2: 16-warp tensor-core forward
+  int tc;         // 0: FP32-FMA kernel, 1: tensor-core kernel, 2: tensor-core forward for D = 16
   int tmem_cols;  // TMEM columns allocated by each CTA (power of two)
   int smem_bytes;
   float tw;
@@ -103,8 +103,8 @@ cudaError_t prepare_wide_kernels();
 // Warp-specialised tensor-core forward (D in {8, 16}).
 bool fwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_fwd_tc(int D, const FastArgs& a, int grid, cudaStream_t stream);
-// Warp-specialised tensor-core forward for D = 16 with 16 compute warps
-// (plan->tc = 2).
+// Warp-specialised tensor-core forward for D = 16 (8 compute warps, two TMEM
+// accumulator sets; plan->tc = 2).
 bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_fwd_tc16(const FastArgs& a, int grid, cudaStream_t stream);
 // Warp-specialised tensor-core backward (D = 16).
