@@ -7,13 +7,14 @@
 // + Batch-Parallel Scans", Design 1, Steps 1-2; output step as the layer fixes
 // it). Per tile:
 //   pass 1   the producer warp streams 32-column chunks of h_history and h_s2
-//            (TMA boxes, 128-byte swizzle). The MMA warp computes
+//            (TMA boxes, 128-byte swizzle). One MMA thread computes
 //            A|B = h . [W_A|W_B] with the chunk as the A operand straight from
 //            shared memory (the tensor core reads trunc(h)); the compute warps
-//            write h - trunc(h) (rounded to tf32) into tensor memory and the MMA
-//            warp adds that product (3 x tf32 in all). A stage is free once its
-//            main MMAs are done and the compute warps have read it. The compute
-//            warps form C = h_s2 . W_C on the FMA pipe meanwhile.
+//            write h - trunc(h) (rounded to tf32) into tensor memory and a
+//            second MMA thread adds that product (3 x tf32 in all). A stage is
+//            free once its main MMAs are done and the compute warps have read
+//            it. The compute warps form C = h_s2 . W_C on the FMA pipe
+//            meanwhile.
 //   scan     x_t = sigmoid(A_t) x_{t-1} + B_t, one thread per (sample, state);
 //            ctx = C x_{K-1}.
 //   output   h_enriched = h_s2 + tw ctx . W_O over the tile's h_s2 rows, in
@@ -27,24 +28,30 @@ namespace {
 
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kFwdThreads = kComputeThreads + 64;
+constexpr int kFwdThreads = kComputeThreads + 96;
 constexpr int kProducerWarp = kComputeWarps;
-constexpr int kMmaWarp = kComputeWarps + 1;
+constexpr int kMmaWarp = kComputeWarps + 1;    // main products trunc(h) . [W_hi | W_lo]
+constexpr int kCorrWarp = kComputeWarps + 2;   // remainder products (h - trunc h) . W_hi
 constexpr int kChunkRing = 6;
 constexpr int kLoBufs = 3;
 
+// Two threads issue the tensor-core work, each with its own commits: a
+// commit stalls only the stream of the thread that issues it, so the main
+// and the remainder products of a chunk overlap each other's stalls.
 struct FwdBars {
   uint64_t full[kMaxStages];     // producer -> all: stage loaded
+  uint64_t empty[kMaxStages];    // chunk stage s free: main products done (commit) + compute read (arrive)
   uint64_t outdone[kMaxStages];  // compute -> producer: output written over the h_s2 item in stage s
-  uint64_t loready[kChunkRing];  // compute -> MMA: chunk c read, h - trunc(h) in TMEM
-  uint64_t cdone[kChunkRing];    // MMA -> all: every product of chunk c (and before) done
-  uint64_t accempty[2];          // compute -> MMA: projections of accumulator set s read back
+  uint64_t loready[kChunkRing];  // compute -> remainder MMA thread: chunk c read, h - trunc(h) in TMEM
+  uint64_t lofree[kLoBufs];      // remainder MMA thread -> all: remainder buffer's products done
+  uint64_t mdone[2];             // main MMA thread -> compute: main products of tile t (set t & 1) done
+  uint64_t accempty[2];          // compute -> MMA threads: projections of accumulator set s read back
   uint32_t tslot;
   uint32_t pad;
 };
 
 // TMEM columns: two accumulator sets, tile t using set t & 1 at 256 (t & 1),
-// so that the MMA warp starts the next tile's products while the compute
+// so that the MMA threads start the next tile's products while the compute
 // warps still read back, scan and write out this one. Within a set: [0, 128)
 // trunc(h) . [W_hi | W_lo] of the even and of the odd chunks, [224, 256)
 // (h - trunc h) . W_hi. [128, 224): three buffers of h - trunc(h), shared
@@ -122,12 +129,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_hs)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
+      mbar_init(&bb->empty[s], 2);
+      mbar_init(&bb->outdone[s], 1);
     }
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
-    for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->cdone[s], 1);
-    for (int s = 0; s < NST; ++s) mbar_init(&bb->outdone[s], 1);
-    mbar_init(&bb->accempty[0], 1);
-    mbar_init(&bb->accempty[1], 1);
+    for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bb->mdone[s], 1);
+      mbar_init(&bb->accempty[s], 1);  // waited for by both MMA threads
+    }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&bb->tslot, 2 * kSetCols);
@@ -140,17 +150,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   // the item of tile u - 1's h_s2 rows (u >= 1): the compute warps write the
   // output of a tile over its h_s2 rows after the next tile's chunks, and the
   // producer stores it before it reuses the stage
-  RingPos lp, rp, rcd;  // rcd: cdone position of the next chunk to release
+  RingPos lp, rp;
+  uint32_t rch = 0;     // bit s: parity of the next empty[s] phase (chunks only)
   uint32_t rout = 0;    // bit s: parity of the next outdone[s] phase (h_s2 items only)
   int pn = 0, pround = 0, pit = 0;
   int rn = 0, rround = 0, rit = 0;
   auto round_items = [&](int u) { return (u < T ? NC : 0) + (u >= 1 ? 1 : 0); };
   auto release_one = [&]() {
     if (rit < (rround < T ? NC : 0)) {
-      // a chunk: free once its products are done (they follow the compute
-      // warps' read of it)
-      bounded_wait(&bb->cdone[rcd.i], rcd.ph, a.err);
-      rcd.next(kChunkRing);
+      // a chunk: free once its main products are done and the compute warps
+      // have read it
+      bounded_wait(&bb->empty[rp.i], (rch >> rp.i) & 1u, a.err);
+      rch ^= 1u << rp.i;
     } else {
       bounded_wait(&bb->outdone[rp.i], (rout >> rp.i) & 1u, a.err);
       rout ^= 1u << rp.i;
@@ -237,64 +248,68 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       bulk_wait_all();
     }
   } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------------- MMA
+    // ------------------------------------------- MMA: main products
+    // trunc(h) . [W_hi | W_lo] of each chunk as it lands, into the even- or
+    // odd-chunk accumulator of the tile's set; a commit per chunk frees the
+    // stage (with the remainder thread's arrival), one per tile hands the
+    // main products to the compute warps. descriptor + 2 u = 32 u bytes on.
     if (lane == 0) {
       constexpr uint32_t idesc64 = umma_idesc_tf32(128, 64);
-      constexpr uint32_t idesc32 = umma_idesc_tf32(128, 32);
       const uint32_t ring = smem_addr(base);
       const uint32_t w0 = smem_addr(sW);
-      RingPos tp, lr, lf;  // lr: loready / cdone position of the next remainder product
+      RingPos tp;
       for (int t = 0; t < T; ++t) {
         // the set's previous tile (t - 2) has been read back
         if (t >= 2) bounded_wait(&bb->accempty[t & 1], ((t - 2) >> 1) & 1, a.err);
-        tc_fence_after();
         const uint32_t acc = tmem + kSetCols * static_cast<uint32_t>(t & 1);
-        // remainder products of a chunk as soon as it is written, else main
-        // products of the next landed chunk; each kind in chunk order into its
-        // own accumulator. descriptor + 2 u = 32 u bytes on.
         RingPos pm = tp;
-        int qm = 0, qc = 0;
-        IdleClock clk;
-        while (qc < NC) {
-          bool did = false;
-          if (qc < qm && mbar_test_wait(&bb->loready[lr.i], lr.ph)) {
-            TRACE_AT(2, 700 + qc);
-            tc_fence_after();
-            const uint32_t al = tmem + kColLo + 32u * lf.i;
-            const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
+        for (int qm = 0; qm < NC; ++qm) {
+          bounded_wait(&bb->full[pm.i], pm.ph, a.err);
+          tc_fence_after();
+          TRACE_AT(2, 600 + qm);
+          const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
+          const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_tf32_ta(acc + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
-            // one commit per chunk: it frees the remainder buffer and the
-            // chunk's stage, and after the last chunk it hands the
-            // projections to the compute warps
-            umma_commit(&bb->cdone[lr.i]);
-            TRACE_AT(2, 400 + qc);
-            lr.next(kChunkRing);
-            lf.next(kLoBufs);
-            ++qc;
-            did = true;
-          }
-          if (!did && qm < NC && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
-            TRACE_AT(2, 600 + qm);
-            tc_fence_after();
-            const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
-            const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_tf32(acc + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
-            TRACE_AT(2, 300 + qm);
-            pm.next(NST);
-            ++qm;
-            did = true;
-          }
-          if (did)
-            clk.progress();
-          else if (clk.idle(a.err))
-            break;
+          for (int ks = 0; ks < 4; ++ks)
+            umma_tf32(acc + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
+          umma_commit(&bb->empty[pm.i]);
+          TRACE_AT(2, 300 + qm);
+          pm.next(NST);
         }
+        umma_commit(&bb->mdone[t & 1]);
         for (int i = 0; i < round_items(t); ++i) tp.next(NST);  // this tile's chunks, the previous tile's rows
-        TRACE_AT(2, 500);
+      }
+    }
+  } else if (warp == kCorrWarp) {
+    // ------------------------------------- MMA: remainder products
+    // (h - trunc h) . W_hi of each chunk once the compute warps have written
+    // its remainder; a commit per chunk frees the remainder buffer, and the
+    // one after the tile's last chunk hands the tile over.
+    if (lane == 0) {
+      constexpr uint32_t idesc32 = umma_idesc_tf32(128, 32);
+      const uint32_t w0 = smem_addr(sW);
+      RingPos tp, lr, lf;
+      for (int t = 0; t < T; ++t) {
+        if (t >= 2) bounded_wait(&bb->accempty[t & 1], ((t - 2) >> 1) & 1, a.err);
+        const uint32_t acc = tmem + kSetCols * static_cast<uint32_t>(t & 1);
+        RingPos pc = tp;
+        for (int qc = 0; qc < NC; ++qc) {
+          bounded_wait(&bb->loready[lr.i], lr.ph, a.err);
+          tc_fence_after();
+          TRACE_AT(3, 700 + qc);
+          mbar_arrive(&bb->empty[pc.i]);  // the compute warps are done with the stage
+          const uint32_t al = tmem + kColLo + 32u * lf.i;
+          const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_tf32_ta(acc + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&bb->lofree[lf.i]);
+          TRACE_AT(3, 400 + qc);
+          lr.next(kChunkRing);
+          lf.next(kLoBufs);
+          pc.next(NST);
+        }
+        for (int i = 0; i < round_items(t); ++i) tp.next(NST);
       }
     }
   } else {
@@ -316,8 +331,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     int c = 0;
     PROF_DECL;
     // ====== output of tile tt: h_enriched = h_s2 + tw ctx . W_O, in place over
-    // its h_s2 rows; runs after the next tile's chunks, while the MMA warp
-    // finishes that tile's projections
+    // its h_s2 rows; runs after the next tile's chunks, while the MMA threads
+    // finish that tile's projections
     auto output_tile = [&](int tt) {
       const int S_t = static_cast<int>(tile_start(tt + 1) - tile_start(tt));
       {
@@ -419,7 +434,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
         }
         PROF_BEGIN();
         // the buffer's previous chunk c - 3 is done
-        if (c >= kLoBufs) bounded_wait(&bb->cdone[(c - kLoBufs) % kChunkRing], ((c - kLoBufs) / kChunkRing) & 1, a.err);
+        if (c >= kLoBufs) bounded_wait(&bb->lofree[lf.i], lf.ph ^ 1u, a.err);
         PROF_END(3);
         PROF_BEGIN();
         tc_fence_after();
@@ -469,7 +484,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       // ==================================== projections: TMEM -> shared memory
       PROF_BEGIN();
       if (tid == 0) TRACE_AT(0, 20);
-      bounded_wait(&bb->cdone[(c - 1) % kChunkRing], ((c - 1) / kChunkRing) & 1, a.err);  // the tile's last chunk
+      // the tile's main products and the remainder products of its last chunk
+      bounded_wait(&bb->mdone[t & 1], (t >> 1) & 1, a.err);
+      bounded_wait(&bb->lofree[(c - 1) % kLoBufs], ((c - 1) / kLoBufs) & 1, a.err);
       if (tid == 0) TRACE_AT(0, 21);
       PROF_END(6);
       PROF_BEGIN();
