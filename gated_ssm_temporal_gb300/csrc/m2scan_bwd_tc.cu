@@ -9,11 +9,13 @@
 //            recomputes A|B = h . [W_A|W_B] with the chunk as the A operand
 //            straight from shared memory (the tensor core reads the top 19 bits
 //            of each fp32, i.e. trunc(h)); meanwhile the compute warps write
-//            h - trunc(h) into tensor memory and the MMA warp adds that
-//            remainder's product. One commit per chunk, after its remainder
-//            products, frees the chunk's stage and remainder buffer. The
-//            compute warps also form C = h_s2 . W_C and d_ctx = tw dY . W_O^T
-//            on the FMA pipe.
+//            h - trunc(h) into tensor memory and a second MMA thread adds that
+//            remainder's product. Each thread commits once per chunk (a commit
+//            stalls only the issuing thread's MMA stream, so the two overlap):
+//            the main commit and the remainder thread's arrival free the
+//            chunk's stage, the remainder commit its TMEM buffer. The compute
+//            warps also form C = h_s2 . W_C and d_ctx = tw dY . W_O^T on the
+//            FMA pipe.
 //   scan     replay of the forward scan and the reverse scan of the
 //            implementation plan's Task 2 ("Custom Kernel Optimization
 //            Implementation Plan"): dB_t = dx, dA_t = dx x_{t-1} sigmoid'(A_t),
@@ -42,22 +44,25 @@ namespace {
 
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kBwdThreads = kComputeThreads + 64;
+constexpr int kBwdThreads = kComputeThreads + 96;
 constexpr int kProducerWarp = kComputeWarps;
-constexpr int kMmaWarp = kComputeWarps + 1;
+constexpr int kMmaWarp = kComputeWarps + 1;   // projections trunc(h) . [W_hi | W_lo], d_h, dW
+constexpr int kCorrWarp = kComputeWarps + 2;  // projection remainders (h - trunc h) . W_hi
 constexpr int kRowItem = 16;       // h_history rows per dW item
 constexpr int kBwdSampleItem = 8;  // samples per dW_C/dW_O/d_h_s2 item
 constexpr int kChunkRing = 6;      // chunk hand-off barriers (>= the copy ring's depth)
-// A chunk's stage is free once its products are done (the commit on cdone,
-// which follows the compute warps' read of the chunk); a sample or row item's
-// stage once the compute warps arrive on empty.
+// A chunk's stage is free once its main products are done and the compute
+// warps have read it (cempty); a sample or row item's stage once the compute
+// warps arrive on empty.
 constexpr int kLoBufs = 3;  // TMEM buffers of h - trunc(h) for the projections
 
 struct BwdBars {
   uint64_t full[kMaxStages];          // producer -> all: stage loaded
   uint64_t empty[kMaxStages];         // compute -> producer: sample / row item in stage s released (one arrival per warp)
-  uint64_t loready[kChunkRing];       // compute -> MMA: chunk c read, h - trunc(h) in TMEM
-  uint64_t cdone[kChunkRing];         // MMA -> all: every product of chunk c (and before) done
+  uint64_t cempty[kMaxStages];        // chunk in stage s released: main products done (commit) + compute read (arrive)
+  uint64_t loready[kChunkRing];       // compute -> remainder MMA thread: chunk c read, h - trunc(h) in TMEM
+  uint64_t lofree[kLoBufs];           // remainder MMA thread -> all: remainder buffer's products done
+  uint64_t mdone;              // main MMA thread -> compute: the tile's main projection products done
   uint64_t bready;             // compute -> MMA: dA|dB operands written
   uint64_t dhready[2];         // MMA -> compute: d_h of a 64-row half done
   uint64_t dhfree[2];          // compute -> MMA: that d_h read back
@@ -131,33 +136,6 @@ __device__ __forceinline__ void post_item(int p, int NSI, int NRI, int& kind, in
   idx = 4 + (p - s1);
 }
 
-// Time limit for a thread that polls several barriers: call progress() after
-// every step, idle() when nothing was ready; idle() returns true once the
-// limit has passed (or another wait already gave up) and sets the error bit.
-struct IdleClock {
-  unsigned long long t0 = 0;
-  uint32_t n = 0;
-  __device__ __forceinline__ void progress() {
-    n = 0;
-    t0 = 0;
-  }
-  __device__ __forceinline__ bool idle(unsigned* err) {
-    if ((++n & 7u) != 0u) return false;
-    const unsigned long long now = global_timer_ns();
-    if (t0 == 0) {
-      t0 = now;
-      return false;
-    }
-    if ((*reinterpret_cast<volatile unsigned*>(err) & kErrWaitTimeout) != 0u) return true;
-    if (now - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrWaitTimeout);
-      return true;
-    }
-    __nanosleep(100);
-    return false;
-  }
-};
-
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_constant__ FastArgs a) {
   constexpr int D = 16, TD = 32, FD = 64;
   extern __shared__ unsigned char smem_raw[];
@@ -200,9 +178,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
       mbar_init(&bb->empty[s], kComputeWarps);
+      mbar_init(&bb->cempty[s], 2);
     }
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
-    for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->cdone[s], 1);
+    for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
+    mbar_init(&bb->mdone, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bb->dhready[s], 1);
       mbar_init(&bb->dhfree[s], kComputeWarps);
@@ -224,14 +204,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   // A stage that held a sample or row item holds that item's output once the
   // compute warps release it: the producer stores it before reusing the stage.
   RingPos lp, rp;                  // next stage to load, oldest stage not yet released
-  RingPos rcd;                     // cdone position of the next chunk to release
   uint32_t eph = 0;                // bit s: parity of the next empty[s] phase
+  uint32_t cph = 0;                // bit s: parity of the next cempty[s] phase
   int pn = 0, ptile = 0, pit = 0;  // items loaded; tile and item of the next load
   int rn = 0, rtile = 0, rit = 0;  // items released; tile and item of the next release
   auto release_one = [&]() {
     if (rit < NC) {
-      bounded_wait(&bb->cdone[rcd.i], rcd.ph, a.err);
-      rcd.next(kChunkRing);
+      bounded_wait(&bb->cempty[rp.i], (cph >> rp.i) & 1u, a.err);
+      cph ^= 1u << rp.i;
     } else {
       bounded_wait(&bb->empty[rp.i], (eph >> rp.i) & 1u, a.err);
       eph ^= 1u << rp.i;
@@ -399,8 +379,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         }
       };
       RingPos tp;  // stage of the tile's first item
-      RingPos lr;  // loready / cdone position of the next remainder
-      RingPos lf;  // remainder buffer of the next remainder
       int ri = 0;
       bool dw_first = true;
       for (int t = 0; t < T; ++t) {
@@ -408,54 +386,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
         const int NSI = n_sample_items(S_t), NRI = n_row_items(S_t);
         TRACE_AT(2, 290);
-        if (t > 0) {
-          bounded_wait(&bb->dhfree[1], (t - 1) & 1, a.err);
-          // the corrections accumulate over the previous tile's transposed rows
-          bounded_wait(&bb->htfree[(ri - 1) & 1], ((ri - 1) >> 1) & 1, a.err);
-        }
-        tc_fence_after();
-        // pass 1: the remainder products of a chunk as soon as the compute
-        // warps have written it, else the main products of the next chunk that
-        // has landed; each kind in chunk order into its own accumulator. One
-        // commit per chunk, after its remainder products: it frees the chunk's
-        // stage and remainder buffer, and after the last chunk it hands the
-        // projections to the compute warps.
+        // the previous tile's d_h has been read back (its dW MMAs, which read
+        // the columns of the remainder products, were issued by this thread)
+        if (t > 0) bounded_wait(&bb->dhfree[1], (t - 1) & 1, a.err);
+        // pass 1: the main products of each chunk as it lands, in chunk order
+        // into the even- or odd-chunk accumulator; a commit per chunk frees
+        // the stage (with the remainder thread's arrival), one per tile hands
+        // the main products to the compute warps
         {
-          RingPos pm = tp;  // stage of the next main chunk
-          int qm = 0, qc = 0;
-          IdleClock clk;
-          while (qc < NC) {
-            bool did = false;
-            if (qc < qm && mbar_test_wait(&bb->loready[lr.i], lr.ph)) {
-              TRACE_AT(2, 400 + qc);
-              tc_fence_after();
-              const uint32_t al = tmem + kColLo + 32u * lf.i;
-              const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
+          RingPos pm = tp;
+          for (int qm = 0; qm < NC; ++qm) {
+            bounded_wait(&bb->full[pm.i], pm.ph, a.err);
+            tc_fence_after();
+            const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
+            const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                umma_tf32_ta(tmem + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
-              umma_commit(&bb->cdone[lr.i]);
-              lr.next(kChunkRing);
-              lf.next(kLoBufs);
-              ++qc;
-              did = true;
-            }
-            if (!did && qm < NC && mbar_test_wait(&bb->full[pm.i], pm.ph)) {
-              tc_fence_after();
-              const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
-              const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qm * FD * 128));
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                umma_tf32(tmem + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
-              pm.next(NST);
-              ++qm;
-              did = true;
-            }
-            if (did)
-              clk.progress();
-            else if (clk.idle(a.err))
-              break;
+            for (int ks = 0; ks < 4; ++ks)
+              umma_tf32(tmem + 64u * (qm & 1), ad + 2u * ks, bd + 2u * ks, idesc64, (qm >= 2 || ks > 0) ? 1u : 0u);
+            umma_commit(&bb->cempty[pm.i]);
+            pm.next(NST);
           }
+          umma_commit(&bb->mdone);
         }
         for (int i = 0; i < NC + NSI + NRI; ++i) tp.next(NST);
         TRACE_AT(2, 500);
@@ -497,6 +448,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         TRACE_AT(2, 601);
       }
       umma_commit(&bb->dwdone);
+    }
+  } else if (warp == kCorrWarp) {
+    // ------------------------------------- MMA: projection remainders
+    // (h - trunc h) . W_hi of each chunk once the compute warps have written
+    // its remainder, into a sum of its own; a commit per chunk frees the
+    // remainder buffer. These columns hold the previous tile's transposed
+    // rows until its dW MMAs are done; the compute warps wait for that
+    // before they hand over the tile's first remainder.
+    if (lane == 0) {
+      constexpr uint32_t idesc32 = umma_idesc_tf32(128, 32);
+      const uint32_t w0 = smem_addr(sW);
+      RingPos tp, lr, lf;
+      for (int t = 0; t < T; ++t) {
+        const int S_t = static_cast<int>(tile_start(t + 1) - tile_start(t));
+        RingPos pc = tp;
+        for (int qc = 0; qc < NC; ++qc) {
+          bounded_wait(&bb->loready[lr.i], lr.ph, a.err);
+          tc_fence_after();
+          TRACE_AT(3, 400 + qc);
+          mbar_arrive(&bb->cempty[pc.i]);  // the compute warps are done with the stage
+          const uint32_t al = tmem + kColLo + 32u * lf.i;
+          const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(qc * FD * 128));
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_tf32_ta(tmem + kColCorr, al + 8u * ks, bd + 2u * ks, idesc32, (qc > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&bb->lofree[lf.i]);
+          lr.next(kChunkRing);
+          lf.next(kLoBufs);
+          pc.next(NST);
+        }
+        for (int i = 0; i < NC + n_sample_items(S_t) + n_row_items(S_t); ++i) tp.next(NST);
+      }
     }
   } else {
     // ------------------------------------------------------------- compute
@@ -544,8 +527,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       if (ri >= 2) bounded_wait(&bb->htfree[ri & 1], ((ri - 2) >> 1) & 1, a.err);
       // ====================================================== pass 1 chunks
       // Per chunk: h - trunc(h) into its TMEM buffer; the C / d_ctx dots run
-      // while that store lands, and the chunk is handed to the MMA warp at
-      // the top of the next iteration (or after the last one).
+      // while that store lands, and the chunk is handed to the remainder MMA
+      // thread at the top of the next iteration (or after the last one).
       RingPos lr_prev = lr;
       for (int q = 0; q < NC; ++q, ++c) {
         const float4 w = sd_role == 0 ? lds4(sd_w + q * kChunk)
@@ -572,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           lr_prev = lr;
         }
         // the buffer's previous chunk c - 3 is done
-        if (c >= kLoBufs) bounded_wait(&bb->cdone[(c - kLoBufs) % kChunkRing], ((c - kLoBufs) / kChunkRing) & 1, a.err);
+        if (c >= kLoBufs) bounded_wait(&bb->lofree[lf.i], lf.ph ^ 1u, a.err);
         tc_fence_after();
         tmem_st16(lane_base + kColLo + 32u * lf.i + 16u * sub, lo);
         lr.next(kChunkRing);
@@ -610,7 +593,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       }
       // ==================================== projections: TMEM -> shared memory
       if (tid == 0) TRACE_AT(0, 20);
-      bounded_wait(&bb->cdone[(c - 1) % kChunkRing], ((c - 1) / kChunkRing) & 1, a.err);  // the tile's last chunk
+      // the tile's main products and the remainder products of its last chunk
+      bounded_wait(&bb->mdone, t & 1, a.err);
+      bounded_wait(&bb->lofree[(c - 1) % kLoBufs], ((c - 1) / kLoBufs) & 1, a.err);
       if (tid == 0) TRACE_AT(0, 21);
       tc_fence_after();
       {

@@ -71,30 +71,6 @@ struct RingPos {
   }
 };
 
-struct IdleClock {
-  unsigned long long t0 = 0;
-  uint32_t n = 0;
-  __device__ __forceinline__ void progress() {
-    n = 0;
-    t0 = 0;
-  }
-  __device__ __forceinline__ bool idle(unsigned* err) {
-    if ((++n & 7u) != 0u) return false;
-    const unsigned long long now = global_timer_ns();
-    if (t0 == 0) {
-      t0 = now;
-      return false;
-    }
-    if ((*reinterpret_cast<volatile unsigned*>(err) & kErrWaitTimeout) != 0u) return true;
-    if (now - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrWaitTimeout);
-      return true;
-    }
-    __nanosleep(100);
-    return false;
-  }
-};
-
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_constant__ FastArgs a) {
   constexpr int D = 16, TD = 32, FD = 64;
   extern __shared__ unsigned char smem_raw[];
