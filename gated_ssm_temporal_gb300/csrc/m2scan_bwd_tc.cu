@@ -278,28 +278,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     }
   };
 
-  // ---- weights: projection B tiles and W_C^T into shared memory, [W_A|W_B]
-  // rows into TMEM; every global load is issued before the first store
-  constexpr int kWPer = (4096 + kBwdThreads - 1) / kBwdThreads;
+  // ---- weights: compute thread = row j of W_A, W_B, W_C (j < SH2 <= 256):
+  // [W_A|W_B] row j into TMEM, the projection B tiles and W_C^T into shared
+  // memory; the 32 threads of a warp hold 32 consecutive rows, so every
+  // transposed or swizzled store of a warp lands in one 128-byte row (no bank
+  // conflicts). Every global load is issued before the first store.
   {
     const int wh = warp >> 2;  // j-half of this compute warp's TMEM rows
     const int wj = 128 * wh + 32 * (warp & 3) + lane;
-    float4 wr[8];
+    const bool wok = warp < kComputeWarps && wj < SH2;
+    float4 wr[8], wcr[4];
     if (warp < kComputeWarps) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float* src = (q < 4 ? a.W_A : a.W_B) + wj * D + 4 * (q & 3);
-        wr[q] = wj < SH2 ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        wr[q] = wok ? __ldg(reinterpret_cast<const float4*>(src)) : z;
       }
-    }
-    float wa[kWPer], wb[kWPer], wc[kWPer];
 #pragma unroll
-    for (int u = 0; u < kWPer; ++u) {
-      const int i = tid + u * kBwdThreads;
-      const bool ok = i < SH2 * D;
-      wa[u] = ok ? __ldg(a.W_A + i) : 0.f;
-      wb[u] = ok ? __ldg(a.W_B + i) : 0.f;
-      wc[u] = ok ? __ldg(a.W_C + i) : 0.f;
+      for (int q = 0; q < 4; ++q) wcr[q] = wok ? __ldg(reinterpret_cast<const float4*>(a.W_C + wj * D + 4 * q)) : z;
     }
     // the first stages are requested after the weights, so that the weight
     // loads are not queued behind them
@@ -322,22 +319,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       tmem_st16(tw0 + 16u, hi + 16);
       tmem_st16(tw0 + 32u, lo);
       tmem_st16(tw0 + 48u, lo + 16);
-    }
+      if (wok) {
+        float* tile = sW + (wj >> 5) * FD * 32;
+        const int jj = wj & 31;
 #pragma unroll
-    for (int u = 0; u < kWPer; ++u) {
-      const int i = tid + u * kBwdThreads;
-      if (i >= SH2 * D) break;
-      const int j = i / D, d = i - (i / D) * D;
-      float* tile = sW + (j >> 5) * FD * 32;
-      const int jj = j & 31;
-      const float ha = tf32_rn(wa[u]), hb = tf32_rn(wb[u]);
-      tile[sw128_idx(d, jj)] = ha;
-      tile[sw128_idx(D + d, jj)] = hb;
-      tile[sw128_idx(TD + d, jj)] = wa[u] - ha;
-      tile[sw128_idx(TD + D + d, jj)] = wb[u] - hb;
-      sW_Ct[d * SH2 + j] = wc[u];
+        for (int d = 0; d < D; ++d) {
+          tile[sw128_idx(d, jj)] = hi[d];
+          tile[sw128_idx(D + d, jj)] = hi[D + d];
+          tile[sw128_idx(TD + d, jj)] = lo[d];
+          tile[sw128_idx(TD + D + d, jj)] = lo[D + d];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          sW_Ct[(4 * q) * SH2 + wj] = wcr[q].x;
+          sW_Ct[(4 * q + 1) * SH2 + wj] = wcr[q].y;
+          sW_Ct[(4 * q + 2) * SH2 + wj] = wcr[q].z;
+          sW_Ct[(4 * q + 3) * SH2 + wj] = wcr[q].w;
+        }
+      }
+      tmem_st_wait();
     }
-    if (warp < kComputeWarps) tmem_st_wait();
   }
   fence_proxy_async_smem();
   tc_fence_before();

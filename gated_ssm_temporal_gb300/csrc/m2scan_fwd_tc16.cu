@@ -178,18 +178,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     }
   };
 
-  // ---- weights: projection B tiles, W_C^T and W_O into shared memory
-  constexpr int kWPer = (4096 + kFwdThreads - 1) / kFwdThreads;
+  // ---- weights: projection B tiles, W_C^T and W_O into shared memory.
+  // Thread = (state quad dq, row j), j fastest: one float4 of each of W_A, W_B,
+  // W_C row j, so that the transposed and swizzled stores of a warp go to 32
+  // consecutive columns (no bank conflicts); W_O is copied as float4.
+  constexpr int kWPer = (256 * 4 + kFwdThreads - 1) / kFwdThreads;  // SH2 x D/4 items, SH2 <= 256
   {
-    float wa[kWPer], wb[kWPer], wc[kWPer], wo[kWPer];
+    float4 wa[kWPer], wb[kWPer], wc[kWPer], wo[kWPer];
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
       const int i = tid + u * kFwdThreads;
-      const bool ok = i < SH2 * D;
-      wa[u] = ok ? __ldg(a.W_A + i) : 0.f;
-      wb[u] = ok ? __ldg(a.W_B + i) : 0.f;
-      wc[u] = ok ? __ldg(a.W_C + i) : 0.f;
-      wo[u] = ok ? __ldg(a.W_O + i) : 0.f;
+      const bool ok = i < SH2 * 4;
+      const int j = i % SH2, dq = i / SH2;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      wa[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_A + j * D + 4 * dq)) : z;
+      wb[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_B + j * D + 4 * dq)) : z;
+      wc[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_C + j * D + 4 * dq)) : z;
+      wo[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_O) + i) : z;
     }
     // the first stages are requested after the weights, so that the weight
     // loads are not queued behind them
@@ -198,17 +203,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
 #pragma unroll
     for (int u = 0; u < kWPer; ++u) {
       const int i = tid + u * kFwdThreads;
-      if (i >= SH2 * D) break;
-      const int j = i / D, d = i - (i / D) * D;
+      if (i >= SH2 * 4) break;
+      const int j = i % SH2, dq = i / SH2;
       float* tile = sW + (j >> 5) * FD * 32;
       const int jj = j & 31;
-      const float ha = tf32_rn(wa[u]), hb = tf32_rn(wb[u]);
-      tile[sw128_idx(d, jj)] = ha;
-      tile[sw128_idx(D + d, jj)] = hb;
-      tile[sw128_idx(TD + d, jj)] = wa[u] - ha;
-      tile[sw128_idx(TD + D + d, jj)] = wb[u] - hb;
-      sW_Ct[d * SH2 + j] = wc[u];
-      sW_O[i] = wo[u];
+      const float va[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+      const float vb[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+      const float vc[4] = {wc[u].x, wc[u].y, wc[u].z, wc[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 4 * dq + e;
+        const float ha = tf32_rn(va[e]), hb = tf32_rn(vb[e]);
+        tile[sw128_idx(d, jj)] = ha;
+        tile[sw128_idx(D + d, jj)] = hb;
+        tile[sw128_idx(TD + d, jj)] = va[e] - ha;
+        tile[sw128_idx(TD + D + d, jj)] = vb[e] - hb;
+        sW_Ct[d * SH2 + j] = vc[e];
+      }
+      sts4(sW_O + 4 * i, wo[u]);
     }
   }
   fence_proxy_async_smem();
