@@ -752,18 +752,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           if (cw_own) {
             const float* rowp = (cw_role == 0 ? hsb : gb) + 4 * cw_jq;
             const float* vecp = (cw_role == 0 ? sDC : sCtx) + s0 * D + 8 * cw_dh;
+            auto accumulate = [&](int s) {
+              const float4 hv = lds4(rowp + s * SH2);
+              const float4 v0 = lds4(vecp + s * D), v1 = lds4(vecp + s * D + 4);
+              const float hvv[4] = {hv.x, hv.y, hv.z, hv.w};
+              const float vvv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int s = 0; s < kBwdSampleItem; ++s)
-              if (s < ns) {
-                const float4 hv = lds4(rowp + s * SH2);
-                const float4 v0 = lds4(vecp + s * D), v1 = lds4(vecp + s * D + 4);
-                const float hvv[4] = {hv.x, hv.y, hv.z, hv.w};
-                const float vvv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+              for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int e = 0; e < 8; ++e) cacc[i][e] = fmaf(hvv[i], vvv[e], cacc[i][e]);
+            };
+            if (ns == kBwdSampleItem) {
+              // a full item: no per-sample condition, so the loads of later
+              // samples can be issued ahead of the products of earlier ones
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) cacc[i][e] = fmaf(hvv[i], vvv[e], cacc[i][e]);
-              }
+              for (int s = 0; s < kBwdSampleItem; ++s) accumulate(s);
+            } else {
+              for (int s = 0; s < ns; ++s) accumulate(s);
+            }
           }
           named_sync(1, kComputeThreads);  // h_s2 rows no longer needed: d_h_s2 goes there
           {
