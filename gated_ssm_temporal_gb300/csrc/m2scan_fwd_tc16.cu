@@ -17,9 +17,9 @@
 //            meanwhile.
 //   scan     x_t = sigmoid(A_t) x_{t-1} + B_t, one thread per (sample, state);
 //            ctx = C x_{K-1}.
-//   output   h_enriched = h_s2 + tw ctx . W_O over the tile's h_s2 rows, in
-//            place in their stage; the producer warp stores them before it
-//            reuses the stage.
+//   output   h_enriched = h_s2 + tw ctx . W_O from the tile's h_s2 rows
+//            (a stage of their own, loaded after the next tile's chunks),
+//            written straight to global memory.
 #include "m2scan_device.cuh"
 #include "m2scan_internal.h"
 
@@ -41,7 +41,7 @@ constexpr int kLoBufs = 3;
 struct FwdBars {
   uint64_t full[kMaxStages];     // producer -> all: stage loaded
   uint64_t empty[kMaxStages];    // chunk stage s free: main products done (commit) + compute read (arrive)
-  uint64_t outdone[kMaxStages];  // compute -> producer: output written over the h_s2 item in stage s
+  uint64_t outdone[kMaxStages];  // compute -> producer: h_s2 item in stage s read (one arrival per warp)
   uint64_t loready[kChunkRing];  // compute -> remainder MMA thread: chunk c read, h - trunc(h) in TMEM
   uint64_t lofree[kLoBufs];      // remainder MMA thread -> all: remainder buffer's products done
   uint64_t mdone[2];             // main MMA thread -> compute: main products of tile t (set t & 1) done
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
       mbar_init(&bb->empty[s], 2);
-      mbar_init(&bb->outdone[s], 1);
+      mbar_init(&bb->outdone[s], kComputeWarps);
     }
     for (int s = 0; s < kChunkRing; ++s) mbar_init(&bb->loready[s], kComputeWarps);
     for (int s = 0; s < kLoBufs; ++s) mbar_init(&bb->lofree[s], 1);
@@ -123,14 +123,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   const uint32_t tmem = bb->tslot;
 
   // ---- producer: in round u = 0 .. T the NC chunks of tile u (u < T), then
-  // the item of tile u - 1's h_s2 rows (u >= 1): the compute warps write the
-  // output of a tile over its h_s2 rows after the next tile's chunks, and the
-  // producer stores it before it reuses the stage
+  // the item of tile u - 1's h_s2 rows (u >= 1): the compute warps read a
+  // tile's h_s2 rows after the next tile's chunks and write its output
+  // straight to global memory
   RingPos lp, rp;
   uint32_t rch = 0;     // bit s: parity of the next empty[s] phase (chunks only)
   uint32_t rout = 0;    // bit s: parity of the next outdone[s] phase (h_s2 items only)
   int pn = 0, pround = 0, pit = 0;
-  int rn = 0, rround = 0, rit = 0;
+  int rround = 0, rit = 0;
   auto round_items = [&](int u) { return (u < T ? NC : 0) + (u >= 1 ? 1 : 0); };
   auto release_one = [&]() {
     if (rit < (rround < T ? NC : 0)) {
@@ -141,14 +141,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     } else {
       bounded_wait(&bb->outdone[rp.i], (rout >> rp.i) & 1u, a.err);
       rout ^= 1u << rp.i;
-      const long long tb0 = tile_start(rround - 1);
-      const int S_t = static_cast<int>(tile_start(rround) - tb0);
-      bulk_store(a.out0 + tb0 * SH2, stage_ptr(rp.i), static_cast<uint32_t>(S_t) * SH2 * 4u);
-      bulk_commit();
-      bulk_wait_read_all();
     }
     rp.next(NST);
-    ++rn;
     if (++rit == round_items(rround)) {
       rit = 0;
       ++rround;
@@ -232,8 +226,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       while (pround <= T) produce_one();
-      while (rn < pn) release_one();
-      bulk_wait_all();
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------- MMA: main products
@@ -318,9 +310,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     RingPos ip, lr, lf;
     int c = 0;
     PROF_DECL;
-    // ====== output of tile tt: h_enriched = h_s2 + tw ctx . W_O, in place over
-    // its h_s2 rows; runs after the next tile's chunks, while the MMA threads
-    // finish that tile's projections
+    // ====== output of tile tt: h_enriched = h_s2 + tw ctx . W_O from its h_s2
+    // rows, straight to global memory; runs after the next tile's chunks,
+    // while the MMA threads finish that tile's projections
     auto output_tile = [&](int tt) {
       const int S_t = static_cast<int>(tile_start(tt + 1) - tile_start(tt));
       {
@@ -363,19 +355,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
           for (int u = 0; u < 4; ++u) {
             const int s = sq + 4 * u;
             if (s < S_t) {
-              float* hp = hs + s * SH2 + 4 * jq;
-              float4 h = lds4(hp);
+              float4 h = lds4(hs + s * SH2 + 4 * jq);
               h.x = fmaf(a.tw, o[u].x, h.x);
               h.y = fmaf(a.tw, o[u].y, h.y);
               h.z = fmaf(a.tw, o[u].z, h.z);
               h.w = fmaf(a.tw, o[u].w, h.w);
-              sts4(hp, h);
+              *reinterpret_cast<float4*>(a.out0 + (tile_start(tt) + s) * SH2 + 4 * jq) = h;
             }
           }
         }
-        fence_proxy_async_smem();
-        named_sync(1, kComputeThreads);
-        if (tid == 0) mbar_arrive(&bb->outdone[st]);  // the producer stores it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bb->outdone[st]);  // per warp: its reads of the h_s2 rows are done
         PROF_END(10);
       }
     };
