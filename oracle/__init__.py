@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the gated temporal scan layer (test infrastructure).
+"""fp64 CPU oracle for the gated temporal scan layer and the bias-gradient
+column sum (test infrastructure).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package. The CUDA library never calls it and shares no
@@ -54,7 +55,8 @@ def open_library(path: str):
     lib.m2o_forward.argtypes = [dp] * 6 + [dbl, i64, i32, i32, i32, dp, i32]
     lib.m2o_backward.argtypes = ([dp] * 6 + [dbl, dp, i64, i32, i32, i32]
                                  + [dp] * 6 + [i32])
-    for f in (lib.m2o_scan_state, lib.m2o_forward, lib.m2o_backward):
+    lib.m2o_bias_grad.argtypes = [dp, i64, i32, dp, i32, dp]
+    for f in (lib.m2o_scan_state, lib.m2o_forward, lib.m2o_backward, lib.m2o_bias_grad):
         f.restype = ctypes.c_int
     return lib
 
@@ -132,4 +134,19 @@ def backward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, n_threads=No
         n_threads or default_threads())
     if rc:
         raise RuntimeError("oracle backward failed (%d)" % rc)
+    return out
+
+
+def bias_grad(dy, db=None, accumulate=False, lib=None):
+    """Column sums of dy [N, C] in float64 (plus db when accumulating): the
+    bias gradient of a fully connected layer."""
+    d = _f64(dy)
+    if d.ndim != 2:
+        raise ValueError("dy must be [N, C]")
+    N, C = d.shape
+    out = np.empty(C)
+    dbi = _f64(db) if accumulate else np.zeros(C)
+    rc = _load(lib).m2o_bias_grad(_ptr(d), N, C, _ptr(dbi), 1 if accumulate else 0, _ptr(out))
+    if rc:
+        raise RuntimeError("oracle bias_grad failed (%d)" % rc)
     return out

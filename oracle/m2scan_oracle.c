@@ -249,3 +249,27 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
   free(part);
   return fail;
 }
+
+/*
+ * Bias gradient of a fully connected layer: column sums of a row-major
+ * [N, C] matrix of upstream gradients,
+ *
+ *   db[c] = sum over rows r = 0 .. N-1 of dy[r, c]
+ *
+ * ("Phase 3 Kernel Optimization Implementation Plan", Task 2: the reduction
+ * over the batch of every output feature's gradient). The pages keep two
+ * conventions: the main network's backward adds the sum into db, the
+ * curiosity trainer (Task 3) overwrites grad_b; `accumulate` selects the
+ * first (db_out = db_in + sum), else db_out = sum. One fp64 accumulator per
+ * column, rows added in order.
+ */
+int m2o_bias_grad(const double* dy, int64_t N, int C, const double* db_in, int accumulate,
+                  double* db_out) {
+  if (N < 0 || C < 1 || (N > 0 && !dy) || !db_out || (accumulate && !db_in)) return 1;
+  for (int c = 0; c < C; c++) {
+    double acc = 0.0;
+    for (int64_t r = 0; r < N; r++) acc += dy[r * C + c];
+    db_out[c] = accumulate ? db_in[c] + acc : acc;
+  }
+  return 0;
+}
