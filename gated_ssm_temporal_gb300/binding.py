@@ -77,6 +77,10 @@ def load_library(path: str | None = None):
         lib.m2scan_read_device_flags.restype = ctypes.c_int
         lib.m2scan_last_launch_count.argtypes = []
         lib.m2scan_last_launch_count.restype = ctypes.c_int
+        lib.m2scan_bias_grad_workspace_bytes.argtypes = [i64, i32]
+        lib.m2scan_bias_grad_workspace_bytes.restype = sz
+        lib.m2scan_bias_grad.argtypes = [vp, i64, i32, vp, i32, vp, sz, vp]
+        lib.m2scan_bias_grad.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -109,6 +113,15 @@ NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 def m2scan_bwd_workspace_bytes(B, K, SH2, D):
     return load_library().m2scan_bwd_workspace_bytes(B, K, SH2, D)
+
+
+def m2scan_bias_grad_workspace_bytes(N, C):
+    return load_library().m2scan_bias_grad_workspace_bytes(N, C)
+
+
+def m2scan_bias_grad(dy, N, C, db, accumulate, workspace, workspace_bytes, stream=0):
+    return load_library().m2scan_bias_grad(dy, N, C, db, int(accumulate), workspace,
+                                           workspace_bytes, stream)
 
 
 def m2scan_status_str(status):
@@ -214,3 +227,25 @@ def bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, outs=None, worksp
     if st != M2SCAN_OK:
         raise M2ScanError(st, "m2scan_bwd")
     return outs
+
+
+def bias_grad(dy, db=None, accumulate=False, workspace=None, stream=None):
+    """db [C] = column sums of dy [N, C] (added into db when ``accumulate``);
+    float32 CUDA tensors, contiguous. Returns db."""
+    import torch
+    if dy.dim() != 2:
+        raise ValueError("dy must be [N, C]")
+    N, C = (int(v) for v in dy.shape)
+    if db is None:
+        if accumulate:
+            raise ValueError("accumulate needs db")
+        db = torch.empty((C,), device=dy.device, dtype=torch.float32)
+    need = m2scan_bias_grad_workspace_bytes(N, C)
+    if workspace is None:
+        workspace = torch.empty((max(1, need // 4),), device=dy.device, dtype=torch.float32)
+    st = m2scan_bias_grad(_check(dy, "dy", (N, C)), N, C, _check(db, "db", (C,)),
+                          accumulate, workspace.data_ptr(), workspace.numel() * 4,
+                          _stream(stream))
+    if st != M2SCAN_OK:
+        raise M2ScanError(st, "m2scan_bias_grad")
+    return db

@@ -280,6 +280,43 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
   return M2SCAN_OK;
 }
 
+size_t m2scan_bias_grad_workspace_bytes(int64_t N, int32_t C) {
+  if (N < 0 || C < 1 || static_cast<uint64_t>(N) * static_cast<uint64_t>(C) > (1ull << 40)) return 0;
+  if (N == 0) return 0;
+  return static_cast<size_t>(colsum_partials(N)) * static_cast<size_t>(C) * sizeof(float);
+}
+
+m2scan_status m2scan_bias_grad(const float* dy, int64_t N, int32_t C, float* db,
+                               int32_t accumulate, void* workspace, size_t workspace_bytes,
+                               m2scan_stream_t stream) {
+  t_last_launches = 0;
+  if (N < 0 || C < 1 || static_cast<uint64_t>(N) * static_cast<uint64_t>(C) > (1ull << 40))
+    return M2SCAN_ERR_SHAPE;
+  if (!db || (N > 0 && !dy)) return M2SCAN_ERR_NULL;
+  if (!aligned16(dy) || !aligned16(db)) return M2SCAN_ERR_ALIGN;
+  const size_t need = m2scan_bias_grad_workspace_bytes(N, C);
+  if (N > 0 && (!workspace || workspace_bytes < need)) return M2SCAN_ERR_WORKSPACE;
+  if (N > 0 && !aligned16(workspace)) return M2SCAN_ERR_ALIGN;
+  const Span out = span(db, static_cast<uint64_t>(C) * 4);
+  const Span in = span(dy, static_cast<uint64_t>(N) * C * 4);
+  const Span ws = span(workspace, N > 0 ? need : 0);
+  if (overlaps(out, in) || overlaps(out, ws) || overlaps(in, ws)) return M2SCAN_ERR_ALIAS;
+  int dev = 0;
+  m2scan_status st = prepare_device(&dev);
+  if (st != M2SCAN_OK) return st;
+  if (N == 0) {
+    if (accumulate) return M2SCAN_OK;  // adding an empty sum
+    const cudaError_t e = cudaMemsetAsync(db, 0, static_cast<size_t>(C) * 4, stream);
+    return e == cudaSuccess ? M2SCAN_OK : cuda_fail(e);
+  }
+  int n = 0;
+  const cudaError_t e = launch_colsum(dy, N, C, db, accumulate ? 1 : 0,
+                                      static_cast<float*>(workspace), stream, &n);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = n;
+  return M2SCAN_OK;
+}
+
 m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float* W_A,
                          const float* W_B, const float* W_C, const float* W_O, float tw,
                          const float* d_h_enriched, int64_t B, int32_t K, int32_t SH2,

@@ -115,6 +115,11 @@ cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem
 cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float* dW_B,
                           float* dW_C, float* dW_O, cudaStream_t stream);
 cudaError_t prepare_kernels(int max_smem_optin);
+// Bias-gradient column sum (two launches): partial sums of P = colsum_partials(N)
+// row ranges into part [P][C], then their fixed-order sum into db.
+int colsum_partials(long long N);
+cudaError_t launch_colsum(const float* dy, long long N, int C, float* db, int accumulate,
+                          float* part, cudaStream_t stream, int* n_launches);
 
 unsigned* device_error_word();  // device address of the error word (current device)
 

@@ -93,3 +93,29 @@ def algorithmic_bytes(B: int, K: int, SH2: int) -> dict:
     fwd = 4 * SH2 * (K + 2) * B
     bwd = 4 * SH2 * (2 * K + 3) * B
     return dict(fwd=fwd, bwd=bwd, total=fwd + bwd)
+
+
+# The bias-gradient column sum: the per-output-feature gradient dy [N, C] of
+# a fully connected layer of the pages' network ("Phase 3 Kernel Optimization
+# Implementation Plan": batch 8192, out_dim from 3 to 256 for the main
+# network, 42 and 128 for the curiosity module). Same generator: PCG64
+# ``default_rng(seed)`` float32 standard normals, one [N, C] draw.
+@dataclass(frozen=True)
+class BiasWorkload:
+    name: str
+    N: int
+    C: int
+    seed: int
+
+
+BIAS_WORKLOADS = {
+    "bias_fc": BiasWorkload("bias_fc", N=8192, C=256, seed=11),
+    "bias_narrow": BiasWorkload("bias_narrow", N=8192, C=3, seed=12),
+    "bias_curiosity_out": BiasWorkload("bias_curiosity_out", N=8192, C=42, seed=13),
+    "bias_curiosity_hidden": BiasWorkload("bias_curiosity_hidden", N=8192, C=128, seed=14),
+}
+
+
+def make_bias_input(N: int, C: int, seed: int):
+    """dy [N, C] float32 standard normals (C-contiguous)."""
+    return np.random.default_rng(seed).standard_normal((N, C), dtype=np.float32)

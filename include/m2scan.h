@@ -143,6 +143,33 @@ m2scan_status m2scan_bwd_noalloc(const float* h_history, const float* h_s2, cons
                                  float* dW_A, float* dW_B, float* dW_C, float* dW_O,
                                  m2scan_stream_t stream);
 
+/*
+ * Bias gradient of a fully connected layer ("Phase 3 Kernel Optimization
+ * Implementation Plan", Tasks 2 and 3): the column sums of a row-major fp32
+ * matrix dy [N, C],
+ *     db[c] = sum over r = 0 .. N-1 of dy[r, c]           (accumulate == 0)
+ *     db[c] = db[c] + sum over r of dy[r, c]              (accumulate != 0)
+ * The pages use both: their main backward adds into db, their curiosity
+ * trainer overwrites grad_b.
+ *   dy [N, C] (device, 16-byte aligned; rows need not be): input, N >= 0,
+ *       C >= 1, N * C <= 2^40.
+ *   db [C] (device, 16-byte aligned): output, read too when accumulating.
+ *   workspace: caller-owned device scratch of at least
+ *       m2scan_bias_grad_workspace_bytes(N, C) bytes, 16-byte aligned, for
+ *       the per-block partial sums; contents on entry do not matter. May be
+ *       NULL when N == 0.
+ * None of dy, db and workspace may overlap. Two kernel launches: partial
+ * sums of fixed row ranges (the split depends on N only), then their sum in
+ * range order, so db is bit-identical from run to run. N == 0: db is
+ * zero-filled with cudaMemsetAsync (or left alone when accumulating).
+ * Same error conventions as the layer calls (host checks, nothing launched
+ * on failure).
+ */
+size_t m2scan_bias_grad_workspace_bytes(int64_t N, int32_t C);
+m2scan_status m2scan_bias_grad(const float* dy, int64_t N, int32_t C, float* db,
+                               int32_t accumulate, void* workspace, size_t workspace_bytes,
+                               m2scan_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* m2scan_status_str(m2scan_status status);
 
@@ -169,8 +196,8 @@ int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
  */
 m2scan_status m2scan_read_device_flags(uint32_t* flags);
 
-/* Number of CUDA kernels launched by the most recent successful m2scan_fwd
- * or m2scan_bwd call on the calling thread. */
+/* Number of CUDA kernels launched by the most recent successful m2scan_fwd,
+ * m2scan_bwd or m2scan_bias_grad call on the calling thread. */
 int m2scan_last_launch_count(void);
 
 #ifdef __cplusplus

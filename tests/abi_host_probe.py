@@ -69,5 +69,32 @@ res["path_tiny"] = g.m2scan_path_for(8, 32, 4)
 res["path_wide"] = g.m2scan_path_for(16, 512, 64)
 res["path_K129"] = g.m2scan_path_for(129, 256, 16)
 res["path_huge"] = g.m2scan_path_for(100000, 256, 64)
+
+
+def bias(**kw):
+    N, C = kw.pop("N", 100), kw.pop("C", 7)
+    args = dict(dy=W[15], N=N, C=C, db=W[16], accumulate=0, workspace=W[17],
+                workspace_bytes=g.m2scan_bias_grad_workspace_bytes(N, C), stream=0)
+    args.update(kw)
+    return g.m2scan_bias_grad(**args)
+
+
+res["bg_null_db"] = bias(db=0)
+res["bg_null_dy"] = bias(dy=0)
+res["bg_C0"] = bias(C=0)
+res["bg_N_neg"] = bias(N=-1)
+res["bg_misaligned_dy"] = bias(dy=W[15] + 4)
+res["bg_misaligned_db"] = bias(db=W[16] + 8)
+res["bg_null_ws"] = bias(workspace=0)
+res["bg_short_ws"] = bias(workspace_bytes=g.m2scan_bias_grad_workspace_bytes(100, 7) - 4)
+res["bg_misaligned_ws"] = bias(workspace=W[17] + 4)
+res["bg_alias_db_dy"] = bias(db=W[15] + 32)
+res["bg_alias_ws_dy"] = bias(workspace=W[15] + 16)
+res["bg_alias_db_ws"] = bias(db=W[17])
+res["bg_ws_pages"] = g.m2scan_bias_grad_workspace_bytes(8192, 256)
+res["bg_ws_one"] = g.m2scan_bias_grad_workspace_bytes(1, 3)
+res["bg_ws_N0"] = g.m2scan_bias_grad_workspace_bytes(0, 5)
+res["bg_ws_big"] = g.m2scan_bias_grad_workspace_bytes(100000, 7)
+res["bg_ws_bad"] = g.m2scan_bias_grad_workspace_bytes(10, 0)
 res["status_str_ok"] = g.m2scan_status_str(0)
 print(json.dumps(res))

@@ -53,6 +53,10 @@ NULL, SHAPE, ALIGN, ALIAS, WORKSPACE = 1, 2, 3, 4, 5
     ("bwd_null_ws", WORKSPACE), ("bwd_short_ws", WORKSPACE), ("bwd_null_dWO", NULL),
     ("bwd_null_g", NULL), ("bwd_shape", SHAPE), ("bwd_misaligned_ws", ALIGN),
     ("bwd_alias_out_out", ALIAS), ("bwd_alias_ws_in", ALIAS), ("bwd_alias_dh_g", ALIAS),
+    ("bg_null_db", NULL), ("bg_null_dy", NULL), ("bg_C0", SHAPE), ("bg_N_neg", SHAPE),
+    ("bg_misaligned_dy", ALIGN), ("bg_misaligned_db", ALIGN), ("bg_null_ws", WORKSPACE),
+    ("bg_short_ws", WORKSPACE), ("bg_misaligned_ws", ALIGN), ("bg_alias_db_dy", ALIAS),
+    ("bg_alias_ws_dy", ALIAS), ("bg_alias_db_ws", ALIAS),
 ])
 def test_host_validation(probe, key, expect):
     assert probe[key] == expect, (key, probe[key])
@@ -65,6 +69,15 @@ def test_workspace_query(probe):
     assert probe["ws_bytes_bad"] == 0
     # wide states: 38 slots plus dA|dB [B*K][128] and [dC | ctx] [B][128]
     assert probe["ws_bytes_wide"] == (38 * 4 * 512 * 64 + 16384 * 16 * 128 + 16384 * 128) * 4
+
+
+def test_bias_grad_workspace_query(probe):
+    # one partial per column for each range of about 64 rows, at most 152 ranges
+    assert probe["bg_ws_pages"] == 128 * 256 * 4
+    assert probe["bg_ws_one"] == 1 * 3 * 4
+    assert probe["bg_ws_N0"] == 0
+    assert probe["bg_ws_big"] == 152 * 7 * 4
+    assert probe["bg_ws_bad"] == 0
 
 
 def test_path_choice(probe):
