@@ -8,9 +8,12 @@ timed intervals, so both read their inputs from HBM. Each rank times K steps
 with CUDA events on its stream; the line reports the maximum over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                  [--workload pages|long_history|wide_state|stress|tiny|bias_fc|...]
 
 Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
-(the only reference the layer has) on the host cores instead.
+(the only reference the layer has) on the host cores instead. The ``bias_*``
+workloads time the bias-gradient column sum (m2scan_bias_grad) instead of the
+layer: one step = one call over dy [N, C], L2 flushed before each.
 """
 from __future__ import annotations
 
@@ -430,13 +433,177 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ bias-gradient column sum
+
+def bias_metric(w) -> str:
+    return "bias-gradient column sum GB/s of dy (N=%d, C=%d)" % (w.N, w.C)
+
+
+def run_bias_native(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import gated_ssm_temporal_gb300 as g
+    from gated_ssm_temporal_gb300 import build as gbuild
+    from gated_ssm_temporal_gb300.workloads import BIAS_WORKLOADS, make_bias_input
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    gbuild.build()
+    g.load_library()
+    w = BIAS_WORKLOADS[args.workload]
+    N, C = w.N, w.C
+    dy_h = make_bias_input(N, C, w.seed + rank)
+    dev = torch.device("cuda", local)
+    dy = torch.from_numpy(dy_h).to(dev)
+    db = torch.empty((C,), device=dev)
+    ws = torch.empty((max(1, g.m2scan_bias_grad_workspace_bytes(N, C) // 4),), device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def call(src, dst):
+        g.bias_grad(src, dst, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call(dy, db)
+    torch.cuda.synchronize()
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    sampler = ClockSampler()
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(dist, local)
+    torch.cuda.synchronize()
+    launches = 0
+    wall0 = time.perf_counter()
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call(dy, db)
+        launches += g.m2scan_last_launch_count()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop(gpus=list(range(max(world, 1)))) if rank == 0 else None
+    t_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    (t_ms,) = max_over_ranks(dist, [t_ms], device=dev)
+    nbytes = N * C * 4
+    value = nbytes * world / (t_ms / 1e3) / 1e9
+
+    # end to end through the same call: dy copied in from pinned host memory,
+    # db copied back, every step (copy-in of step i+1 overlaps step i)
+    host_dy = torch.from_numpy(dy_h).pin_memory()
+    host_db = torch.empty((C,)).pin_memory()
+    dev_dy = [dy, torch.empty_like(dy)]
+    s_in = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    cnt = [0]
+
+    def e2e_step():
+        b = cnt[0] & 1
+        cnt[0] += 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_done[b])
+            dev_dy[b].copy_(host_dy, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        call(dev_dy[b], db)
+        host_db.copy_(db, non_blocking=True)
+        ev_done[b].record(stream)
+
+    for _ in range(4):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    (e2e_ms,) = max_over_ranks(dist, [e2e_ms], device=dev)
+    if rank != 0:
+        return
+    peak, peak_src = measured_peaks()
+    achieved = nbytes / (t_ms / 1e3) / 1e9
+    line = {
+        "metric": bias_metric(w), "value": value, "unit": "GB/s", "n_gpus": world, "steps": n,
+        "warmup": max(3, args.warmup), "ms_per_step": t_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "%s: N=%d C=%d per rank" % (w.name, N, C), "N": N, "C": C,
+                   "parallelism": "replicas x%d" % world,
+                   "l2": "flushed (512 MiB write) before every timed call"},
+        "roofline": {"kernel": "m2scan_bias_grad (partial sums + ordered final sum)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src + " hbm_gbs burst", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "algorithmic_bytes": nbytes},
+        "e2e": {"value": nbytes * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": C * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        done, t0 = 0, time.perf_counter()
+        while True:
+            oracle.bias_grad(dy_h)
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= min(args.cpu_seconds, 5.0):
+                break
+        line["cpu_baseline"] = {"value": nbytes * done / el / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": "%d passes over the full [%d, %d] matrix (%.1f s)"
+                                          % (done, N, C, el)}
+    print(json.dumps(line), flush=True)
+
+
+def run_bias_reference(args, rank, world):
+    """The fp64 oracle column sum on the host (one core: a plain loop), rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    from gated_ssm_temporal_gb300.workloads import BIAS_WORKLOADS, make_bias_input
+    w = BIAS_WORKLOADS[args.workload]
+    dy = make_bias_input(w.N, w.C, w.seed)
+    for _ in range(max(0, args.warmup)):
+        oracle.bias_grad(dy)
+    done, t0 = 0, time.perf_counter()
+    while done < max(1, args.steps):
+        oracle.bias_grad(dy)
+        done += 1
+        if time.perf_counter() - t0 > 60.0:  # keep the run within about a minute
+            break
+    el = time.perf_counter() - t0
+    value = w.N * w.C * 4 * done / el / 1e9
+    line = {
+        "impl": "reference", "metric": bias_metric(w), "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": done, "warmup": args.warmup, "ms_per_step": el / done * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "%s: N=%d C=%d" % (w.name, w.N, w.C), "N": w.N, "C": w.C},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "the full matrix per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
+    bias = args.workload.startswith("bias_")
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        (run_bias_reference if bias else run_reference)(args, rank, world)
     else:
-        run_native(args, rank, world, local)
+        (run_bias_native if bias else run_native)(args, rank, world, local)
 
 
 if __name__ == "__main__":

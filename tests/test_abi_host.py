@@ -72,8 +72,8 @@ def test_workspace_query(probe):
 
 
 def test_bias_grad_workspace_query(probe):
-    # one partial per column for each range of about 64 rows, at most 152 ranges
-    assert probe["bg_ws_pages"] == 128 * 256 * 4
+    # one partial per column for each range of about 16 rows, at most 152 ranges
+    assert probe["bg_ws_pages"] == 152 * 256 * 4
     assert probe["bg_ws_one"] == 1 * 3 * 4
     assert probe["bg_ws_N0"] == 0
     assert probe["bg_ws_big"] == 152 * 7 * 4

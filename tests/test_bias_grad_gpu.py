@@ -2,9 +2,10 @@
 
 Tolerance: the kernels add fp32 values; every input reaches its column's
 result through at most L additions (its position in a thread's row sum, the
-row phases of its column, the range partials of one lane, the lane combine,
-and the add into db), so |got - exact| <= L * 2^-24 * (sum |dy| + |db|) to
-first order. L is computed from the shapes with the kernels' row split.
+pairwise tree over the row phases of its column, the range partials of one
+lane, the lane combine, and the add into db), so
+|got - exact| <= L * 2^-24 * (sum |dy| + |db|) to first order. L is computed
+from the shapes with the kernels' row split.
 """
 import math
 
@@ -24,13 +25,14 @@ def depth(N, C, accumulate):
     """Largest number of fp32 additions between an input and its column's result."""
     if N == 0:
         return 1
-    P = min(152, max(1, -(-N // 64)))
+    P = min(152, max(1, -(-N // 16)))
     rows = -(-N // P)  # rows of the largest range
+    L = C // 4 if C % 4 == 0 else C  # lanes per row: column quads or columns
     worst = 0
-    for c0 in range(0, C, 256):
-        cb = min(256, C - c0)
+    for l0 in range(0, L, 256):
+        cb = min(256, L - l0)
         RY = 256 // cb
-        worst = max(worst, -(-rows // RY) + RY - 1)
+        worst = max(worst, -(-rows // RY) + math.ceil(math.log2(RY)))
     return worst + -(-P // 8) + 7 + (1 if accumulate else 0)
 
 
