@@ -51,9 +51,9 @@ def open_library(path: str):
     lib = ctypes.CDLL(path)
     dp = ctypes.POINTER(ctypes.c_double)
     i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-    lib.m2o_scan_state.argtypes = [dp] * 5 + [i64, i32, i32, i32] + [dp] * 5
-    lib.m2o_forward.argtypes = [dp] * 6 + [dbl, i64, i32, i32, i32, dp, i32]
-    lib.m2o_backward.argtypes = ([dp] * 6 + [dbl, dp, i64, i32, i32, i32]
+    lib.m2o_scan_state.argtypes = [dp] * 5 + [i64, i32, i32, i32, dbl] + [dp] * 5
+    lib.m2o_forward.argtypes = [dp] * 6 + [dbl, i64, i32, i32, i32, dbl, dp, i32]
+    lib.m2o_backward.argtypes = ([dp] * 6 + [dbl, dp, i64, i32, i32, i32, dbl]
                                  + [dp] * 6 + [i32])
     lib.m2o_bias_grad.argtypes = [dp, i64, i32, dp, i32, dp]
     for f in (lib.m2o_scan_state, lib.m2o_forward, lib.m2o_backward, lib.m2o_bias_grad):
@@ -90,26 +90,28 @@ def _dims(h_history, W_A):
     return B, K, SH2, D
 
 
-def scan_state(h_history, h_s2, W_A, W_B, W_C, lib=None):
-    """Per-sample intermediates: A, Bv, x (all [B,K,D]) and C, ctx ([B,D])."""
+def scan_state(h_history, h_s2, W_A, W_B, W_C, lib=None, gate_scale=1.0):
+    """Per-sample intermediates: A, Bv, x (all [B,K,D]) and C, ctx ([B,D]).
+    ``gate_scale`` multiplies every gate (the pages' optional gate multiplier)."""
     h, hs, wa, wb, wc = map(_f64, (h_history, h_s2, W_A, W_B, W_C))
     B, K, SH2, D = _dims(h, wa)
     A = np.empty((B, K, D)); Bv = np.empty((B, K, D)); x = np.empty((B, K, D))
     C = np.empty((B, D)); ctx = np.empty((B, D))
     rc = _load(lib).m2o_scan_state(_ptr(h), _ptr(hs), _ptr(wa), _ptr(wb), _ptr(wc),
-                                B, K, SH2, D, _ptr(A), _ptr(Bv), _ptr(x), _ptr(C), _ptr(ctx))
+                                B, K, SH2, D, float(gate_scale), _ptr(A), _ptr(Bv), _ptr(x),
+                                _ptr(C), _ptr(ctx))
     if rc:
         raise RuntimeError("oracle scan_state failed (%d)" % rc)
     return A, Bv, x, C, ctx
 
 
-def forward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, n_threads=None, lib=None):
-    """h_enriched [B,SH2] in float64."""
+def forward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, n_threads=None, lib=None, gate_scale=1.0):
+    """h_enriched [B,SH2] in float64; ``gate_scale`` multiplies every gate."""
     h, hs, wa, wb, wc, wo = map(_f64, (h_history, h_s2, W_A, W_B, W_C, W_O))
     B, K, SH2, D = _dims(h, wa)
     out = np.empty((B, SH2))
     rc = _load(lib).m2o_forward(_ptr(h), _ptr(hs), _ptr(wa), _ptr(wb), _ptr(wc), _ptr(wo),
-                             float(tw), B, K, SH2, D, _ptr(out),
+                             float(tw), B, K, SH2, D, float(gate_scale), _ptr(out),
                              n_threads or default_threads())
     if rc:
         raise RuntimeError("oracle forward failed (%d)" % rc)
@@ -117,8 +119,9 @@ def forward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, n_threads=None, lib=None):
 
 
 def backward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, n_threads=None,
-             lib=None):
-    """Returns dict of float64 arrays: d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O."""
+             lib=None, gate_scale=1.0):
+    """Returns dict of float64 arrays: d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O.
+    ``gate_scale`` multiplies every gate (a constant: it gets no gradient)."""
     h, hs, wa, wb, wc, wo, g = map(_f64, (h_history, h_s2, W_A, W_B, W_C, W_O,
                                          d_h_enriched))
     B, K, SH2, D = _dims(h, wa)
@@ -129,7 +132,7 @@ def backward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, n_threads=No
     }
     rc = _load(lib).m2o_backward(
         _ptr(h), _ptr(hs), _ptr(wa), _ptr(wb), _ptr(wc), _ptr(wo), float(tw), _ptr(g),
-        B, K, SH2, D, _ptr(out["d_h_history"]), _ptr(out["d_h_s2"]), _ptr(out["dW_A"]),
+        B, K, SH2, D, float(gate_scale), _ptr(out["d_h_history"]), _ptr(out["d_h_s2"]), _ptr(out["dW_A"]),
         _ptr(out["dW_B"]), _ptr(out["dW_C"]), _ptr(out["dW_O"]),
         n_threads or default_threads())
     if rc:

@@ -63,10 +63,13 @@
 static double sigmoid(double a) { return 1.0 / (1.0 + exp(-a)); }
 
 /* Projections and forward scan of one sample. A, Bv, sig, x are [K,D]; C and
- * ctx are [D]. x[t] is the state after step t. */
+ * ctx are [D]. x[t] is the state after step t; sig[t] = sigmoid(A[t]) before
+ * the gate scale gs (the pages' optional gate multiplier, "Custom Kernel
+ * Optimization Implementation Plan", Task 1: gate *= isv_signals[11]; 1 when
+ * absent), so the gate of step t is gs * sig[t]. */
 static void sample_forward(const double* h, const double* hs, const double* W_A,
                            const double* W_B, const double* W_C, int K, int SH2,
-                           int D, double* A, double* Bv, double* sig, double* x,
+                           int D, double gs, double* A, double* Bv, double* sig, double* x,
                            double* C, double* ctx) {
   for (int t = 0; t < K; t++) {
     for (int s = 0; s < D; s++) {
@@ -89,7 +92,7 @@ static void sample_forward(const double* h, const double* hs, const double* W_A,
     for (int t = 0; t < K; t++) {
       double g = sigmoid(A[t * D + s]);
       sig[t * D + s] = g;
-      xs = g * xs + Bv[t * D + s];
+      xs = gs * g * xs + Bv[t * D + s];
       x[t * D + s] = xs;
     }
     ctx[s] = C[s] * xs;
@@ -100,12 +103,12 @@ static void sample_forward(const double* h, const double* hs, const double* W_A,
  * A, Bv, x: [B,K,D]; C, ctx: [B,D]. */
 int m2o_scan_state(const double* h_history, const double* h_s2, const double* W_A,
                    const double* W_B, const double* W_C, int64_t B, int K, int SH2,
-                   int D, double* A, double* Bv, double* x, double* C, double* ctx) {
+                   int D, double gs, double* A, double* Bv, double* x, double* C, double* ctx) {
   if (B < 0 || K < 1 || SH2 < 1 || D < 1) return 1;
   double* sig = (double*)malloc(sizeof(double) * (size_t)K * D);
   if (!sig) return 2;
   for (int64_t b = 0; b < B; b++) {
-    sample_forward(h_history + b * K * SH2, h_s2 + b * SH2, W_A, W_B, W_C, K, SH2, D,
+    sample_forward(h_history + b * K * SH2, h_s2 + b * SH2, W_A, W_B, W_C, K, SH2, D, gs,
                    A + b * K * D, Bv + b * K * D, sig, x + b * K * D, C + b * D,
                    ctx + b * D);
   }
@@ -115,7 +118,8 @@ int m2o_scan_state(const double* h_history, const double* h_s2, const double* W_
 
 int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
                 const double* W_B, const double* W_C, const double* W_O, double tw,
-                int64_t B, int K, int SH2, int D, double* h_enriched, int n_threads) {
+                int64_t B, int K, int SH2, int D, double gs, double* h_enriched,
+                int n_threads) {
   if (B < 0 || K < 1 || SH2 < 1 || D < 1) return 1;
   if (n_threads < 1) n_threads = 1;
   int fail = 0;
@@ -132,7 +136,7 @@ int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
       double *A = buf, *Bv = A + K * D, *sig = Bv + K * D, *x = sig + K * D;
       double *C = x + K * D, *ctx = C + D;
       const double* hs = h_s2 + b * SH2;
-      sample_forward(h_history + b * K * SH2, hs, W_A, W_B, W_C, K, SH2, D, A, Bv,
+      sample_forward(h_history + b * K * SH2, hs, W_A, W_B, W_C, K, SH2, D, gs, A, Bv,
                      sig, x, C, ctx);
       for (int j = 0; j < SH2; j++) {
         double o = 0.0;
@@ -147,7 +151,7 @@ int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
 
 int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
                  const double* W_B, const double* W_C, const double* W_O, double tw,
-                 const double* d_h_enriched, int64_t B, int K, int SH2, int D,
+                 const double* d_h_enriched, int64_t B, int K, int SH2, int D, double gs,
                  double* d_h_history, double* d_h_s2, double* dW_A, double* dW_B,
                  double* dW_C, double* dW_O, int n_threads) {
   if (B < 0 || K < 1 || SH2 < 1 || D < 1) return 1;
@@ -179,7 +183,7 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
         const double* h = h_history + b * K * SH2;
         const double* hs = h_s2 + b * SH2;
         const double* g = d_h_enriched + b * SH2;
-        sample_forward(h, hs, W_A, W_B, W_C, K, SH2, D, A, Bv, sig, x, C, ctx);
+        sample_forward(h, hs, W_A, W_B, W_C, K, SH2, D, gs, A, Bv, sig, x, C, ctx);
         /* output step */
         for (int s = 0; s < D; s++) {
           double acc = 0.0;
@@ -188,15 +192,16 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
           for (int j = 0; j < SH2; j++) pO[(int64_t)s * SH2 + j] += tw * ctx[s] * g[j];
           dC[s] = dctx[s] * x[(K - 1) * D + s];
         }
-        /* reverse scan */
+        /* reverse scan; the gate of step t is gs * sigmoid(A[t]) (same plan,
+         * Task 2: d_gate and d_x both carry the stability factor) */
         for (int s = 0; s < D; s++) {
           double dx = dctx[s] * C[s];
           for (int t = K - 1; t >= 0; t--) {
             double gt = sig[t * D + s];
             double xprev = (t > 0) ? x[(t - 1) * D + s] : 0.0;
             dBv[t * D + s] = dx;
-            dA[t * D + s] = dx * xprev * gt * (1.0 - gt);
-            dx = dx * gt;
+            dA[t * D + s] = dx * xprev * gs * gt * (1.0 - gt);
+            dx = dx * gs * gt;
           }
         }
         /* weight gradients */

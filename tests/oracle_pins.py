@@ -11,7 +11,10 @@ raises AssertionError when the oracle disagrees with:
   * linearity of h_enriched - h_s2 in tw, W_O, W_C and W_B,
   * float64 autograd of the same layer written with torch operators,
   * the hand-derived example in tests/golden/hand_k2.txt,
-  * independence from the number of threads.
+  * independence from the number of threads,
+  * for the optional gate multiplier g (every gate g * sig(A_t), the pages'
+    isv_signals[11]): the closed form with g, central differences and torch
+    autograd with g, and g = 1 giving the plain layer bit for bit.
 ``tests/test_oracle_mutants.py`` plants mistakes in copies of the oracle and
 checks that these pins catch each one.
 """
@@ -234,6 +237,70 @@ def pin_thread_count_invariance(lib=None):
     assert np.array_equal(fwd(x, lib, n_threads=1), fwd(x, lib, n_threads=4))
 
 
+def pin_gate_scale_closed_form(lib=None):
+    """x_{K-1} = sum_t (prod_{u>t} g sig(A_u)) B_t with a gate multiplier g."""
+    gs = 0.6
+    x = rand_inputs(4, 5, 7, 3, 13, wscale=2.0)
+    h, hs = x["h_history"], x["h_s2"]
+    sig = sigmoid(h @ x["W_A"])
+    Bv = h @ x["W_B"]
+    K = h.shape[1]
+    xk = np.zeros((h.shape[0], x["W_A"].shape[1]))
+    for t in range(K):
+        xk += np.prod(gs * sig[:, t + 1:, :], axis=1) * Bv[:, t, :]
+    _, _, ox, oC, _ = oracle.scan_state(h, hs, x["W_A"], x["W_B"], x["W_C"], lib=lib,
+                                        gate_scale=gs)
+    close(ox[:, K - 1, :], xk, 1e-12, 1e-13, "closed-form x_{K-1} with a gate multiplier")
+    y = hs + x["tw"] * ((oC * xk) @ x["W_O"])
+    close(fwd(x, lib, gate_scale=gs), y, 1e-12, 1e-13, "output with a gate multiplier")
+    # g = 1 is the plain layer, bit for bit
+    assert np.array_equal(fwd(x, lib, gate_scale=1.0), fwd(x, lib))
+    g1, g0 = bwd(x, lib, gate_scale=1.0), bwd(x, lib)
+    for k in g0:
+        assert np.array_equal(g1[k], g0[k]), "gate multiplier 1 changed %s" % k
+
+
+def pin_gate_scale_gradients(lib=None):
+    """All six gradients with a gate multiplier: central differences and torch autograd."""
+    import torch
+    gs = 0.7
+    x = rand_inputs(2, 3, 4, 3, 14, wscale=2.0)
+    g = bwd(x, lib, gate_scale=gs)
+    dy = x["d_h_enriched"]
+
+    def loss(xx):
+        return float(np.sum(dy * fwd(xx, lib, gate_scale=gs)))
+
+    eps = 1e-6
+    for p in PARAMS:
+        num = np.zeros_like(x[p])
+        flat = num.reshape(-1)
+        for i in range(flat.size):
+            xp = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in x.items()}
+            xm = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in x.items()}
+            xp[p].reshape(-1)[i] += eps
+            xm[p].reshape(-1)[i] -= eps
+            flat[i] = (loss(xp) - loss(xm)) / (2 * eps)
+        close(g[GRADS[p]], num, 1e-6, 1e-8, "finite differences d%s with a gate multiplier" % p)
+    x = rand_inputs(3, 6, 9, 4, 15, wscale=3.0)
+    t = {k: torch.tensor(x[k], dtype=torch.float64, requires_grad=True) for k in PARAMS}
+    A = t["h_history"] @ t["W_A"]
+    Bv = t["h_history"] @ t["W_B"]
+    C = t["h_s2"] @ t["W_C"]
+    state = torch.zeros(3, 4, dtype=torch.float64)
+    for k in range(6):
+        state = gs * torch.sigmoid(A[:, k]) * state + Bv[:, k]
+    y = t["h_s2"] + x["tw"] * ((C * state) @ t["W_O"])
+    (y * torch.tensor(x["d_h_enriched"])).sum().backward()
+    close(fwd(x, lib, gate_scale=gs), y.detach().numpy(), 1e-12, 1e-13,
+          "autograd output with a gate multiplier")
+    g = bwd(x, lib, gate_scale=gs)
+    for p in PARAMS:
+        close(g[GRADS[p]], t[p].grad.numpy(), 1e-10, 1e-12,
+              "autograd d%s with a gate multiplier" % p)
+
+
 ALL_PINS = [pin_finite_differences, pin_closed_form_scan, pin_reverse_closed_form, pin_k1,
             pin_k2, pin_saturated_gates, pin_tw_zero, pin_linearity, pin_torch_autograd,
-            pin_golden_hand_example, pin_thread_count_invariance]
+            pin_golden_hand_example, pin_thread_count_invariance, pin_gate_scale_closed_form,
+            pin_gate_scale_gradients]

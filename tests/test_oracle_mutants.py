@@ -15,9 +15,11 @@ from oracle_pins import ALL_PINS
 SRC = os.path.join(os.path.dirname(oracle.__file__), "m2scan_oracle.c")
 
 MUTANTS = {
-    "gate_complement": ("xs = g * xs + Bv[t * D + s];", "xs = (1.0 - g) * xs + Bv[t * D + s];"),
+    "gate_complement": ("xs = gs * g * xs + Bv[t * D + s];",
+                        "xs = gs * (1.0 - g) * xs + Bv[t * D + s];"),
     "state_init_one": ("double xs = 0.0; /* x_{-1} = 0 */", "double xs = 1.0;"),
-    "drop_B_term": ("xs = g * xs + Bv[t * D + s];", "xs = g * xs + 0.0 * Bv[t * D + s];"),
+    "drop_B_term": ("xs = gs * g * xs + Bv[t * D + s];",
+                    "xs = gs * g * xs + 0.0 * Bv[t * D + s];"),
     "ctx_without_C": ("ctx[s] = C[s] * xs;", "ctx[s] = xs;"),
     "output_no_residual": ("h_enriched[b * SH2 + j] = hs[j] + tw * o;",
                            "h_enriched[b * SH2 + j] = tw * o;"),
@@ -26,9 +28,16 @@ MUTANTS = {
     "dctx_without_tw": ("dctx[s] = tw * acc;", "dctx[s] = acc;"),
     "dC_without_x": ("dC[s] = dctx[s] * x[(K - 1) * D + s];", "dC[s] = dctx[s];"),
     "dx_without_C": ("double dx = dctx[s] * C[s];", "double dx = dctx[s];"),
-    "dx_complement_gate": ("dx = dx * gt;", "dx = dx * (1.0 - gt);"),
-    "sigmoid_derivative_dropped": ("dA[t * D + s] = dx * xprev * gt * (1.0 - gt);",
-                                   "dA[t * D + s] = dx * xprev * gt;"),
+    "dx_complement_gate": ("dx = dx * gs * gt;", "dx = dx * gs * (1.0 - gt);"),
+    "sigmoid_derivative_dropped": ("dA[t * D + s] = dx * xprev * gs * gt * (1.0 - gt);",
+                                   "dA[t * D + s] = dx * xprev * gs * gt;"),
+    "gate_scale_dropped_forward": ("xs = gs * g * xs + Bv[t * D + s];",
+                                   "xs = g * xs + Bv[t * D + s];"),
+    "gate_scale_dropped_in_dA": ("dA[t * D + s] = dx * xprev * gs * gt * (1.0 - gt);",
+                                 "dA[t * D + s] = dx * xprev * gt * (1.0 - gt);"),
+    "gate_scale_dropped_in_dx": ("dx = dx * gs * gt;", "dx = dx * gt;"),
+    "gate_scale_squared_in_dA": ("dA[t * D + s] = dx * xprev * gs * gt * (1.0 - gt);",
+                                 "dA[t * D + s] = dx * xprev * gs * gs * gt * (1.0 - gt);"),
     "xprev_off_by_one": ("double xprev = (t > 0) ? x[(t - 1) * D + s] : 0.0;",
                          "double xprev = x[t * D + s];"),
     "dWB_uses_dA": ("sb += h[(int64_t)t * SH2 + j] * dBv[t * D + s];",
