@@ -57,6 +57,11 @@ def load_library(path: str | None = None):
                                  ctypes.c_float, ctypes.c_size_t)
         lib.m2scan_fwd.argtypes = [vp] * 6 + [f32, i64, i32, i32, i32, vp, vp]
         lib.m2scan_fwd.restype = ctypes.c_int
+        lib.m2scan_fwd_ex.argtypes = [vp] * 6 + [f32, vp, i64, i32, i32, i32, vp, vp]
+        lib.m2scan_fwd_ex.restype = ctypes.c_int
+        lib.m2scan_bwd_ex.argtypes = ([vp] * 6 + [f32, vp, vp, i64, i32, i32, i32] + [vp] * 6
+                                      + [vp, sz, vp])
+        lib.m2scan_bwd_ex.restype = ctypes.c_int
         lib.m2scan_bwd.argtypes = ([vp] * 6 + [f32, vp, i64, i32, i32, i32] + [vp] * 6
                                    + [vp, sz, vp])
         lib.m2scan_bwd.restype = ctypes.c_int
@@ -98,6 +103,21 @@ def m2scan_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2,
     return load_library().m2scan_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, float(tw),
                                      d_h_enriched, B, K, SH2, D, d_h_history, d_h_s2, dW_A,
                                      dW_B, dW_C, dW_O, workspace, workspace_bytes, stream)
+
+
+def m2scan_fwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, tw, gate_scale, B, K, SH2, D, h_enriched,
+                  stream=0):
+    return load_library().m2scan_fwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, float(tw), gate_scale,
+                                        B, K, SH2, D, h_enriched, stream)
+
+
+def m2scan_bwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, tw, gate_scale, d_h_enriched, B, K, SH2,
+                  D, d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, workspace_bytes,
+                  stream=0):
+    return load_library().m2scan_bwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, float(tw),
+                                        gate_scale, d_h_enriched, B, K, SH2, D, d_h_history,
+                                        d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace,
+                                        workspace_bytes, stream)
 
 
 def m2scan_bwd_noalloc(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2, D,
@@ -177,16 +197,22 @@ def dims_of(h_history, W_A):
     return B, K, SH2, int(W_A.shape[1])
 
 
-def fwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, out=None, stream=None):
-    """h_enriched [B,SH2] = layer forward; all tensors float32 CUDA, contiguous."""
+def _gate_ptr(gate_scale):
+    return 0 if gate_scale is None else _check(gate_scale, "gate_scale", (1,))
+
+
+def fwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, out=None, stream=None, gate_scale=None):
+    """h_enriched [B,SH2] = layer forward; all tensors float32 CUDA, contiguous.
+    ``gate_scale``: optional one-element tensor g multiplying every gate."""
     import torch
     B, K, SH2, D = dims_of(h_history, W_A)
     if out is None:
         out = torch.empty((B, SH2), device=h_history.device, dtype=torch.float32)
-    st = m2scan_fwd(_check(h_history, "h_history", (B, K, SH2)), _check(h_s2, "h_s2", (B, SH2)),
-                    _check(W_A, "W_A", (SH2, D)), _check(W_B, "W_B", (SH2, D)),
-                    _check(W_C, "W_C", (SH2, D)), _check(W_O, "W_O", (D, SH2)), tw, B, K, SH2,
-                    D, _check(out, "h_enriched", (B, SH2)), _stream(stream))
+    st = m2scan_fwd_ex(_check(h_history, "h_history", (B, K, SH2)), _check(h_s2, "h_s2", (B, SH2)),
+                       _check(W_A, "W_A", (SH2, D)), _check(W_B, "W_B", (SH2, D)),
+                       _check(W_C, "W_C", (SH2, D)), _check(W_O, "W_O", (D, SH2)), tw,
+                       _gate_ptr(gate_scale), B, K, SH2, D, _check(out, "h_enriched", (B, SH2)),
+                       _stream(stream))
     if st != M2SCAN_OK:
         raise M2ScanError(st, "m2scan_fwd")
     return out
@@ -207,18 +233,19 @@ def alloc_workspace(B, K, SH2, D, device):
 
 
 def bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, outs=None, workspace=None,
-        stream=None):
-    """Layer backward; returns dict d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O."""
+        stream=None, gate_scale=None):
+    """Layer backward; returns dict d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O.
+    ``gate_scale``: optional one-element tensor g multiplying every gate."""
     B, K, SH2, D = dims_of(h_history, W_A)
     if outs is None:
         outs = alloc_bwd_outputs(B, K, SH2, D, h_history.device)
     if workspace is None:
         workspace = alloc_workspace(B, K, SH2, D, h_history.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = m2scan_bwd(
+    st = m2scan_bwd_ex(
         _check(h_history, "h_history", (B, K, SH2)), _check(h_s2, "h_s2", (B, SH2)),
         _check(W_A, "W_A", (SH2, D)), _check(W_B, "W_B", (SH2, D)),
-        _check(W_C, "W_C", (SH2, D)), _check(W_O, "W_O", (D, SH2)), tw,
+        _check(W_C, "W_C", (SH2, D)), _check(W_O, "W_O", (D, SH2)), tw, _gate_ptr(gate_scale),
         _check(d_h_enriched, "d_h_enriched", (B, SH2)), B, K, SH2, D,
         _check(outs["d_h_history"], "d_h_history", (B, K, SH2)),
         _check(outs["d_h_s2"], "d_h_s2", (B, SH2)), _check(outs["dW_A"], "dW_A", (SH2, D)),

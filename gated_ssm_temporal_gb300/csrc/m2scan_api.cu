@@ -232,10 +232,10 @@ m2scan_status m2scan_read_device_flags(uint32_t* flags) {
   return M2SCAN_OK;
 }
 
-m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float* W_A,
-                         const float* W_B, const float* W_C, const float* W_O, float tw,
-                         int64_t B, int32_t K, int32_t SH2, int32_t D, float* h_enriched,
-                         m2scan_stream_t stream) {
+m2scan_status m2scan_fwd_ex(const float* h_history, const float* h_s2, const float* W_A,
+                            const float* W_B, const float* W_C, const float* W_O, float tw,
+                            const float* gate_scale, int64_t B, int32_t K, int32_t SH2,
+                            int32_t D, float* h_enriched, m2scan_stream_t stream) {
   t_last_launches = 0;
   m2scan_status st = check_shape(B, K, SH2, D);
   if (st != M2SCAN_OK) return st;
@@ -244,11 +244,12 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
   const void* ptrs[] = {h_history, h_s2, W_A, W_B, W_C, W_O, h_enriched};
   for (const void* p : ptrs)
     if (!aligned16(p)) return M2SCAN_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(gate_scale) & 3u) != 0) return M2SCAN_ERR_ALIGN;
   const uint64_t nw = static_cast<uint64_t>(SH2) * D * 4;
   const uint64_t nb = static_cast<uint64_t>(B) * SH2 * 4;
   const Span out = span(h_enriched, nb);
   const Span ins[] = {span(h_history, nb * K), span(h_s2, nb), span(W_A, nw), span(W_B, nw),
-                      span(W_C, nw), span(W_O, nw)};
+                      span(W_C, nw), span(W_O, nw), span(gate_scale, gate_scale ? 4 : 0)};
   for (const Span& s : ins)
     if (overlaps(out, s)) return M2SCAN_ERR_ALIAS;
   if (B == 0) return M2SCAN_OK;
@@ -262,22 +263,31 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
   if (path == 1) {
     fa.h_history = h_history; fa.h_s2 = h_s2; fa.g = nullptr;
     fa.W_A = W_A; fa.W_B = W_B; fa.W_C = W_C; fa.W_O = W_O;
-    fa.out0 = h_enriched; fa.out1 = nullptr; fa.ws = nullptr;
+    fa.out0 = h_enriched; fa.out1 = nullptr; fa.ws = nullptr; fa.gate_scale = gate_scale;
     fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, nullptr, B)) return M2SCAN_ERR_UNSUPPORTED;
     e = fa.tc == 2 ? launch_fwd_tc16(fa, grid, stream)
         : fa.tc    ? launch_fwd_tc(D, fa, grid, stream)
                    : launch_fast(false, D, fa, grid, stream);
   } else if (path == 3) {
-    e = launch_wide_fwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, B, K, SH2, h_enriched, stream);
+    e = launch_wide_fwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, B, K, SH2, h_enriched,
+                        gate_scale, stream);
   } else {
     GenericArgs ga{h_history, h_s2, nullptr, W_A, W_B, W_C, W_O, h_enriched, nullptr, nullptr,
-                   B, K, SH2, D, tw};
+                   B, K, SH2, D, tw, gate_scale};
     e = launch_generic(false, ga, grid, generic_smem_bytes(false, K, SH2, D), stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_launches = 1;
   return M2SCAN_OK;
+}
+
+m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float* W_A,
+                         const float* W_B, const float* W_C, const float* W_O, float tw,
+                         int64_t B, int32_t K, int32_t SH2, int32_t D, float* h_enriched,
+                         m2scan_stream_t stream) {
+  return m2scan_fwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, tw, nullptr, B, K, SH2, D,
+                       h_enriched, stream);
 }
 
 size_t m2scan_bias_grad_workspace_bytes(int64_t N, int32_t C) {
@@ -317,12 +327,12 @@ m2scan_status m2scan_bias_grad(const float* dy, int64_t N, int32_t C, float* db,
   return M2SCAN_OK;
 }
 
-m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float* W_A,
-                         const float* W_B, const float* W_C, const float* W_O, float tw,
-                         const float* d_h_enriched, int64_t B, int32_t K, int32_t SH2,
-                         int32_t D, float* d_h_history, float* d_h_s2, float* dW_A,
-                         float* dW_B, float* dW_C, float* dW_O, void* workspace,
-                         size_t workspace_bytes, m2scan_stream_t stream) {
+m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const float* W_A,
+                            const float* W_B, const float* W_C, const float* W_O, float tw,
+                            const float* gate_scale, const float* d_h_enriched, int64_t B,
+                            int32_t K, int32_t SH2, int32_t D, float* d_h_history,
+                            float* d_h_s2, float* dW_A, float* dW_B, float* dW_C, float* dW_O,
+                            void* workspace, size_t workspace_bytes, m2scan_stream_t stream) {
   t_last_launches = 0;
   m2scan_status st = check_shape(B, K, SH2, D);
   if (st != M2SCAN_OK) return st;
@@ -333,6 +343,7 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
                         d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace};
   for (const void* p : ptrs)
     if (!aligned16(p)) return M2SCAN_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(gate_scale) & 3u) != 0) return M2SCAN_ERR_ALIGN;
   const size_t need = m2scan_bwd_workspace_bytes(B, K, SH2, D);
   if (need > 0 && (!workspace || workspace_bytes < need)) return M2SCAN_ERR_WORKSPACE;
   const uint64_t nw = static_cast<uint64_t>(SH2) * D * 4;
@@ -340,7 +351,8 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
   const Span outs[] = {span(d_h_history, nb * K), span(d_h_s2, nb), span(dW_A, nw),
                        span(dW_B, nw), span(dW_C, nw), span(dW_O, nw), span(workspace, need)};
   const Span ins[] = {span(h_history, nb * K), span(h_s2, nb), span(W_A, nw), span(W_B, nw),
-                      span(W_C, nw), span(W_O, nw), span(d_h_enriched, nb)};
+                      span(W_C, nw), span(W_O, nw), span(d_h_enriched, nb),
+                      span(gate_scale, gate_scale ? 4 : 0)};
   for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
     for (const Span& s : ins)
       if (overlaps(outs[i], s)) return M2SCAN_ERR_ALIAS;
@@ -366,20 +378,20 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
   if (path == 1) {
     fa.h_history = h_history; fa.h_s2 = h_s2; fa.g = d_h_enriched;
     fa.W_A = W_A; fa.W_B = W_B; fa.W_C = W_C; fa.W_O = W_O;
-    fa.out0 = d_h_history; fa.out1 = d_h_s2; fa.ws = ws;
+    fa.out0 = d_h_history; fa.out1 = d_h_s2; fa.ws = ws; fa.gate_scale = gate_scale;
     fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, d_h_enriched, B)) return M2SCAN_ERR_UNSUPPORTED;
     e = fa.tc ? launch_bwd_tc(fa, grid, stream) : launch_fast(true, D, fa, grid, stream);
   } else if (path == 3) {
     int n = 0;
     e = launch_wide_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2, d_h_history,
-                        d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, stream, &n);
+                        d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, gate_scale, stream, &n);
     t_last_launches = n;
     if (e != cudaSuccess) return cuda_fail(e);
     return M2SCAN_OK;
   } else {
     GenericArgs ga{h_history, h_s2, d_h_enriched, W_A, W_B, W_C, W_O, d_h_history, d_h_s2, ws,
-                   B, K, SH2, D, tw};
+                   B, K, SH2, D, tw, gate_scale};
     e = launch_generic(true, ga, grid, generic_smem_bytes(true, K, SH2, D), stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
@@ -387,6 +399,17 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_launches = 2;
   return M2SCAN_OK;
+}
+
+m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float* W_A,
+                         const float* W_B, const float* W_C, const float* W_O, float tw,
+                         const float* d_h_enriched, int64_t B, int32_t K, int32_t SH2,
+                         int32_t D, float* d_h_history, float* d_h_s2, float* dW_A,
+                         float* dW_B, float* dW_C, float* dW_O, void* workspace,
+                         size_t workspace_bytes, m2scan_stream_t stream) {
+  return m2scan_bwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, tw, nullptr, d_h_enriched, B, K,
+                       SH2, D, d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace,
+                       workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -489,6 +489,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     const int qd = warp & 3, sub = warp >> 2;
     const int row = 32 * qd + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    const float gsc = load_gate_scale(a.gate_scale);
     // C / d_ctx partial dots: thread = (role, state, column quad), all 16
     // samples of a tile; role 0 sums h_s2 . W_C, role 1 dY . W_O^T
     const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_role = tid >> 7;
@@ -645,7 +646,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
             bv[u] = pg[ob[u]];
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) av[u] = sigmoid_fast(av[u]);
+          for (int u = 0; u < 8; ++u) av[u] = gsc * sigmoid_fast(av[u]);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             x = fmaf(av[u], x, bv[u]);
@@ -669,6 +670,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
           for (int u = 7; u >= 0; --u) {
             float sg, dsg;
             sigmoid_and_slope(av[u], sg, dsg);
+            sg *= gsc;
+            dsg *= gsc;
             const float dB = dx, dA = dx * xp[u] * dsg;
             dx *= sg;
             const float ah = tf32_rn(dA), bh = tf32_rn(dB);
@@ -692,7 +695,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
               }
   #pragma unroll
             for (int u = 0; u < 8; ++u)
-              if (u < n) av[u] = sigmoid_fast(av[u]);
+              if (u < n) av[u] = gsc * sigmoid_fast(av[u]);
   #pragma unroll
             for (int u = 0; u < 8; ++u)
               if (u < n) {
@@ -720,6 +723,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
                 const int r = rb + k0 + u;
                 float sg, dsg;
                 sigmoid_and_slope(av[u], sg, dsg);
+                sg *= gsc;
+                dsg *= gsc;
                 const float dB = dx, dA = dx * xp[u] * dsg;
                 dx *= sg;
                 const float ah = tf32_rn(dA), bh = tf32_rn(dB);

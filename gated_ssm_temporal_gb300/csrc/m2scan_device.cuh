@@ -179,6 +179,9 @@ __device__ __forceinline__ void sts4(float* p, float4 v) {
 
 __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
 
+// The optional gate multiplier: every gate is gate_scale * sigmoid(A).
+__device__ __forceinline__ float load_gate_scale(const float* p) { return p ? __ldg(p) : 1.0f; }
+
 // sigmoid(a) from e = exp(-|a|) and r = 1 / (1 + e): sigmoid(|a|) = r and
 // sigmoid(-|a|) = e r, so neither side cancels. Uses the fast exponential and
 // division intrinsics (a few ulp; the layer's results are checked to 1e-4).

@@ -461,17 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     if (tid < S_t * D) {
       const int s = tid / D, d = tid - (tid / D) * D;
       float* pcol = sP + s * K * PS;
+      const float gsc = load_gate_scale(a.gate_scale);
       float x = 0.f;
       if constexpr (!BWD) {
         for (int t = 0; t < K; ++t) {
           const float* pr = pcol + t * PS;
-          x = fmaf(sigmoidf_(pr[d]), x, pr[D + d]);
+          x = fmaf(gsc * sigmoidf_(pr[d]), x, pr[D + d]);
         }
         sCtx[s * D + d] = sC[s * D + d] * x;
       } else {
         for (int t = 0; t < K; ++t) {  // replay: A stays in place, B_t is replaced by x_t
           float* pr = pcol + t * PS;
-          x = fmaf(sigmoidf_(pr[d]), x, pr[D + d]);
+          x = fmaf(gsc * sigmoidf_(pr[d]), x, pr[D + d]);
           pr[D + d] = x;
         }
         const float Cv = sC[s * D + d], dctx = sDctx[s * D + d];
@@ -481,10 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
         for (int t = K - 1; t >= 0; --t) {
           float* pr = pcol + t * PS;
           const float at = pr[d];
-          const float sg = sigmoidf_(at);
+          const float sg0 = sigmoidf_(at);
           // sigmoid'(a) = sigmoid(a) * sigmoid(-a): 1 - sigmoid(a) taken as sigmoid(-a)
           // keeps full relative precision when the gate is saturated near 1.
-          const float dsg = sg * sigmoidf_(-at);
+          const float dsg = gsc * (sg0 * sigmoidf_(-at));
+          const float sg = gsc * sg0;
           const float xprev = t > 0 ? pr[D + d - PS] : 0.f;
           pr[D + d] = dx;                   // dB_t
           pr[d] = dx * xprev * dsg;         // dA_t

@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc_kernel(const __grid_con
       if (tid < S_t * D) {
         const int s = tid / D, d = tid - (tid / D) * D;
         const float* pcol = sP + s * K * PS;
+        const float gsc = load_gate_scale(a.gate_scale);
         float x = 0.f;
         int k = 0;
         for (; k + 8 <= K; k += 8) {  // 8 independent gates, then the 8-step chain
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc_kernel(const __grid_con
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const float* pr = pcol + (k + u) * PS;
-            g8[u] = sigmoidf_(pr[d]);
+            g8[u] = gsc * sigmoidf_(pr[d]);
             b8[u] = pr[D + d];
           }
 #pragma unroll
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc_kernel(const __grid_con
         }
         for (; k < K; ++k) {
           const float* pr = pcol + k * PS;
-          x = fmaf(sigmoidf_(pr[d]), x, pr[D + d]);
+          x = fmaf(gsc * sigmoidf_(pr[d]), x, pr[D + d]);
         }
         sCtx[d * S_max + s] = sC[s * D + d] * x;  // transposed: [D][S_max]
       }

@@ -299,6 +299,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     const int qd = warp & 3, sub = warp >> 2;
     const int row = 32 * qd + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    const float gsc = load_gate_scale(a.gate_scale);
     // C partial dots: thread = (state quad sd_dq, sample pair sd_sp, column
     // quad sd_jq): samples 2 sd_sp, 2 sd_sp + 1 x states 4 sd_dq .. + 3 over 4
     // columns of each chunk
@@ -517,7 +518,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
             bv[u] = pg[ob[u]];
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) av[u] = sigmoid_fast(av[u]);
+          for (int u = 0; u < 8; ++u) av[u] = gsc * sigmoid_fast(av[u]);
 #pragma unroll
           for (int u = 0; u < 8; ++u) x = fmaf(av[u], x, bv[u]);
         }
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
             }
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            if (u < n) av[u] = sigmoid_fast(av[u]);
+            if (u < n) av[u] = gsc * sigmoid_fast(av[u]);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             if (u < n) x = fmaf(av[u], x, bv[u]);

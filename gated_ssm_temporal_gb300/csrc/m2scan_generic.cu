@@ -61,11 +61,12 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
     }
     __syncthreads();
     // scan (and reverse scan)
+    const float gsc = load_gate_scale(a.gate_scale);
     for (int d = tid; d < D; d += kThreads) {
       float x = 0.f;
       for (int t = 0; t < K; ++t) {
         float* pr = sAB + t * TD;
-        x = fmaf(sigmoidf_(pr[d]), x, pr[D + d]);
+        x = fmaf(gsc * sigmoidf_(pr[d]), x, pr[D + d]);
         if (BWD) pr[D + d] = x;  // A stays in place, B_t is replaced by x_t
       }
       sCtx[d] = sC[d] * x;
@@ -75,8 +76,9 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
         for (int t = K - 1; t >= 0; --t) {
           float* pr = sAB + t * TD;
           const float at = pr[d];
-          const float sg = sigmoidf_(at);
-          const float dsg = sg * sigmoidf_(-at);  // sigmoid' without cancellation near 1
+          const float sg0 = sigmoidf_(at);
+          const float dsg = gsc * (sg0 * sigmoidf_(-at));  // sigmoid' without cancellation near 1
+          const float sg = gsc * sg0;
           const float xprev = t > 0 ? pr[D + d - TD] : 0.f;
           pr[D + d] = dx;
           pr[d] = dx * xprev * dsg;

@@ -36,6 +36,7 @@ struct alignas(128) FastArgs {
   float* out0;  // forward: h_enriched; backward: d_h_history
   float* out1;  // backward: d_h_s2
   float* ws;    // backward: weight-gradient slots [P][4][SH2*D]
+  const float* gate_scale;  // one float multiplying every gate, or null (1)
   unsigned* err;
   unsigned long long* trace;  // debug timeline buffer (builds with M2SCAN_TRACE), else null
   long long B;
@@ -77,6 +78,7 @@ struct GenericArgs {
   int SH2;
   int D;
   float tw;
+  const float* gate_scale;  // one float multiplying every gate, or null (1)
 };
 
 // Fast path shape limits (see m2scan.h).
@@ -93,12 +95,14 @@ bool wide_path_ok(int K, int SH2, int D);
 size_t wide_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2);
 cudaError_t launch_wide_fwd(const float* h_history, const float* h_s2, const float* W_A,
                             const float* W_B, const float* W_C, const float* W_O, float tw, int64_t B,
-                            int K, int SH2, float* h_enriched, cudaStream_t stream);
+                            int K, int SH2, float* h_enriched, const float* gate_scale,
+                            cudaStream_t stream);
 cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const float* W_A,
                             const float* W_B, const float* W_C, const float* W_O, float tw,
                             const float* g, int64_t B, int K, int SH2, float* d_h_history,
                             float* d_h_s2, float* dW_A, float* dW_B, float* dW_C, float* dW_O,
-                            void* workspace, cudaStream_t stream, int* n_launches);
+                            void* workspace, const float* gate_scale, cudaStream_t stream,
+                            int* n_launches);
 cudaError_t prepare_wide_kernels();
 // Warp-specialised tensor-core forward (D in {8, 16}).
 bool fwd_tc_plan(int K, int SH2, int D, FastArgs* a);

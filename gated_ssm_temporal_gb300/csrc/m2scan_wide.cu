@@ -51,6 +51,7 @@ struct WideArgs {
   float* dab;   // backward: dA|dB [B*K][128]
   float* cc;    // backward: [dC | ctx] [B][128]
   float* slots; // backward: weight-gradient slots [P][4][SH2*D]
+  const float* gate_scale;  // one float multiplying every gate, or null (1)
   long long B;
   int K;
   int SH2;
@@ -290,12 +291,13 @@ __global__ void __launch_bounds__(kWT, 1) wide_fwd_kernel(const WideArgs a) {
     tile_projections<false>(a, m, b0, S_t, acc);
     tile_readout<false>(a, m, acc);
     // scan: one (sample, state) pair per thread and step
+    const float gsc = load_gate_scale(a.gate_scale);
     for (int p = tid; p < S_t * kWD; p += kWT) {
       const int s = p >> 6, d = p & 63;
       float x = 0.f;
       for (int u = 0; u < K; ++u) {
         const float* pr = m.AB + (s * K + u) * kLd;
-        x = fmaf(sigmoid_fast(pr[d]), x, pr[kWD + d]);
+        x = fmaf(gsc * sigmoid_fast(pr[d]), x, pr[kWD + d]);
       }
       m.CtxT[d * kWSmax + s] = m.C[s * kWD + d] * x;
     }
@@ -358,12 +360,13 @@ __global__ void __launch_bounds__(kWT, 1) wide_bwd_kernel(const WideArgs a) {
       const int c = e >> 7, r = e & 127;
       if (r >= R_t) m.DABt[c * kLd + r] = 0.f;
     }
+    const float gsc = load_gate_scale(a.gate_scale);
     for (int p = tid; p < S_t * kWD; p += kWT) {
       const int s = p >> 6, d = p & 63;
       float x = 0.f;
       for (int u = 0; u < K; ++u) {  // B_t is replaced by x_t
         float* pr = m.AB + (s * K + u) * kLd;
-        x = fmaf(sigmoid_fast(pr[d]), x, pr[kWD + d]);
+        x = fmaf(gsc * sigmoid_fast(pr[d]), x, pr[kWD + d]);
         pr[kWD + d] = x;
       }
       const float Cv = m.C[s * kWD + d], dctx = m.Dctx[s * kWD + d];
@@ -377,6 +380,8 @@ __global__ void __launch_bounds__(kWT, 1) wide_bwd_kernel(const WideArgs a) {
         const float* pr = m.AB + r * kLd;
         float sg, dsg;
         sigmoid_and_slope(pr[d], sg, dsg);
+        sg *= gsc;
+        dsg *= gsc;
         const float xprev = u > 0 ? pr[kWD + d - kLd] : 0.f;
         const float dA = dx * xprev * dsg, dB = dx;
         dx *= sg;
@@ -564,9 +569,11 @@ static int wide_grid(const WideArgs& w) {
 
 cudaError_t launch_wide_fwd(const float* h_history, const float* h_s2, const float* W_A,
                             const float* W_B, const float* W_C, const float* W_O, float tw, int64_t B,
-                            int K, int SH2, float* h_enriched, cudaStream_t stream) {
+                            int K, int SH2, float* h_enriched, const float* gate_scale,
+                            cudaStream_t stream) {
   WideArgs w = wide_args(h_history, h_s2, nullptr, W_A, W_B, W_C, W_O, tw, B, K, SH2);
   w.out0 = h_enriched;
+  w.gate_scale = gate_scale;
   wide_fwd_kernel<<<wide_grid(w), kWT, tile_smem_floats(false) * sizeof(float), stream>>>(w);
   return cudaGetLastError();
 }
@@ -576,8 +583,9 @@ cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const flo
                             const float* W_B, const float* W_C, const float* W_O, float tw,
                             const float* g, int64_t B, int K, int SH2, float* d_h_history,
                             float* d_h_s2, float* dW_A, float* dW_B, float* dW_C, float* dW_O,
-                            void* workspace, cudaStream_t stream, int* n) {
+                            void* workspace, const float* gate_scale, cudaStream_t stream, int* n) {
   WideArgs w = wide_args(h_history, h_s2, g, W_A, W_B, W_C, W_O, tw, B, K, SH2);
+  w.gate_scale = gate_scale;
   w.out0 = d_h_history;
   w.out1 = d_h_s2;
   w.P = wide_ranges(B);

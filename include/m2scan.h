@@ -113,6 +113,30 @@ m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float*
                          size_t workspace_bytes, m2scan_stream_t stream);
 
 /*
+ * The layer with the pages' optional gate multiplier ("Custom Kernel
+ * Optimization Implementation Plan", Task 1: gate *= isv_signals[11] when
+ * that signal is present; Task 2 carries the same factor into the reverse
+ * scan): every gate becomes g * sigmoid(A_t), so
+ *     x_t = g * sigmoid(A_t) * x_{t-1} + B_t,
+ *     dA_t = dx * x_{t-1} * g * sigmoid'(A_t),  dx <- dx * g * sigmoid(A_t).
+ * `gate_scale` is a DEVICE pointer to the one float g (4-byte aligned; read by
+ * the kernels, so it may change between calls without a host
+ * synchronisation), or NULL for g = 1, which is exactly m2scan_fwd /
+ * m2scan_bwd. g gets no gradient. It must not overlap any output. Every other
+ * argument, check and result is as for m2scan_fwd / m2scan_bwd.
+ */
+m2scan_status m2scan_fwd_ex(const float* h_history, const float* h_s2, const float* W_A,
+                            const float* W_B, const float* W_C, const float* W_O, float tw,
+                            const float* gate_scale, int64_t B, int32_t K, int32_t SH2,
+                            int32_t D, float* h_enriched, m2scan_stream_t stream);
+m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const float* W_A,
+                            const float* W_B, const float* W_C, const float* W_O, float tw,
+                            const float* gate_scale, const float* d_h_enriched, int64_t B,
+                            int32_t K, int32_t SH2, int32_t D, float* d_h_history,
+                            float* d_h_s2, float* dW_A, float* dW_B, float* dW_C, float* dW_O,
+                            void* workspace, size_t workspace_bytes, m2scan_stream_t stream);
+
+/*
  * Backward pass for callers that cannot allocate device memory themselves:
  * code running where the device allocator belongs to someone else (a host
  * framework whose memory pool must account for every byte), latency-critical
@@ -196,8 +220,9 @@ int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
  */
 m2scan_status m2scan_read_device_flags(uint32_t* flags);
 
-/* Number of CUDA kernels launched by the most recent successful m2scan_fwd,
- * m2scan_bwd or m2scan_bias_grad call on the calling thread. */
+/* Number of CUDA kernels launched by the most recent successful call of
+ * m2scan_fwd, m2scan_bwd (or their _ex forms) or m2scan_bias_grad on the
+ * calling thread. */
 int m2scan_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -47,8 +47,15 @@ res["fwd_misaligned_h"] = fwd(h_history=W[0] + 4)
 res["fwd_misaligned_out"] = fwd(h_enriched=W[6] + 8)
 res["fwd_alias_out_h"] = fwd(h_enriched=W[0] + 64)
 res["fwd_alias_out_WO"] = fwd(h_enriched=W[5])
+res["fwdex_misaligned_gs"] = g.m2scan_fwd_ex(W[0], W[1], W[2], W[3], W[4], W[5], 0.5, W[18] + 2,
+                                          B, K, SH2, D, W[6], 0)
+res["fwdex_alias_gs_out"] = g.m2scan_fwd_ex(W[0], W[1], W[2], W[3], W[4], W[5], 0.5, W[6] + 8,
+                                         B, K, SH2, D, W[6], 0)
 res["fwd_B0_ok"] = fwd(B=0, h_history=0, h_s2=0, h_enriched=0)
 res["fwd_launches_B0"] = g.m2scan_last_launch_count()
+res["bwdex_alias_gs_dWA"] = g.m2scan_bwd_ex(
+    W[0], W[1], W[2], W[3], W[4], W[5], 0.5, W[10] + 4, W[7], B, K, SH2, D, W[8], W[9], W[10],
+    W[11], W[12], W[13], W[14], g.m2scan_bwd_workspace_bytes(B, K, SH2, D), 0)
 res["bwd_null_ws"] = bwd(workspace=0)
 res["bwd_short_ws"] = bwd(workspace_bytes=g.m2scan_bwd_workspace_bytes(B, K, SH2, D) - 16)
 res["bwd_null_dWO"] = bwd(dW_O=0)

@@ -50,6 +50,7 @@ NULL, SHAPE, ALIGN, ALIAS, WORKSPACE = 1, 2, 3, 4, 5
     ("fwd_K0", SHAPE), ("fwd_SH2_not4", SHAPE), ("fwd_SH2_small", SHAPE), ("fwd_D0", SHAPE),
     ("fwd_misaligned_h", ALIGN), ("fwd_misaligned_out", ALIGN), ("fwd_alias_out_h", ALIAS),
     ("fwd_alias_out_WO", ALIAS), ("fwd_B0_ok", 0), ("fwd_launches_B0", 0),
+    ("fwdex_misaligned_gs", ALIGN), ("fwdex_alias_gs_out", ALIAS), ("bwdex_alias_gs_dWA", ALIAS),
     ("bwd_null_ws", WORKSPACE), ("bwd_short_ws", WORKSPACE), ("bwd_null_dWO", NULL),
     ("bwd_null_g", NULL), ("bwd_shape", SHAPE), ("bwd_misaligned_ws", ALIGN),
     ("bwd_alias_out_out", ALIAS), ("bwd_alias_ws_in", ALIAS), ("bwd_alias_dh_g", ALIAS),
