@@ -52,8 +52,8 @@ def open_library(path: str):
     dp = ctypes.POINTER(ctypes.c_double)
     i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
     lib.m2o_scan_state.argtypes = [dp] * 5 + [i64, i32, i32, i32, dbl] + [dp] * 5
-    lib.m2o_forward.argtypes = [dp] * 6 + [dbl, i64, i32, i32, i32, dbl, dp, i32]
-    lib.m2o_backward.argtypes = ([dp] * 6 + [dbl, dp, i64, i32, i32, i32, dbl]
+    lib.m2o_forward.argtypes = [dp] * 6 + [dbl, i64, i32, i32, i32, dbl, i32, dp, i32]
+    lib.m2o_backward.argtypes = ([dp] * 6 + [dbl, dp, i64, i32, i32, i32, dbl, i32]
                                  + [dp] * 6 + [i32])
     lib.m2o_bias_grad.argtypes = [dp, i64, i32, dp, i32, dp]
     for f in (lib.m2o_scan_state, lib.m2o_forward, lib.m2o_backward, lib.m2o_bias_grad):
@@ -105,13 +105,18 @@ def scan_state(h_history, h_s2, W_A, W_B, W_C, lib=None, gate_scale=1.0):
     return A, Bv, x, C, ctx
 
 
-def forward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, n_threads=None, lib=None, gate_scale=1.0):
-    """h_enriched [B,SH2] in float64; ``gate_scale`` multiplies every gate."""
-    h, hs, wa, wb, wc, wo = map(_f64, (h_history, h_s2, W_A, W_B, W_C, W_O))
+def forward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, n_threads=None, lib=None, gate_scale=1.0,
+            blend=False):
+    """h_enriched [B,SH2] in float64; ``gate_scale`` multiplies every gate.
+    ``blend``: the pages' output step, W_O is then the per-feature weight
+    vector w [SH2] (None: ones) and tw is ignored."""
+    h, hs, wa, wb, wc = map(_f64, (h_history, h_s2, W_A, W_B, W_C))
     B, K, SH2, D = _dims(h, wa)
+    wo = _f64(np.ones(SH2) if W_O is None else W_O)
     out = np.empty((B, SH2))
     rc = _load(lib).m2o_forward(_ptr(h), _ptr(hs), _ptr(wa), _ptr(wb), _ptr(wc), _ptr(wo),
-                             float(tw), B, K, SH2, D, float(gate_scale), _ptr(out),
+                             float(tw), B, K, SH2, D, float(gate_scale), 1 if blend else 0,
+                             _ptr(out),
                              n_threads or default_threads())
     if rc:
         raise RuntimeError("oracle forward failed (%d)" % rc)
@@ -119,20 +124,22 @@ def forward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, n_threads=None, lib=None, g
 
 
 def backward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, n_threads=None,
-             lib=None, gate_scale=1.0):
+             lib=None, gate_scale=1.0, blend=False):
     """Returns dict of float64 arrays: d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O.
-    ``gate_scale`` multiplies every gate (a constant: it gets no gradient)."""
-    h, hs, wa, wb, wc, wo, g = map(_f64, (h_history, h_s2, W_A, W_B, W_C, W_O,
-                                         d_h_enriched))
+    ``gate_scale`` multiplies every gate (a constant: it gets no gradient).
+    ``blend``: the pages' output step (see ``forward``); dW_O is then the
+    gradient of the per-feature weights, [SH2]."""
+    h, hs, wa, wb, wc, g = map(_f64, (h_history, h_s2, W_A, W_B, W_C, d_h_enriched))
     B, K, SH2, D = _dims(h, wa)
+    wo = _f64(np.ones(SH2) if W_O is None else W_O)
     out = {
         "d_h_history": np.empty((B, K, SH2)), "d_h_s2": np.empty((B, SH2)),
         "dW_A": np.empty((SH2, D)), "dW_B": np.empty((SH2, D)),
-        "dW_C": np.empty((SH2, D)), "dW_O": np.empty((D, SH2)),
+        "dW_C": np.empty((SH2, D)), "dW_O": np.empty((SH2,) if blend else (D, SH2)),
     }
     rc = _load(lib).m2o_backward(
         _ptr(h), _ptr(hs), _ptr(wa), _ptr(wb), _ptr(wc), _ptr(wo), float(tw), _ptr(g),
-        B, K, SH2, D, float(gate_scale), _ptr(out["d_h_history"]), _ptr(out["d_h_s2"]), _ptr(out["dW_A"]),
+        B, K, SH2, D, float(gate_scale), 1 if blend else 0, _ptr(out["d_h_history"]), _ptr(out["d_h_s2"]), _ptr(out["dW_A"]),
         _ptr(out["dW_B"]), _ptr(out["dW_C"]), _ptr(out["dW_O"]),
         n_threads or default_threads())
     if rc:

@@ -116,9 +116,16 @@ int m2o_scan_state(const double* h_history, const double* h_s2, const double* W_
   return 0;
 }
 
+/* Output step, two forms. blend == 0 (the layer's):
+ *   h_enriched[j] = h_s2[j] + tw * sum_s ctx[s] * W_O[s, j].
+ * blend == 1 (the pages' own, "Custom Kernel Optimization Implementation
+ * Plan", Task 1 Step 3): one scalar context per sample, sum_s ctx[s], blended
+ * into every feature with a per-feature weight and a 1/D scale,
+ *   h_enriched[j] = h_s2[j] + w[j] * (sum_s ctx[s]) / D,
+ * W_O then holds w [SH2] (NULL: every weight 1) and tw is not used. */
 int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
                 const double* W_B, const double* W_C, const double* W_O, double tw,
-                int64_t B, int K, int SH2, int D, double gs, double* h_enriched,
+                int64_t B, int K, int SH2, int D, double gs, int blend, double* h_enriched,
                 int n_threads) {
   if (B < 0 || K < 1 || SH2 < 1 || D < 1) return 1;
   if (n_threads < 1) n_threads = 1;
@@ -138,6 +145,15 @@ int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
       const double* hs = h_s2 + b * SH2;
       sample_forward(h_history + b * K * SH2, hs, W_A, W_B, W_C, K, SH2, D, gs, A, Bv,
                      sig, x, C, ctx);
+      if (blend) {
+        double context = 0.0;
+        for (int s = 0; s < D; s++) context += ctx[s];
+        for (int j = 0; j < SH2; j++) {
+          const double w = W_O ? W_O[j] : 1.0;
+          h_enriched[b * SH2 + j] = hs[j] + w * context / D;
+        }
+        continue;
+      }
       for (int j = 0; j < SH2; j++) {
         double o = 0.0;
         for (int s = 0; s < D; s++) o += ctx[s] * W_O[(int64_t)s * SH2 + j];
@@ -152,7 +168,7 @@ int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
 int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
                  const double* W_B, const double* W_C, const double* W_O, double tw,
                  const double* d_h_enriched, int64_t B, int K, int SH2, int D, double gs,
-                 double* d_h_history, double* d_h_s2, double* dW_A, double* dW_B,
+                 int blend, double* d_h_history, double* d_h_s2, double* dW_A, double* dW_B,
                  double* dW_C, double* dW_O, int n_threads) {
   if (B < 0 || K < 1 || SH2 < 1 || D < 1) return 1;
   if (n_threads < 1) n_threads = 1;
@@ -184,8 +200,22 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
         const double* hs = h_s2 + b * SH2;
         const double* g = d_h_enriched + b * SH2;
         sample_forward(h, hs, W_A, W_B, W_C, K, SH2, D, gs, A, Bv, sig, x, C, ctx);
-        /* output step */
-        for (int s = 0; s < D; s++) {
+        /* output step (blend: the scalar context's gradient is shared by every
+         * state, and dW_O holds the per-feature weights' gradient, dw [SH2]) */
+        if (blend) {
+          double context = 0.0, dcontext = 0.0;
+          for (int s = 0; s < D; s++) context += ctx[s];
+          for (int j = 0; j < SH2; j++) {
+            const double w = W_O ? W_O[j] : 1.0;
+            dcontext += g[j] * w / D;
+            pO[j] += g[j] * context / D;
+          }
+          for (int s = 0; s < D; s++) {
+            dctx[s] = dcontext;
+            dC[s] = dcontext * x[(K - 1) * D + s];
+          }
+        }
+        for (int s = 0; s < D && !blend; s++) {
           double acc = 0.0;
           for (int j = 0; j < SH2; j++) acc += g[j] * W_O[(int64_t)s * SH2 + j];
           dctx[s] = tw * acc;
@@ -249,7 +279,7 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
     dW_A[e] = sa;
     dW_B[e] = sb;
     dW_C[e] = sc;
-    dW_O[e] = so;
+    if (!blend || e < SH2) dW_O[e] = so;
   }
   free(part);
   return fail;

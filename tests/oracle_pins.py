@@ -14,7 +14,11 @@ raises AssertionError when the oracle disagrees with:
   * independence from the number of threads,
   * for the optional gate multiplier g (every gate g * sig(A_t), the pages'
     isv_signals[11]): the closed form with g, central differences and torch
-    autograd with g, and g = 1 giving the plain layer bit for bit.
+    autograd with g, and g = 1 giving the plain layer bit for bit,
+  * for the pages' own output step (one scalar context per sample blended
+    into every feature with a weight w[j] and 1/D): central differences and
+    torch autograd of all gradients including dw, the K=1 closed form, and
+    w = 0 giving the identity on h_s2.
 ``tests/test_oracle_mutants.py`` plants mistakes in copies of the oracle and
 checks that these pins catch each one.
 """
@@ -300,7 +304,65 @@ def pin_gate_scale_gradients(lib=None):
               "autograd d%s with a gate multiplier" % p)
 
 
+def pin_blend(lib=None):
+    """The pages' output step h + w[j] * (sum_s ctx_s) / D: closed form, w = 0,
+    central differences and torch autograd of every gradient (dw included)."""
+    import torch
+    x = rand_inputs(3, 1, 6, 4, 16)
+    w = np.random.default_rng(17).standard_normal(6)
+    Bv = x["h_history"][:, 0, :] @ x["W_B"]
+    C = x["h_s2"] @ x["W_C"]
+    want = x["h_s2"] + np.outer((C * Bv).sum(axis=1) / 4.0, w)
+    close(fwd(dict(x, W_O=w), lib, blend=True), want, 1e-12, 1e-13, "blend K=1 closed form")
+    x0 = dict(x, W_O=np.zeros(6))
+    assert np.array_equal(fwd(x0, lib, blend=True), x["h_s2"]), "blend w=0 != h_s2"
+    g0 = bwd(x0, lib, blend=True)
+    assert np.array_equal(g0["d_h_s2"], x["d_h_enriched"])
+    assert np.all(g0["dW_A"] == 0.0) and np.all(g0["d_h_history"] == 0.0)
+    ones = fwd(dict(x, W_O=None), lib, blend=True)
+    assert np.array_equal(ones, fwd(dict(x, W_O=np.ones(6)), lib, blend=True))
+    # every gradient by central differences (dw is the gradient of W_O = w)
+    x = rand_inputs(2, 3, 5, 3, 18, wscale=2.0)
+    x["W_O"] = np.random.default_rng(19).standard_normal(5)
+    gr = bwd(x, lib, blend=True)
+    dy = x["d_h_enriched"]
+
+    def loss(xx):
+        return float(np.sum(dy * fwd(xx, lib, blend=True)))
+
+    eps = 1e-6
+    for p in PARAMS:
+        num = np.zeros_like(x[p])
+        flat = num.reshape(-1)
+        for i in range(flat.size):
+            xp = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in x.items()}
+            xm = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in x.items()}
+            xp[p].reshape(-1)[i] += eps
+            xm[p].reshape(-1)[i] -= eps
+            flat[i] = (loss(xp) - loss(xm)) / (2 * eps)
+        close(gr[GRADS[p]], num, 1e-6, 1e-8, "blend finite differences d%s" % p)
+    # torch float64 autograd, with a gate multiplier as well
+    gs = 0.9
+    x = rand_inputs(3, 5, 7, 4, 20, wscale=3.0)
+    x["W_O"] = np.random.default_rng(21).standard_normal(7)
+    t = {k: torch.tensor(x[k], dtype=torch.float64, requires_grad=True) for k in PARAMS}
+    A = t["h_history"] @ t["W_A"]
+    Bv = t["h_history"] @ t["W_B"]
+    C = t["h_s2"] @ t["W_C"]
+    state = torch.zeros(3, 4, dtype=torch.float64)
+    for k in range(5):
+        state = gs * torch.sigmoid(A[:, k]) * state + Bv[:, k]
+    context = (C * state).sum(dim=1, keepdim=True)
+    y = t["h_s2"] + t["W_O"][None, :] * context / 4.0
+    (y * torch.tensor(x["d_h_enriched"])).sum().backward()
+    close(fwd(x, lib, blend=True, gate_scale=gs), y.detach().numpy(), 1e-12, 1e-13,
+          "blend autograd output")
+    gr = bwd(x, lib, blend=True, gate_scale=gs)
+    for p in PARAMS:
+        close(gr[GRADS[p]], t[p].grad.numpy(), 1e-10, 1e-12, "blend autograd d%s" % p)
+
+
 ALL_PINS = [pin_finite_differences, pin_closed_form_scan, pin_reverse_closed_form, pin_k1,
             pin_k2, pin_saturated_gates, pin_tw_zero, pin_linearity, pin_torch_autograd,
             pin_golden_hand_example, pin_thread_count_invariance, pin_gate_scale_closed_form,
-            pin_gate_scale_gradients]
+            pin_gate_scale_gradients, pin_blend]

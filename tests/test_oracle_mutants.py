@@ -36,6 +36,11 @@ MUTANTS = {
     "gate_scale_dropped_in_dA": ("dA[t * D + s] = dx * xprev * gs * gt * (1.0 - gt);",
                                  "dA[t * D + s] = dx * xprev * gt * (1.0 - gt);"),
     "gate_scale_dropped_in_dx": ("dx = dx * gs * gt;", "dx = dx * gt;"),
+    "blend_without_1_over_D": ("h_enriched[b * SH2 + j] = hs[j] + w * context / D;",
+                               "h_enriched[b * SH2 + j] = hs[j] + w * context;"),
+    "blend_dcontext_without_w": ("dcontext += g[j] * w / D;", "dcontext += g[j] / D;"),
+    "blend_dw_without_context": ("pO[j] += g[j] * context / D;", "pO[j] += g[j] / D;"),
+    "blend_dC_uses_C": ("dC[s] = dcontext * x[(K - 1) * D + s];", "dC[s] = dcontext * C[s];"),
     "gate_scale_squared_in_dA": ("dA[t * D + s] = dx * xprev * gs * gt * (1.0 - gt);",
                                  "dA[t * D + s] = dx * xprev * gs * gs * gt * (1.0 - gt);"),
     "xprev_off_by_one": ("double xprev = (t > 0) ? x[(t - 1) * D + s] : 0.0;",
