@@ -86,6 +86,15 @@ def load_library(path: str | None = None):
         lib.m2scan_bias_grad_workspace_bytes.restype = sz
         lib.m2scan_bias_grad.argtypes = [vp, i64, i32, vp, i32, vp, sz, vp]
         lib.m2scan_bias_grad.restype = ctypes.c_int
+        lib.m2scan_blend_fwd_workspace_bytes.argtypes = [i32, i32]
+        lib.m2scan_blend_fwd_workspace_bytes.restype = sz
+        lib.m2scan_blend_bwd_workspace_bytes.argtypes = [i64, i32, i32, i32]
+        lib.m2scan_blend_bwd_workspace_bytes.restype = sz
+        lib.m2scan_fwd_blend.argtypes = [vp] * 7 + [i64, i32, i32, i32, vp, vp, sz, vp]
+        lib.m2scan_fwd_blend.restype = ctypes.c_int
+        lib.m2scan_bwd_blend.argtypes = ([vp] * 8 + [i64, i32, i32, i32] + [vp] * 6
+                                         + [vp, sz, vp])
+        lib.m2scan_bwd_blend.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -276,3 +285,77 @@ def bias_grad(dy, db=None, accumulate=False, workspace=None, stream=None):
     if st != M2SCAN_OK:
         raise M2ScanError(st, "m2scan_bias_grad")
     return db
+
+
+def m2scan_blend_fwd_workspace_bytes(SH2, D):
+    return load_library().m2scan_blend_fwd_workspace_bytes(SH2, D)
+
+
+def m2scan_blend_bwd_workspace_bytes(B, K, SH2, D):
+    return load_library().m2scan_blend_bwd_workspace_bytes(B, K, SH2, D)
+
+
+def m2scan_fwd_blend(h_history, h_s2, W_A, W_B, W_C, temporal_weight, gate_scale, B, K, SH2, D,
+                     h_enriched, workspace, workspace_bytes, stream=0):
+    return load_library().m2scan_fwd_blend(h_history, h_s2, W_A, W_B, W_C, temporal_weight,
+                                           gate_scale, B, K, SH2, D, h_enriched, workspace,
+                                           workspace_bytes, stream)
+
+
+def m2scan_bwd_blend(h_history, h_s2, W_A, W_B, W_C, temporal_weight, gate_scale, d_h_enriched,
+                     B, K, SH2, D, d_h_history, d_h_s2, dW_A, dW_B, dW_C, d_temporal_weight,
+                     workspace, workspace_bytes, stream=0):
+    return load_library().m2scan_bwd_blend(h_history, h_s2, W_A, W_B, W_C, temporal_weight,
+                                           gate_scale, d_h_enriched, B, K, SH2, D, d_h_history,
+                                           d_h_s2, dW_A, dW_B, dW_C, d_temporal_weight,
+                                           workspace, workspace_bytes, stream)
+
+
+def fwd_blend(h_history, h_s2, W_A, W_B, W_C, temporal_weight=None, gate_scale=None, out=None,
+              stream=None):
+    """The layer with the pages' per-feature blend output step:
+    h_enriched = h_s2 + w[j] * (sum_s ctx_s) / D, w = ``temporal_weight`` [SH2] (None: ones)."""
+    import torch
+    B, K, SH2, D = dims_of(h_history, W_A)
+    if out is None:
+        out = torch.empty((B, SH2), device=h_history.device, dtype=torch.float32)
+    need = m2scan_blend_fwd_workspace_bytes(SH2, D)
+    ws = torch.empty((max(1, need // 4),), device=h_history.device, dtype=torch.float32)
+    tw = 0 if temporal_weight is None else _check(temporal_weight, "temporal_weight", (SH2,))
+    st = m2scan_fwd_blend(_check(h_history, "h_history", (B, K, SH2)), _check(h_s2, "h_s2", (B, SH2)),
+                          _check(W_A, "W_A", (SH2, D)), _check(W_B, "W_B", (SH2, D)),
+                          _check(W_C, "W_C", (SH2, D)), tw, _gate_ptr(gate_scale), B, K, SH2, D,
+                          _check(out, "h_enriched", (B, SH2)), ws.data_ptr(), ws.numel() * 4,
+                          _stream(stream))
+    if st != M2SCAN_OK:
+        raise M2ScanError(st, "m2scan_fwd_blend")
+    return out
+
+
+def bwd_blend(h_history, h_s2, W_A, W_B, W_C, d_h_enriched, temporal_weight=None, gate_scale=None,
+              stream=None):
+    """Backward of ``fwd_blend``: dict d_h_history, d_h_s2, dW_A, dW_B, dW_C and, when
+    ``temporal_weight`` is given, d_temporal_weight [SH2]."""
+    import torch
+    B, K, SH2, D = dims_of(h_history, W_A)
+    dev = h_history.device
+    outs = {"d_h_history": torch.empty((B, K, SH2), device=dev), "d_h_s2": torch.empty((B, SH2), device=dev),
+            "dW_A": torch.empty((SH2, D), device=dev), "dW_B": torch.empty((SH2, D), device=dev),
+            "dW_C": torch.empty((SH2, D), device=dev)}
+    dtw = 0
+    if temporal_weight is not None:
+        outs["d_temporal_weight"] = torch.empty((SH2,), device=dev)
+        dtw = outs["d_temporal_weight"].data_ptr()
+    need = m2scan_blend_bwd_workspace_bytes(B, K, SH2, D)
+    ws = torch.empty((max(1, need // 4),), device=dev, dtype=torch.float32)
+    tw = 0 if temporal_weight is None else _check(temporal_weight, "temporal_weight", (SH2,))
+    st = m2scan_bwd_blend(
+        _check(h_history, "h_history", (B, K, SH2)), _check(h_s2, "h_s2", (B, SH2)),
+        _check(W_A, "W_A", (SH2, D)), _check(W_B, "W_B", (SH2, D)), _check(W_C, "W_C", (SH2, D)),
+        tw, _gate_ptr(gate_scale), _check(d_h_enriched, "d_h_enriched", (B, SH2)), B, K, SH2, D,
+        outs["d_h_history"].data_ptr(), outs["d_h_s2"].data_ptr(), outs["dW_A"].data_ptr(),
+        outs["dW_B"].data_ptr(), outs["dW_C"].data_ptr(), dtw, ws.data_ptr(), ws.numel() * 4,
+        _stream(stream))
+    if st != M2SCAN_OK:
+        raise M2ScanError(st, "m2scan_bwd_blend")
+    return outs

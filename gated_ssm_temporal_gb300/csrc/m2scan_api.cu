@@ -290,6 +290,108 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
                        h_enriched, stream);
 }
 
+size_t m2scan_blend_fwd_workspace_bytes(int32_t SH2, int32_t D) {
+  if (SH2 < 4 || SH2 % 4 != 0 || D < 1) return 0;
+  return static_cast<size_t>(SH2) * D * sizeof(float);
+}
+
+size_t m2scan_blend_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D) {
+  if (check_shape(B, K, SH2, D) != M2SCAN_OK) return 0;
+  return m2scan_bwd_workspace_bytes(B, K, SH2, D) + 2 * m2scan_blend_fwd_workspace_bytes(SH2, D);
+}
+
+m2scan_status m2scan_fwd_blend(const float* h_history, const float* h_s2, const float* W_A,
+                               const float* W_B, const float* W_C, const float* temporal_weight,
+                               const float* gate_scale, int64_t B, int32_t K, int32_t SH2,
+                               int32_t D, float* h_enriched, void* workspace,
+                               size_t workspace_bytes, m2scan_stream_t stream) {
+  t_last_launches = 0;
+  m2scan_status st = check_shape(B, K, SH2, D);
+  if (st != M2SCAN_OK) return st;
+  const size_t need = m2scan_blend_fwd_workspace_bytes(SH2, D);
+  if (!workspace || workspace_bytes < need) return M2SCAN_ERR_WORKSPACE;
+  if (!aligned16(workspace) || !aligned16(temporal_weight)) return M2SCAN_ERR_ALIGN;
+  const uint64_t nb = static_cast<uint64_t>(B) * SH2 * 4, nw = static_cast<uint64_t>(SH2) * D * 4;
+  const Span ws = span(workspace, need);
+  const Span others[] = {span(h_history, nb * K), span(h_s2, nb), span(W_A, nw), span(W_B, nw),
+                         span(W_C, nw), span(h_enriched, nb),
+                         span(temporal_weight, temporal_weight ? SH2 * 4ull : 0),
+                         span(gate_scale, gate_scale ? 4 : 0)};
+  for (const Span& o : others)
+    if (overlaps(ws, o)) return M2SCAN_ERR_ALIAS;
+  if (overlaps(span(h_enriched, nb), span(temporal_weight, temporal_weight ? SH2 * 4ull : 0)))
+    return M2SCAN_ERR_ALIAS;
+  if (B == 0) return M2SCAN_OK;
+  int dev = 0;
+  if ((st = prepare_device(&dev)) != M2SCAN_OK) return st;
+  float* W_O = static_cast<float*>(workspace);
+  cudaError_t e = launch_blend_expand(temporal_weight, SH2, D, W_O, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  st = m2scan_fwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, 1.0f, gate_scale, B, K, SH2, D,
+                     h_enriched, stream);
+  if (st == M2SCAN_OK) t_last_launches += 1;
+  return st;
+}
+
+m2scan_status m2scan_bwd_blend(const float* h_history, const float* h_s2, const float* W_A,
+                               const float* W_B, const float* W_C, const float* temporal_weight,
+                               const float* gate_scale, const float* d_h_enriched, int64_t B,
+                               int32_t K, int32_t SH2, int32_t D, float* d_h_history,
+                               float* d_h_s2, float* dW_A, float* dW_B, float* dW_C,
+                               float* d_temporal_weight, void* workspace, size_t workspace_bytes,
+                               m2scan_stream_t stream) {
+  t_last_launches = 0;
+  m2scan_status st = check_shape(B, K, SH2, D);
+  if (st != M2SCAN_OK) return st;
+  const size_t need = m2scan_blend_bwd_workspace_bytes(B, K, SH2, D);
+  if (!workspace || workspace_bytes < need) return M2SCAN_ERR_WORKSPACE;
+  if (!aligned16(workspace) || !aligned16(temporal_weight) || !aligned16(d_temporal_weight))
+    return M2SCAN_ERR_ALIGN;
+  const size_t base = m2scan_bwd_workspace_bytes(B, K, SH2, D);
+  const size_t nwo = m2scan_blend_fwd_workspace_bytes(SH2, D);
+  unsigned char* w8 = static_cast<unsigned char*>(workspace);
+  float* W_O = reinterpret_cast<float*>(w8 + base);
+  float* dW_O = reinterpret_cast<float*>(w8 + base + nwo);
+  const Span ws = span(workspace, need);
+  const Span tw_in = span(temporal_weight, temporal_weight ? SH2 * 4ull : 0);
+  const Span tw_out = span(d_temporal_weight, d_temporal_weight ? SH2 * 4ull : 0);
+  if (overlaps(ws, tw_in) || overlaps(ws, tw_out) || overlaps(tw_in, tw_out))
+    return M2SCAN_ERR_ALIAS;
+  const uint64_t nb = static_cast<uint64_t>(B) * SH2 * 4, nw = static_cast<uint64_t>(SH2) * D * 4;
+  const Span layer[] = {span(h_history, nb * K), span(h_s2, nb), span(W_A, nw), span(W_B, nw),
+                        span(W_C, nw), span(d_h_enriched, nb), span(d_h_history, nb * K),
+                        span(d_h_s2, nb), span(dW_A, nw), span(dW_B, nw), span(dW_C, nw),
+                        span(gate_scale, gate_scale ? 4 : 0)};
+  for (const Span& o : layer)
+    if (overlaps(ws, o) || overlaps(tw_out, o)) return M2SCAN_ERR_ALIAS;
+  if (B > 0) {
+    int dev = 0;
+    if ((st = prepare_device(&dev)) != M2SCAN_OK) return st;
+  }
+  int n = 0;
+  if (B > 0) {
+    const cudaError_t e = launch_blend_expand(temporal_weight, SH2, D, W_O, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    ++n;
+  }
+  st = m2scan_bwd_ex(h_history, h_s2, W_A, W_B, W_C, W_O, 1.0f, gate_scale, d_h_enriched, B, K,
+                     SH2, D, d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, base, stream);
+  if (st != M2SCAN_OK) return st;
+  n += t_last_launches;
+  if (d_temporal_weight) {
+    if (B == 0) {
+      const cudaError_t e = cudaMemsetAsync(d_temporal_weight, 0, SH2 * 4ull, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    } else {
+      const cudaError_t e = launch_blend_dw(dW_O, SH2, D, d_temporal_weight, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      ++n;
+    }
+  }
+  t_last_launches = n;
+  return M2SCAN_OK;
+}
+
 size_t m2scan_bias_grad_workspace_bytes(int64_t N, int32_t C) {
   if (N < 0 || C < 1 || static_cast<uint64_t>(N) * static_cast<uint64_t>(C) > (1ull << 40)) return 0;
   if (N == 0) return 0;

@@ -122,6 +122,10 @@ cudaError_t prepare_kernels(int max_smem_optin);
 // Bias-gradient column sum (two launches): partial sums of P = colsum_partials(N)
 // row ranges into part [P][C], then their fixed-order sum into db.
 int colsum_partials(long long N);
+// The pages' per-feature blend as the layer's output step: W_O[s, j] = w[j] / D
+// (w may be null: ones), and dw[j] = sum_s dW_O[s, j] / D.
+cudaError_t launch_blend_expand(const float* w, int SH2, int D, float* W_O, cudaStream_t stream);
+cudaError_t launch_blend_dw(const float* dW_O, int SH2, int D, float* dw, cudaStream_t stream);
 cudaError_t launch_colsum(const float* dy, long long N, int C, float* db, int accumulate,
                           float* part, cudaStream_t stream, int* n_launches);
 

@@ -137,6 +137,41 @@ m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const flo
                             void* workspace, size_t workspace_bytes, m2scan_stream_t stream);
 
 /*
+ * The layer with the pages' own output step ("Custom Kernel Optimization
+ * Implementation Plan", Task 1 Step 3) in place of tw * (ctx . W_O): one
+ * scalar context per sample blended into every feature with a per-feature
+ * temporal weight w and a 1/D scale,
+ *     h_enriched[b, j] = h_s2[b, j] + w[j] * (sum_s C[b, s] x_{K-1}[b, s]) / D.
+ *   temporal_weight: w [SH2] (device, 16-byte aligned), or NULL for w = 1.
+ *   gate_scale: as for m2scan_fwd_ex (NULL: none).
+ * It runs the layer's kernels with tw = 1 and W_O[s, j] = w[j] / D, which a
+ * small kernel writes into the workspace first (one more launch):
+ *   m2scan_fwd_blend workspace >= m2scan_blend_fwd_workspace_bytes(SH2, D).
+ * The backward returns d_h_history, d_h_s2, dW_A, dW_B, dW_C as m2scan_bwd
+ * does and, when d_temporal_weight is not NULL, dw [SH2] =
+ * sum_b dY[b, j] * context_b / D (the gradient of that W_O folded back onto
+ * w, states added in order: one more launch);
+ *   m2scan_bwd_blend workspace >= m2scan_blend_bwd_workspace_bytes(B,K,SH2,D)
+ * (m2scan_bwd's workspace plus two D x SH2 scratch arrays). Other arguments,
+ * checks and conventions as for m2scan_fwd / m2scan_bwd; the workspace must
+ * not overlap anything else.
+ */
+size_t m2scan_blend_fwd_workspace_bytes(int32_t SH2, int32_t D);
+size_t m2scan_blend_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D);
+m2scan_status m2scan_fwd_blend(const float* h_history, const float* h_s2, const float* W_A,
+                               const float* W_B, const float* W_C, const float* temporal_weight,
+                               const float* gate_scale, int64_t B, int32_t K, int32_t SH2,
+                               int32_t D, float* h_enriched, void* workspace,
+                               size_t workspace_bytes, m2scan_stream_t stream);
+m2scan_status m2scan_bwd_blend(const float* h_history, const float* h_s2, const float* W_A,
+                               const float* W_B, const float* W_C, const float* temporal_weight,
+                               const float* gate_scale, const float* d_h_enriched, int64_t B,
+                               int32_t K, int32_t SH2, int32_t D, float* d_h_history,
+                               float* d_h_s2, float* dW_A, float* dW_B, float* dW_C,
+                               float* d_temporal_weight, void* workspace, size_t workspace_bytes,
+                               m2scan_stream_t stream);
+
+/*
  * Backward pass for callers that cannot allocate device memory themselves:
  * code running where the device allocator belongs to someone else (a host
  * framework whose memory pool must account for every byte), latency-critical

@@ -103,5 +103,19 @@ res["bg_ws_one"] = g.m2scan_bias_grad_workspace_bytes(1, 3)
 res["bg_ws_N0"] = g.m2scan_bias_grad_workspace_bytes(0, 5)
 res["bg_ws_big"] = g.m2scan_bias_grad_workspace_bytes(100000, 7)
 res["bg_ws_bad"] = g.m2scan_bias_grad_workspace_bytes(10, 0)
+res["bl_fwd_null_ws"] = g.m2scan_fwd_blend(W[0], W[1], W[2], W[3], W[4], W[18], 0, B, K, SH2, D,
+                                          W[6], 0, 0, 0)
+res["bl_fwd_misaligned_w"] = g.m2scan_fwd_blend(W[0], W[1], W[2], W[3], W[4], W[18] + 4, 0, B, K,
+                                               SH2, D, W[6], W[19], 1 << 20, 0)
+res["bl_fwd_alias_ws_out"] = g.m2scan_fwd_blend(W[0], W[1], W[2], W[3], W[4], W[18], 0, B, K, SH2,
+                                               D, W[6], W[6], 1 << 20, 0)
+res["bl_bwd_short_ws"] = g.m2scan_bwd_blend(
+    W[0], W[1], W[2], W[3], W[4], W[18], 0, W[7], B, K, SH2, D, W[8], W[9], W[10], W[11], W[12],
+    W[13], W[14], g.m2scan_blend_bwd_workspace_bytes(B, K, SH2, D) - 16, 0)
+res["bl_bwd_alias_dw_ws"] = g.m2scan_bwd_blend(
+    W[0], W[1], W[2], W[3], W[4], W[18], 0, W[7], B, K, SH2, D, W[8], W[9], W[10], W[11], W[12],
+    W[14] + 64, W[14], g.m2scan_blend_bwd_workspace_bytes(B, K, SH2, D), 0)
+res["bl_ws_fwd"] = g.m2scan_blend_fwd_workspace_bytes(256, 16)
+res["bl_ws_bwd"] = g.m2scan_blend_bwd_workspace_bytes(8192, 8, 256, 16)
 res["status_str_ok"] = g.m2scan_status_str(0)
 print(json.dumps(res))

@@ -58,6 +58,8 @@ NULL, SHAPE, ALIGN, ALIAS, WORKSPACE = 1, 2, 3, 4, 5
     ("bg_misaligned_dy", ALIGN), ("bg_misaligned_db", ALIGN), ("bg_null_ws", WORKSPACE),
     ("bg_short_ws", WORKSPACE), ("bg_misaligned_ws", ALIGN), ("bg_alias_db_dy", ALIAS),
     ("bg_alias_ws_dy", ALIAS), ("bg_alias_db_ws", ALIAS),
+    ("bl_fwd_null_ws", WORKSPACE), ("bl_fwd_misaligned_w", ALIGN), ("bl_fwd_alias_ws_out", ALIAS),
+    ("bl_bwd_short_ws", WORKSPACE), ("bl_bwd_alias_dw_ws", ALIAS),
 ])
 def test_host_validation(probe, key, expect):
     assert probe[key] == expect, (key, probe[key])
@@ -79,6 +81,12 @@ def test_bias_grad_workspace_query(probe):
     assert probe["bg_ws_N0"] == 0
     assert probe["bg_ws_big"] == 152 * 7 * 4
     assert probe["bg_ws_bad"] == 0
+
+
+def test_blend_workspace_query(probe):
+    # W_O = w / D broadcast to [D, SH2]; the backward adds it and dW_O to its own workspace
+    assert probe["bl_ws_fwd"] == 16 * 256 * 4
+    assert probe["bl_ws_bwd"] == probe["ws_bytes_pages"] + 2 * 16 * 256 * 4
 
 
 def test_path_choice(probe):
