@@ -32,6 +32,26 @@ def test_autograd_matches_oracle(B, K, SH2, D):
         assert_parity(name, leaves[k].grad.cpu().numpy(), ref[name])
 
 
+def test_autograd_with_gate_multiplier():
+    import torch
+    import oracle
+    from gated_ssm_temporal_gb300.autograd import gated_temporal_scan
+    ensure_built()
+    x = make_inputs(Workload("custom", 200, 8, 256, 16, 0.3, 9, 1.0, 1.0))
+    d = to_dev(x)
+    leaves = _leaves(d)
+    gs = torch.tensor([0.8], device="cuda")
+    y = gated_temporal_scan(*(leaves[k] for k in GRADS), d["tw"], gs)
+    y.backward(d["d_h_enriched"])
+    ref = {"h_enriched": oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"],
+                                        x["W_O"], x["tw"], gate_scale=0.8)}
+    ref.update(oracle.backward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"], x["W_O"],
+                               x["tw"], x["d_h_enriched"], gate_scale=0.8))
+    assert_parity("h_enriched", y.detach().cpu().numpy(), ref["h_enriched"])
+    for k, name in GRADS.items():
+        assert_parity(name, leaves[k].grad.cpu().numpy(), ref[name])
+
+
 def test_cuda_graph_replays_the_eager_step():
     import torch
     from gated_ssm_temporal_gb300.autograd import gated_temporal_scan
