@@ -86,6 +86,8 @@ def load_library(path: str | None = None):
         lib.m2scan_bias_grad_workspace_bytes.restype = sz
         lib.m2scan_bias_grad.argtypes = [vp, i64, i32, vp, i32, vp, sz, vp]
         lib.m2scan_bias_grad.restype = ctypes.c_int
+        lib.m2scan_fwd_bf16.argtypes = [vp] * 6 + [f32, vp, i64, i32, i32, i32, vp, vp]
+        lib.m2scan_fwd_bf16.restype = ctypes.c_int
         lib.m2scan_blend_fwd_workspace_bytes.argtypes = [i32, i32]
         lib.m2scan_blend_fwd_workspace_bytes.restype = sz
         lib.m2scan_blend_bwd_workspace_bytes.argtypes = [i64, i32, i32, i32]
@@ -359,3 +361,36 @@ def bwd_blend(h_history, h_s2, W_A, W_B, W_C, d_h_enriched, temporal_weight=None
     if st != M2SCAN_OK:
         raise M2ScanError(st, "m2scan_bwd_blend")
     return outs
+
+
+def m2scan_fwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, tw, gate_scale, B, K, SH2, D, h_enriched,
+                    stream=0):
+    return load_library().m2scan_fwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, float(tw),
+                                          gate_scale, B, K, SH2, D, h_enriched, stream)
+
+
+def _check_bf16(t, name, shape):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+        raise TypeError("%s must be a bfloat16 CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t.data_ptr()
+
+
+def fwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, tw, out=None, stream=None, gate_scale=None):
+    """Layer forward with bfloat16 h_history, h_s2 and h_enriched (fp32 weights and sums)."""
+    import torch
+    B, K, SH2, D = dims_of(h_history, W_A)
+    if out is None:
+        out = torch.empty((B, SH2), device=h_history.device, dtype=torch.bfloat16)
+    st = m2scan_fwd_bf16(_check_bf16(h_history, "h_history", (B, K, SH2)),
+                         _check_bf16(h_s2, "h_s2", (B, SH2)), _check(W_A, "W_A", (SH2, D)),
+                         _check(W_B, "W_B", (SH2, D)), _check(W_C, "W_C", (SH2, D)),
+                         _check(W_O, "W_O", (D, SH2)), tw, _gate_ptr(gate_scale), B, K, SH2, D,
+                         _check_bf16(out, "h_enriched", (B, SH2)), _stream(stream))
+    if st != M2SCAN_OK:
+        raise M2ScanError(st, "m2scan_fwd_bf16")
+    return out

@@ -75,6 +75,7 @@ m2scan_status prepare_device(int* dev_out) {
   if ((e = prepare_fwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_bwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_fwd_tc16_kernels(smem)) != cudaSuccess) return cuda_fail(e);
+  if ((e = prepare_fwd_bf16_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_wide_kernels()) != cudaSuccess) return cuda_fail(e);
   void* p = nullptr;
   if ((e = cudaGetSymbolAddress(&p, g_m2scan_err_word)) != cudaSuccess) return cuda_fail(e);
@@ -148,11 +149,32 @@ int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_
 }
 
 CUresult encode_map(CUtensorMap* m, const float* ptr, int rank, const cuuint64_t* dims,
-                    const cuuint64_t* strides, const cuuint32_t* box) {
+                    const cuuint64_t* strides, const cuuint32_t* box,
+                    CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_FLOAT32) {
   const cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<float*>(ptr), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return g_encode(m, type, rank, const_cast<float*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// bf16 h_history [SH2, K, B] (box [64, K, S_max]) and h_s2 [SH2, B] (box
+// [64, S_max]): 64 bf16 = one 128-byte swizzled row per box row.
+bool encode_bf16_maps(FastArgs* a, const void* h_history, const void* h_s2, int64_t B) {
+  const cuuint64_t SH2 = static_cast<cuuint64_t>(a->SH2), K = static_cast<cuuint64_t>(a->K);
+  const cuuint64_t d3[3] = {SH2, K, static_cast<cuuint64_t>(B)};
+  const cuuint64_t s3[2] = {SH2 * 2, SH2 * K * 2};
+  const cuuint32_t b3[3] = {64u, static_cast<cuuint32_t>(K), static_cast<cuuint32_t>(a->S_max)};
+  if (encode_map(&a->tm_h, static_cast<const float*>(h_history), 3, d3, s3, b3,
+                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t d2[2] = {SH2, static_cast<cuuint64_t>(B)};
+  const cuuint64_t s2[1] = {SH2 * 2};
+  const cuuint32_t b2[2] = {64u, static_cast<cuuint32_t>(a->S_max)};
+  if (encode_map(&a->tm_hs, static_cast<const float*>(h_s2), 2, d2, s2, b2,
+                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != CUDA_SUCCESS)
+    return false;
+  std::memcpy(&a->tm_g, &a->tm_hs, sizeof(CUtensorMap));
+  return true;
 }
 
 // Tensor maps of the fast kernels: h_history as [SH2, K, B] with box
@@ -277,6 +299,46 @@ m2scan_status m2scan_fwd_ex(const float* h_history, const float* h_s2, const flo
                    B, K, SH2, D, tw, gate_scale};
     e = launch_generic(false, ga, grid, generic_smem_bytes(false, K, SH2, D), stream);
   }
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = 1;
+  return M2SCAN_OK;
+}
+
+m2scan_status m2scan_fwd_bf16(const void* h_history, const void* h_s2, const float* W_A,
+                              const float* W_B, const float* W_C, const float* W_O, float tw,
+                              const float* gate_scale, int64_t B, int32_t K, int32_t SH2,
+                              int32_t D, void* h_enriched, m2scan_stream_t stream) {
+  t_last_launches = 0;
+  m2scan_status st = check_shape(B, K, SH2, D);
+  if (st != M2SCAN_OK) return st;
+  FastArgs fa;
+  if (!fwd_bf16_plan(K, SH2, D, &fa) || B > 0x7fffffffll) return M2SCAN_ERR_UNSUPPORTED;
+  if (!W_A || !W_B || !W_C || !W_O) return M2SCAN_ERR_NULL;
+  if (B > 0 && (!h_history || !h_s2 || !h_enriched)) return M2SCAN_ERR_NULL;
+  const void* ptrs[] = {h_history, h_s2, W_A, W_B, W_C, W_O, h_enriched};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return M2SCAN_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(gate_scale) & 3u) != 0) return M2SCAN_ERR_ALIGN;
+  const uint64_t nw = static_cast<uint64_t>(SH2) * D * 4;
+  const uint64_t nb = static_cast<uint64_t>(B) * SH2 * 2;  // bf16 rows
+  const Span out = span(h_enriched, nb);
+  const Span ins[] = {span(h_history, nb * K), span(h_s2, nb), span(W_A, nw), span(W_B, nw),
+                      span(W_C, nw), span(W_O, nw), span(gate_scale, gate_scale ? 4 : 0)};
+  for (const Span& s : ins)
+    if (overlaps(out, s)) return M2SCAN_ERR_ALIAS;
+  if (B == 0) return M2SCAN_OK;
+  int dev = 0;
+  if ((st = prepare_device(&dev)) != M2SCAN_OK) return st;
+  if (fa.smem_bytes > g_max_smem[dev]) return M2SCAN_ERR_UNSUPPORTED;
+  fa.h_history = static_cast<const float*>(h_history);
+  fa.h_s2 = static_cast<const float*>(h_s2);
+  fa.g = nullptr;
+  fa.W_A = W_A; fa.W_B = W_B; fa.W_C = W_C; fa.W_O = W_O;
+  fa.out0 = static_cast<float*>(h_enriched); fa.out1 = nullptr; fa.ws = nullptr;
+  fa.gate_scale = gate_scale;
+  fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
+  if (!encode_bf16_maps(&fa, h_history, h_s2, B)) return M2SCAN_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_fwd_bf16(fa, slots_for(B), stream);
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_launches = 1;
   return M2SCAN_OK;

@@ -111,6 +111,11 @@ cudaError_t launch_fwd_tc(int D, const FastArgs& a, int grid, cudaStream_t strea
 // accumulator sets; plan->tc = 2).
 bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_fwd_tc16(const FastArgs& a, int grid, cudaStream_t stream);
+// Tensor-core forward with bf16 activations (D = 16, SH2 % 64 == 0, SH2 <= 256,
+// K <= 128; plan->tc = 3). tm_h / tm_hs must describe bf16 tensors.
+bool fwd_bf16_plan(int K, int SH2, int D, FastArgs* a);
+cudaError_t launch_fwd_bf16(const FastArgs& a, int grid, cudaStream_t stream);
+cudaError_t prepare_fwd_bf16_kernels(int max_smem);
 // Warp-specialised tensor-core backward (D = 16).
 bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_bwd_tc(const FastArgs& a, int grid, cudaStream_t stream);

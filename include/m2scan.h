@@ -137,6 +137,22 @@ m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const flo
                             void* workspace, size_t workspace_bytes, m2scan_stream_t stream);
 
 /*
+ * Forward pass with bf16 activations ("bf16 inputs/outputs with fp32
+ * accumulation", which halves the bytes of this memory-bound pass):
+ * h_history [B,K,SH2] and h_s2 [B,SH2] are bfloat16 (raw 16-bit words, device,
+ * 16-byte aligned), the weights fp32 as for m2scan_fwd, h_enriched [B,SH2]
+ * bfloat16 (the fp32 result rounded to nearest even). Every product and sum
+ * is fp32; the projections use W split into two bf16 parts (16 significant
+ * bits, against the output's 8). gate_scale as for m2scan_fwd_ex. Shapes:
+ * D = 16, SH2 % 64 == 0, SH2 <= 256, K <= 128; others return
+ * M2SCAN_ERR_UNSUPPORTED. One kernel launch (none when B == 0).
+ */
+m2scan_status m2scan_fwd_bf16(const void* h_history, const void* h_s2, const float* W_A,
+                              const float* W_B, const float* W_C, const float* W_O, float tw,
+                              const float* gate_scale, int64_t B, int32_t K, int32_t SH2,
+                              int32_t D, void* h_enriched, m2scan_stream_t stream);
+
+/*
  * The layer with the pages' own output step ("Custom Kernel Optimization
  * Implementation Plan", Task 1 Step 3) in place of tw * (ctx . W_O): one
  * scalar context per sample blended into every feature with a per-feature
