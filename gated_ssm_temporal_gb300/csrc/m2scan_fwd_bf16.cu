@@ -400,7 +400,32 @@ __global__ void __launch_bounds__(kBfThreads, 1) fwd_bf16_kernel(const __grid_co
       named_sync(1, kBfComputeThreads);
       if (tid == 0) mbar_arrive(&bb->accempty[t & 1]);
       // ============================== scan: one thread per (sample, state)
-      if (tid < S_t * D) {
+      if (tid < S_t * D && (K & 7) == 0) {
+        // K a multiple of 8: the swizzle offsets within a group of 8 rows are
+        // the same for every group
+        const int s = tid >> 4, d = tid & 15, rb = s * K;
+        int oa[8], ob[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          oa[u] = u * 32 + (((d >> 2) ^ u) << 2) + (d & 3);
+          ob[u] = u * 32 + (((4 + (d >> 2)) ^ u) << 2) + (d & 3);
+        }
+        float x = 0.f;
+        for (int g8 = 0; g8 < K; g8 += 8) {
+          const float* pg = sP + (rb + g8) * 32;
+          float av[8], bv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            av[u] = pg[oa[u]];
+            bv[u] = pg[ob[u]];
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) av[u] = gsc * sigmoid_fast(av[u]);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) x = fmaf(av[u], x, bv[u]);
+        }
+        sCtx[s * D + d] = sC[s * D + d] * x;
+      } else if (tid < S_t * D) {
         const int s = tid >> 4, d = tid & 15, rb = s * K;
         float x = 0.f;
         for (int k0 = 0; k0 < K; k0 += 8) {
