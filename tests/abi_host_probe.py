@@ -117,5 +117,13 @@ res["bl_bwd_alias_dw_ws"] = g.m2scan_bwd_blend(
     W[14] + 64, W[14], g.m2scan_blend_bwd_workspace_bytes(B, K, SH2, D), 0)
 res["bl_ws_fwd"] = g.m2scan_blend_fwd_workspace_bytes(256, 16)
 res["bl_ws_bwd"] = g.m2scan_blend_bwd_workspace_bytes(8192, 8, 256, 16)
+res["bf16_B0_ok"] = g.m2scan_fwd_bf16(0, 0, W[2], W[3], W[4], W[5], 0.1, 0, 0, 8, 256, 16, 0, 0)
+res["bf16_sh2_96"] = g.m2scan_fwd_bf16(W[0], W[1], W[2], W[3], W[4], W[5], 0.1, 0, 8, 8, 96, 16,
+                                       W[6], 0)
+res["bf16_d8"] = g.m2scan_fwd_bf16(W[0], W[1], W[2], W[3], W[4], W[5], 0.1, 0, 8, 8, 256, 8, W[6], 0)
+res["bf16_misaligned"] = g.m2scan_fwd_bf16(W[0] + 2, W[1], W[2], W[3], W[4], W[5], 0.1, 0, 8, 8,
+                                           256, 16, W[6], 0)
+res["bf16_alias"] = g.m2scan_fwd_bf16(W[0], W[1], W[2], W[3], W[4], W[5], 0.1, 0, 8, 8, 256, 16,
+                                      W[0] + 1024, 0)
 res["status_str_ok"] = g.m2scan_status_str(0)
 print(json.dumps(res))

@@ -60,6 +60,8 @@ NULL, SHAPE, ALIGN, ALIAS, WORKSPACE = 1, 2, 3, 4, 5
     ("bg_alias_ws_dy", ALIAS), ("bg_alias_db_ws", ALIAS),
     ("bl_fwd_null_ws", WORKSPACE), ("bl_fwd_misaligned_w", ALIGN), ("bl_fwd_alias_ws_out", ALIAS),
     ("bl_bwd_short_ws", WORKSPACE), ("bl_bwd_alias_dw_ws", ALIAS),
+    ("bf16_B0_ok", 0), ("bf16_sh2_96", 6), ("bf16_d8", 6), ("bf16_misaligned", ALIGN),
+    ("bf16_alias", ALIAS),
 ])
 def test_host_validation(probe, key, expect):
     assert probe[key] == expect, (key, probe[key])
