@@ -1,0 +1,516 @@
+"""Executable models of the mbarrier protocols of the tensor-core kernels.
+
+Each model replays, for one CTA, the sequence of barrier waits, arrivals and
+tensor-core commits of every role of a kernel (producer, MMA issuers,
+compute warps) as Python generators, and a scheduler runs them in random
+interleavings with asynchronous completions: TMA loads complete in any
+order, the commits of one issuing thread in issue order. The run fails on
+
+* a deadlock (no role can move and nothing is in flight),
+* parity aliasing (a waiter two phases behind its barrier, which a parity
+  wait cannot tell apart from the phase it wants),
+* a hazard: a stage reloaded while a role still reads it, a tensor-memory
+  buffer or accumulator set written while another role reads or writes it.
+
+The models follow the kernels' source (``fwd_tc16_kernel``,
+``bwd_tc_kernel``, ``fwd_bf16_kernel``): the same item order, barrier
+counts, ring sizes and wait parities. ``mutation`` plants a protocol mistake
+(a dropped wait) so that the tests can check the checker.
+"""
+import random
+
+kRowItem = 16
+kBwdSampleItem = 8
+kChunkRing = 6
+kLoBufs = 3
+
+
+class Bar:
+    """An mbarrier: ``count`` arrivals complete a phase."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.completed = name, count, count, 0
+
+    def arrive(self, n=1):
+        self.pending -= n
+        assert self.pending >= 0, ("over-arrival", self.name)
+        if self.pending == 0:
+            self.completed += 1
+            self.pending = self.count
+
+
+def W(name, n):
+    """Wait for phase n of a barrier (the kernels wait with parity n & 1)."""
+    return ("wait", name, n)
+
+
+def schedule(actors, bars, events, seed, limit=10 ** 6):
+    """Run the role generators to completion in a random interleaving."""
+    rnd = random.Random(seed)
+    blocked = {k: None for k in actors}
+    done = set()
+    for _ in range(limit):
+        if len(done) == len(actors):
+            break
+        runnable = []
+        for k in actors:
+            if k in done:
+                continue
+            w = blocked[k]
+            if w is None or w[0] == "yield":
+                runnable.append(k)
+            else:
+                b = bars[w[1]]
+                assert b.completed <= w[2] + 1, ("parity aliasing", k, w, b.completed)
+                if b.completed >= w[2] + 1:
+                    runnable.append(k)
+        queues = [q for q in events if events[q]]
+        if queues and (not runnable or rnd.random() < 0.5):
+            q = rnd.choice(queues)
+            name, cb = events[q].pop(rnd.randrange(len(events[q])) if q == "tma" else 0)
+            if cb:
+                cb()
+            bars[name].arrive()
+            continue
+        if not runnable:
+            raise RuntimeError("deadlock: %s" % {k: blocked[k] for k in actors if k not in done})
+        k = rnd.choice(runnable)
+        blocked[k] = None
+        try:
+            blocked[k] = next(actors[k])
+        except StopIteration:
+            done.add(k)
+    else:
+        raise RuntimeError("no progress within the step limit")
+    assert not any(events.values()), "completions left over"
+
+
+def tiles(B, P, cta, K):
+    """Sample counts of the CTA's tiles (the kernels' balanced split)."""
+    S_max = min(128 // K, 16)
+    cb0 = B * cta // P
+    n_c = B * (cta + 1) // P - cb0
+    T = (n_c + S_max - 1) // S_max
+    if T == 0:
+        return []
+    t_base, t_extra = n_c // T, n_c - (n_c // T) * T
+    ts = lambda i: cb0 + i * t_base + min(i, t_extra)
+    return [ts(i + 1) - ts(i) for i in range(T)]
+
+
+def post_item(p, NSI, NRI):
+    """The backward's item order after a tile's chunks: sample item 0, row
+    items 0-3, the other sample items, the other row items."""
+    if NSI > 0:
+        if p == 0:
+            return 1, 0
+        p -= 1
+    r1 = min(NRI, 4)
+    if p < r1:
+        return 2, p
+    p -= r1
+    s1 = NSI - 1 if NSI > 0 else 0
+    if p < s1:
+        return 1, 1 + p
+    return 2, 4 + (p - s1)
+
+
+# --------------------------------------------------------------- forward
+
+def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
+    """fwd_tc16_kernel: producer rounds (tile u's chunks, then tile u-1's h_s2
+    rows), a main and a remainder MMA thread, the compute warps."""
+    S = tiles(B, P, cta, K)
+    T, NC = len(S), SH2 // 32
+    bars = {}
+    for s in range(NST):
+        bars["full%d" % s] = Bar("full", 1)
+        bars["empty%d" % s] = Bar("empty", 2)
+        bars["outdone%d" % s] = Bar("outdone", 1)
+    for s in range(kChunkRing):
+        bars["loready%d" % s] = Bar("loready", 1)
+    for s in range(kLoBufs):
+        bars["lofree%d" % s] = Bar("lofree", 1)
+    for s in range(2):
+        bars["mdone%d" % s] = Bar("mdone", 1)
+        bars["accempty%d" % s] = Bar("accempty", 1)
+    events = {"tma": [], "main": [], "corr": []}
+    st_read = [set() for _ in range(NST)]
+    lo_read = [0] * kLoBufs
+    acc_w, acc_r = [0, 0], [None, None]
+    rounds = lambda u: (NC if u < T else 0) + (1 if u >= 1 else 0)
+    items = []
+    for u in range(T + 1):
+        items += ["chunk"] * (NC if u < T else 0) + (["out"] if u >= 1 else [])
+
+    def producer():
+        use = {"empty": [0] * NST, "outdone": [0] * NST}
+        for pn in range(len(items)):
+            if pn >= NST:
+                rn = pn - NST
+                b = "empty" if items[rn] == "chunk" else "outdone"
+                st = rn % NST
+                yield W("%s%d" % (b, st), use[b][st])
+                use[b][st] += 1
+            st = pn % NST
+            assert not st_read[st], ("stage reloaded while read", st)
+            events["tma"].append(("full%d" % st, None))
+
+    def main():
+        tp = 0
+        for t in range(T):
+            if t >= 2 and mutation != "no_accempty_wait":
+                yield W("accempty%d" % (t & 1), (t - 2) >> 1)
+            assert acc_r[t & 1] is None, "main products into a set being read"
+            for q in range(NC):
+                it = tp + q
+                st = it % NST
+                yield W("full%d" % st, it // NST)
+                st_read[st].add(("m", it))
+                acc_w[t & 1] += 1
+
+                def done(st=st, it=it, s=t & 1):
+                    st_read[st].discard(("m", it))
+                    acc_w[s] -= 1
+                events["main"].append(("empty%d" % st, done))
+            events["main"].append(("mdone%d" % (t & 1), None))
+            tp += rounds(t)
+
+    def corr():
+        tp = c = 0
+        for t in range(T):
+            if t >= 2:
+                yield W("accempty%d" % (t & 1), (t - 2) >> 1)
+            for q in range(NC):
+                yield W("loready%d" % (c % kChunkRing), c // kChunkRing)
+                assert acc_r[t & 1] is None, "remainder products into a set being read"
+                bars["empty%d" % ((tp + q) % NST)].arrive()
+                b = c % kLoBufs
+                lo_read[b] += 1
+                acc_w[t & 1] += 1
+
+                def done(b=b, s=t & 1):
+                    lo_read[b] -= 1
+                    acc_w[s] -= 1
+                events["corr"].append(("lofree%d" % b, done))
+                c += 1
+            tp += rounds(t)
+
+    def compute():
+        seq = c = 0
+        for t in range(T):
+            for q in range(NC):
+                st = seq % NST
+                yield W("full%d" % st, seq // NST)
+                st_read[st].add(("c", seq))
+                if q > 0:
+                    bars["loready%d" % ((c - 1) % kChunkRing)].arrive()
+                    st_read[(seq - 1) % NST].discard(("c", seq - 1))
+                if c >= kLoBufs and mutation != "no_lofree_wait":
+                    yield W("lofree%d" % (c % kLoBufs), c // kLoBufs - 1)
+                assert lo_read[c % kLoBufs] == 0, "remainder buffer written while read"
+                seq += 1
+                c += 1
+            bars["loready%d" % ((c - 1) % kChunkRing)].arrive()
+            st_read[(seq - 1) % NST].discard(("c", seq - 1))
+            if t >= 1:
+                st = seq % NST
+                yield W("full%d" % st, seq // NST)
+                st_read[st].add(("o", seq))
+                yield ("yield",)
+                st_read[st].discard(("o", seq))
+                bars["outdone%d" % st].arrive()
+                seq += 1
+            yield W("mdone%d" % (t & 1), t >> 1)
+            if mutation != "no_last_lofree_wait":
+                yield W("lofree%d" % ((c - 1) % kLoBufs), (c - 1) // kLoBufs)
+            assert acc_w[t & 1] == 0, "projections read while written"
+            acc_r[t & 1] = t
+            yield ("yield",)
+            acc_r[t & 1] = None
+            bars["accempty%d" % (t & 1)].arrive()
+        if T:
+            st = seq % NST
+            yield W("full%d" % st, seq // NST)
+            bars["outdone%d" % st].arrive()
+
+    schedule({"p": producer(), "m": main(), "r": corr(), "c": compute()}, bars, events, seed)
+
+
+def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
+    """fwd_bf16_kernel: the same rounds with 64-column chunks and one MMA
+    thread; a chunk stage is freed by the MMA commit and the compute warps."""
+    S = tiles(B, P, cta, K)
+    T, NC = len(S), SH2 // 64
+    bars = {}
+    for s in range(NST):
+        bars["full%d" % s] = Bar("full", 1)
+        bars["empty%d" % s] = Bar("empty", 2)
+        bars["outdone%d" % s] = Bar("outdone", 1)
+    for s in range(2):
+        bars["mdone%d" % s] = Bar("mdone", 1)
+        bars["accempty%d" % s] = Bar("accempty", 1)
+    events = {"tma": [], "mma": []}
+    st_read = [set() for _ in range(NST)]
+    acc_w, acc_r = [0, 0], [None, None]
+    rounds = lambda u: (NC if u < T else 0) + (1 if u >= 1 else 0)
+    items = []
+    for u in range(T + 1):
+        items += ["chunk"] * (NC if u < T else 0) + (["out"] if u >= 1 else [])
+
+    def producer():
+        use = {"empty": [0] * NST, "outdone": [0] * NST}
+        for pn in range(len(items)):
+            if pn >= NST:
+                rn = pn - NST
+                b = "empty" if items[rn] == "chunk" else "outdone"
+                st = rn % NST
+                yield W("%s%d" % (b, st), use[b][st])
+                use[b][st] += 1
+            st = pn % NST
+            assert not st_read[st], ("stage reloaded while read", st)
+            events["tma"].append(("full%d" % st, None))
+
+    def mma():
+        tp = 0
+        for t in range(T):
+            if t >= 2 and mutation != "no_accempty_wait":
+                yield W("accempty%d" % (t & 1), (t - 2) >> 1)
+            assert acc_r[t & 1] is None, "products into a set being read"
+            for q in range(NC):
+                it = tp + q
+                st = it % NST
+                yield W("full%d" % st, it // NST)
+                st_read[st].add(("m", it))
+                acc_w[t & 1] += 1
+
+                def done(st=st, it=it, s=t & 1):
+                    st_read[st].discard(("m", it))
+                    acc_w[s] -= 1
+                events["mma"].append(("empty%d" % st, done))
+            events["mma"].append(("mdone%d" % (t & 1), None))
+            tp += rounds(t)
+
+    def compute():
+        seq = 0
+        for t in range(T):
+            for q in range(NC):
+                st = seq % NST
+                yield W("full%d" % st, seq // NST)
+                if mutation == "early_empty":
+                    bars["empty%d" % st].arrive()
+                st_read[st].add(("c", seq))
+                yield ("yield",)
+                st_read[st].discard(("c", seq))
+                if mutation != "early_empty":
+                    bars["empty%d" % st].arrive()
+                seq += 1
+            if t >= 1:
+                st = seq % NST
+                yield W("full%d" % st, seq // NST)
+                st_read[st].add(("o", seq))
+                yield ("yield",)
+                st_read[st].discard(("o", seq))
+                bars["outdone%d" % st].arrive()
+                seq += 1
+            if mutation != "no_mdone_wait":
+                yield W("mdone%d" % (t & 1), t >> 1)
+            assert acc_w[t & 1] == 0, "projections read while written"
+            acc_r[t & 1] = t
+            yield ("yield",)
+            acc_r[t & 1] = None
+            bars["accempty%d" % (t & 1)].arrive()
+        if T:
+            st = seq % NST
+            yield W("full%d" % st, seq // NST)
+            bars["outdone%d" % st].arrive()
+
+    schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)
+
+
+# -------------------------------------------------------------- backward
+
+def bwd_tc(B, P, cta, K, SH2, NST, seed, mutation=None):
+    """bwd_tc_kernel: producer (chunks, then sample and row items; it stores
+    an item's outputs before reusing its stage), the main MMA thread (main
+    projection products, d_h halves, dW per row item), the remainder MMA
+    thread, the compute warps."""
+    S = tiles(B, P, cta, K)
+    if not S:
+        return
+    NC = SH2 // 32
+    NSI = lambda s: (s + kBwdSampleItem - 1) // kBwdSampleItem
+    NRI = lambda s: (s * K + kRowItem - 1) // kRowItem
+    bars = {}
+    for s in range(NST):
+        bars["full%d" % s] = Bar("full", 1)
+        bars["empty%d" % s] = Bar("empty", 1)
+        bars["cempty%d" % s] = Bar("cempty", 2)
+    for s in range(kChunkRing):
+        bars["loready%d" % s] = Bar("loready", 1)
+    for s in range(kLoBufs):
+        bars["lofree%d" % s] = Bar("lofree", 1)
+    for s in range(2):
+        for n in ("dhready", "dhfree", "htready", "htfree"):
+            bars["%s%d" % (n, s)] = Bar(n, 1)
+    for n in ("bready", "dwdone", "mdone"):
+        bars[n] = Bar(n, 1)
+    events = {"tma": [], "main": [], "corr": []}
+    fl = {"main": 0, "corr": 0, "dh": 0, "dw": [0, 0], "lo": [0] * kLoBufs}
+    st_read = [set() for _ in range(NST)]
+    reading = {"P": False, "L": False}
+    kinds = []
+    for s in S:
+        kinds += ["chunk"] * NC + ["item"] * (NSI(s) + NRI(s))
+
+    def producer():
+        use = {"cempty": [0] * NST, "empty": [0] * NST}
+        for pn in range(len(kinds)):
+            if pn >= NST:
+                rn = pn - NST
+                b = "cempty" if kinds[rn] == "chunk" else "empty"
+                st = rn % NST
+                yield W("%s%d" % (b, st), use[b][st])
+                use[b][st] += 1
+            st = pn % NST
+            assert not st_read[st], ("stage reloaded while read", st)
+            events["tma"].append(("full%d" % st, None))
+
+    def main():
+        seq = ri = 0
+        for t, s in enumerate(S):
+            nsi, nri = NSI(s), NRI(s)
+            if t > 0 and mutation != "no_dhfree1_wait":
+                yield W("dhfree1", t - 1)
+            for q in range(NC):
+                it = seq + q
+                st = it % NST
+                yield W("full%d" % st, it // NST)
+                # d_h of the previous tile may still run: same thread, in order
+                assert not reading["P"], "main products over P in use"
+                st_read[st].add(("m", it))
+                fl["main"] += 1
+
+                def done(st=st, it=it):
+                    st_read[st].discard(("m", it))
+                    fl["main"] -= 1
+                events["main"].append(("cempty%d" % st, done))
+            events["main"].append(("mdone", None))
+            seq += NC + nsi + nri
+            yield W("bready", t)
+
+            def dh():
+                assert not reading["P"], "d_h over P in use"
+                fl["dh"] += 1
+
+                def done():
+                    fl["dh"] -= 1
+                return done
+            events["main"].append(("dhready0", dh()))
+            for k in range(nri):
+                if k == 4:
+                    yield W("dhfree0", t)
+                    events["main"].append(("dhready1", dh()))
+                yield W("htready%d" % (ri & 1), ri >> 1)
+                p = ri & 1
+                fl["dw"][p] += 1
+
+                def done(p=p):
+                    fl["dw"][p] -= 1
+                events["main"].append(("htfree%d" % p, done))
+                ri += 1
+            if nri <= 4:
+                yield W("dhfree0", t)
+                events["main"].append(("dhready1", dh()))
+        events["main"].append(("dwdone", None))
+
+    def corr():
+        seq = c = 0
+        for s in S:
+            for q in range(NC):
+                yield W("loready%d" % (c % kChunkRing), c // kChunkRing)
+                assert fl["dw"] == [0, 0] and not reading["L"], "remainder products over L in use"
+                bars["cempty%d" % ((seq + q) % NST)].arrive()
+                b = c % kLoBufs
+                fl["lo"][b] += 1
+                fl["corr"] += 1
+
+                def done(b=b):
+                    fl["lo"][b] -= 1
+                    fl["corr"] -= 1
+                events["corr"].append(("lofree%d" % b, done))
+                c += 1
+            seq += NC + NSI(s) + NRI(s)
+
+    def compute():
+        seq = c = ri = 0
+        for t, s in enumerate(S):
+            nsi, nri = NSI(s), NRI(s)
+            if mutation != "no_htfree_wait":
+                if ri >= 1:
+                    yield W("htfree%d" % ((ri - 1) & 1), (ri - 1) >> 1)
+                if ri >= 2:
+                    yield W("htfree%d" % (ri & 1), (ri - 2) >> 1)
+            for q in range(NC):
+                st = seq % NST
+                yield W("full%d" % st, seq // NST)
+                st_read[st].add(("c", seq))
+                if q > 0:
+                    bars["loready%d" % ((c - 1) % kChunkRing)].arrive()
+                    st_read[(seq - 1) % NST].discard(("c", seq - 1))
+                if c >= kLoBufs:
+                    yield W("lofree%d" % (c % kLoBufs), c // kLoBufs - 1)
+                assert fl["lo"][c % kLoBufs] == 0 and fl["dw"] == [0, 0], \
+                    "remainder written over L in use"
+                seq += 1
+                c += 1
+            bars["loready%d" % ((c - 1) % kChunkRing)].arrive()
+            st_read[(seq - 1) % NST].discard(("c", seq - 1))
+            yield W("mdone", t)
+            yield W("lofree%d" % ((c - 1) % kLoBufs), (c - 1) // kLoBufs)
+            assert fl["main"] == 0 and fl["corr"] == 0 and fl["dh"] == 0, "projections read early"
+            reading["P"] = reading["L"] = True
+            yield ("yield",)
+            reading["P"] = reading["L"] = False
+            bars["bready"].arrive()
+            for p in range(nsi + nri):
+                kind, k = post_item(p, nsi, nri)
+                st = seq % NST
+                yield W("full%d" % st, seq // NST)
+                if kind == 1:
+                    bars["empty%d" % st].arrive()
+                    seq += 1
+                    continue
+                if ri >= 2:
+                    yield W("htfree%d" % (ri & 1), (ri - 2) >> 1)
+                assert fl["dw"][ri & 1] == 0 and fl["corr"] == 0, "transposed rows over L in use"
+                bars["htready%d" % (ri & 1)].arrive()
+                rh = k >> 2
+                if mutation == "early_row_empty":
+                    bars["empty%d" % st].arrive()
+                    st_read[st].add(("r", seq))
+                    yield ("yield",)
+                if (k & 3) == 0:
+                    yield W("dhready%d" % rh, t)
+                    assert fl["dh"] == 0 and fl["main"] == 0, "d_h read early"
+                    reading["P"] = True
+                assert fl["main"] == 0, "d_h overwritten while read"
+                yield ("yield",)  # the item's d_h rows read back
+                assert fl["main"] == 0, "d_h overwritten while read"
+                if (k & 3) == 3 or k == nri - 1:
+                    reading["P"] = False
+                    bars["dhfree%d" % rh].arrive()
+                if mutation == "early_row_empty":
+                    st_read[st].discard(("r", seq))
+                else:
+                    bars["empty%d" % st].arrive()
+                seq += 1
+                ri += 1
+            if nri <= 4:
+                bars["dhfree1"].arrive()
+        yield W("dwdone", 0)
+
+    schedule({"p": producer(), "m": main(), "r": corr(), "c": compute()}, bars, events, seed)
+
+
+MODELS = {"fwd_tc16": fwd_tc16, "fwd_bf16": fwd_bf16, "bwd_tc": bwd_tc}

@@ -1,0 +1,69 @@
+"""The barrier protocols of the tensor-core kernels, checked on executable
+models (``protocol_models``): random interleavings of every role over the
+kernels' tile splits, ring depths and item counts must finish without a
+deadlock, a parity alias or a buffer hazard, and each planted protocol
+mistake must be caught."""
+import itertools
+
+import pytest
+
+import protocol_models as pm
+
+P = 152
+# (B, K): the layer's workload, ragged splits, a CTA with one or no sample,
+# the narrowest and widest histories
+SHAPES = [(8192, 8), (65536, 8), (1000, 8), (300, 16), (152, 8), (20, 8), (700, 1), (400, 128), (333, 3)]
+WIDTHS = {"fwd_tc16": (256, 64, 32), "fwd_bf16": (256, 128, 64), "bwd_tc": (256, 64, 32)}
+
+
+@pytest.mark.parametrize("model", sorted(pm.MODELS))
+def test_protocol_runs_clean(model):
+    f = pm.MODELS[model]
+    for (B, K), SH2, NST, cta in itertools.product(SHAPES, WIDTHS[model], (2, 3, 5, 6), (0, 77, P - 1)):
+        for seed in range(6):
+            f(B, P, cta, K, SH2, NST, seed)
+
+
+def test_tile_split_covers_the_slice():
+    for B, K in SHAPES:
+        S_max = min(128 // K, 16)
+        total = 0
+        for cta in range(P):
+            sizes = pm.tiles(B, P, cta, K)
+            assert all(1 <= s <= S_max for s in sizes)
+            assert not sizes or max(sizes) - min(sizes) <= 1
+            total += sum(sizes)
+        assert total == B
+
+
+def test_post_item_order_is_a_permutation():
+    for nsi, nri in itertools.product(range(0, 4), range(0, 10)):
+        seen = [pm.post_item(p, nsi, nri) for p in range(nsi + nri)]
+        assert sorted(seen) == sorted([(1, i) for i in range(nsi)] + [(2, i) for i in range(nri)])
+        if nsi and nri:
+            assert seen[0] == (1, 0) and seen[1] == (2, 0)
+
+
+MUTATIONS = [
+    ("fwd_tc16", "no_lofree_wait"),
+    ("fwd_tc16", "no_last_lofree_wait"),
+    ("fwd_tc16", "no_accempty_wait"),
+    ("fwd_bf16", "no_accempty_wait"),
+    ("fwd_bf16", "no_mdone_wait"),
+    ("fwd_bf16", "early_empty"),
+    ("bwd_tc", "no_htfree_wait"),
+    ("bwd_tc", "no_dhfree1_wait"),
+    ("bwd_tc", "early_row_empty"),
+]
+
+
+@pytest.mark.parametrize("model,mutation", MUTATIONS)
+def test_planted_protocol_mistake_is_caught(model, mutation):
+    f = pm.MODELS[model]
+    for (B, K), SH2, NST in itertools.product(SHAPES[:3], WIDTHS[model], (6, 4, 3)):
+        for seed in range(4):
+            try:
+                f(B, P, 0, K, SH2, NST, seed, mutation=mutation)
+            except (AssertionError, RuntimeError):
+                return
+    pytest.fail("%s: %s not detected" % (model, mutation))
