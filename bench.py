@@ -50,6 +50,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32",
+                    help="activations (h_history, h_s2, d_h_enriched and the layer's outputs) "
+                         "in fp32 or bfloat16; arithmetic is fp32 either way")
     return ap.parse_args(argv)
 
 
@@ -238,20 +241,34 @@ def run_native(args, rank, world, local):
     B, K, SH2, D = w.B, w.K, w.SH2, w.D
     x = make_inputs(w)
     dev = torch.device("cuda", local)
+    bf16 = args.dtype == "bf16"
+    act_dtype = torch.bfloat16 if bf16 else torch.float32
+    acts = ("h_history", "h_s2", "d_h_enriched")
     d = {k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v) for k, v in x.items()}
-    y = torch.empty((B, SH2), device=dev)
-    outs = g.alloc_bwd_outputs(B, K, SH2, D, dev)
+    for k in acts:
+        d[k] = d[k].to(act_dtype)
+
+    def alloc_outs():
+        o = g.alloc_bwd_outputs(B, K, SH2, D, dev)
+        for k in ("d_h_history", "d_h_s2"):
+            o[k] = o[k].to(act_dtype)
+        return o
+
+    y = torch.empty((B, SH2), device=dev, dtype=act_dtype)
+    outs = alloc_outs()
     ws = g.alloc_workspace(B, K, SH2, D, dev)
     flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream()
+    fwd_call = g.fwd_bf16 if bf16 else g.fwd
+    bwd_call = g.bwd_bf16 if bf16 else g.bwd
 
     def fwd():
-        g.fwd(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"], out=y,
-              stream=stream)
+        fwd_call(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"], out=y,
+                 stream=stream)
 
     def bwd():
-        g.bwd(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"],
-              d["d_h_enriched"], outs=outs, workspace=ws, stream=stream)
+        bwd_call(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"],
+                 d["d_h_enriched"], outs=outs, workspace=ws, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -296,14 +313,15 @@ def run_native(args, rank, world, local):
     # sets of device buffers let step i+1's copy-in and step i-1's copy-out
     # run during step i's kernels (the host link is full duplex); the time
     # runs from the first copy-in to the last copy-out.
-    host_in = {k: torch.from_numpy(x[k]).pin_memory() for k in ("h_history", "h_s2", "d_h_enriched")}
-    host_out = {"h_enriched": torch.empty((B, SH2)).pin_memory()}
-    host_out.update({k: torch.empty(tuple(v.shape)).pin_memory() for k, v in outs.items()})
-    h2d = sum(t.numel() * 4 for t in host_in.values())
-    d2h = sum(t.numel() * 4 for t in host_out.values())
+    host_in = {k: torch.from_numpy(x[k]).to(act_dtype).pin_memory() for k in acts}
+    host_out = {"h_enriched": torch.empty((B, SH2), dtype=act_dtype).pin_memory()}
+    host_out.update({k: torch.empty(tuple(v.shape), dtype=v.dtype).pin_memory()
+                     for k, v in outs.items()})
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     dev_in = [d, dict(d, **{k: torch.empty_like(d[k]) for k in host_in})]
     dev_y = [y, torch.empty_like(y)]
-    dev_outs = [outs, g.alloc_bwd_outputs(B, K, SH2, D, dev)]
+    dev_outs = [outs, alloc_outs()]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
@@ -324,10 +342,10 @@ def run_native(args, rank, world, local):
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])  # step i-2's outputs have been copied out
-        g.fwd(di["h_history"], di["h_s2"], di["W_A"], di["W_B"], di["W_C"], di["W_O"], di["tw"],
-              out=dev_y[b], stream=stream)
-        g.bwd(di["h_history"], di["h_s2"], di["W_A"], di["W_B"], di["W_C"], di["W_O"], di["tw"],
-              di["d_h_enriched"], outs=do, workspace=ws, stream=stream)
+        fwd_call(di["h_history"], di["h_s2"], di["W_A"], di["W_B"], di["W_C"], di["W_O"], di["tw"],
+                 out=dev_y[b], stream=stream)
+        bwd_call(di["h_history"], di["h_s2"], di["W_A"], di["W_B"], di["W_C"], di["W_O"], di["tw"],
+                 di["d_h_enriched"], outs=do, workspace=ws, stream=stream)
         ev_comp[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
@@ -351,22 +369,25 @@ def run_native(args, rank, world, local):
 
     if rank != 0:
         return
-    ab = algorithmic_bytes(B, K, SH2)
+    ab = algorithmic_bytes(B, K, SH2, elem=2 if bf16 else 4)
     peak, peak_src = measured_peaks()
     achieved = ab["bwd"] / (bwd_ms / 1e3) / 1e9
-    traffic = recorded_traffic("m2scan_bwd")
+    traffic = recorded_traffic("m2scan_bwd_bf16" if bf16 else "m2scan_bwd")
+    bwd_kernel = ("m2scan_bwd_bf16 (per-sample generic kernel + slot reduction)" if bf16 else
+                  "m2scan_bwd (fused backward + slot reduction)")
     line = {
-        "metric": metric_for(w), "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
+        "metric": metric_for(w) + (" with bf16 activations" if bf16 else ""), "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g per rank" % (w.name, B, K, SH2, D,
                                                                              w.tw),
                    "B": B, "K": K, "SH2": SH2, "D": D, "parallelism": "replicas x%d" % world,
+                   "activations": args.dtype,
                    "l2": "flushed (512 MiB write) before every timed fwd and every timed bwd"},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "hbm_gbs": ab["total"] / (step_ms / 1e3) / 1e9,
         "hbm_frac_of_measured": ab["total"] / (step_ms / 1e3) / 1e9 / peak,
-        "roofline": {"kernel": "m2scan_bwd (fused backward + slot reduction)", "bound": "hbm",
+        "roofline": {"kernel": bwd_kernel, "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src + " hbm_gbs burst",
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": ab["bwd"]},

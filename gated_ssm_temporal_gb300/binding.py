@@ -88,6 +88,9 @@ def load_library(path: str | None = None):
         lib.m2scan_bias_grad.restype = ctypes.c_int
         lib.m2scan_fwd_bf16.argtypes = [vp] * 6 + [f32, vp, i64, i32, i32, i32, vp, vp]
         lib.m2scan_fwd_bf16.restype = ctypes.c_int
+        lib.m2scan_bwd_bf16.argtypes = ([vp] * 6 + [f32, vp, vp, i64, i32, i32, i32] + [vp] * 6
+                                        + [vp, sz, vp])
+        lib.m2scan_bwd_bf16.restype = ctypes.c_int
         lib.m2scan_blend_fwd_workspace_bytes.argtypes = [i32, i32]
         lib.m2scan_blend_fwd_workspace_bytes.restype = sz
         lib.m2scan_blend_bwd_workspace_bytes.argtypes = [i64, i32, i32, i32]
@@ -369,6 +372,15 @@ def m2scan_fwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, tw, gate_scale, B, K, S
                                           gate_scale, B, K, SH2, D, h_enriched, stream)
 
 
+def m2scan_bwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, tw, gate_scale, d_h_enriched, B, K, SH2,
+                    D, d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, workspace_bytes,
+                    stream=0):
+    return load_library().m2scan_bwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, float(tw),
+                                          gate_scale, d_h_enriched, B, K, SH2, D, d_h_history,
+                                          d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace,
+                                          workspace_bytes, stream)
+
+
 def _check_bf16(t, name, shape):
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
@@ -394,3 +406,33 @@ def fwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, tw, out=None, stream=None, gat
     if st != M2SCAN_OK:
         raise M2ScanError(st, "m2scan_fwd_bf16")
     return out
+
+
+def bwd_bf16(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, outs=None, workspace=None,
+             stream=None, gate_scale=None):
+    """Layer backward with bfloat16 h_history, h_s2, d_h_enriched in and bfloat16
+    d_h_history, d_h_s2 out; fp32 weights, weight gradients and sums. Returns
+    the dict of ``bwd``."""
+    import torch
+    B, K, SH2, D = dims_of(h_history, W_A)
+    if outs is None:
+        f = dict(device=h_history.device, dtype=torch.float32)
+        b = dict(device=h_history.device, dtype=torch.bfloat16)
+        outs = {"d_h_history": torch.empty((B, K, SH2), **b), "d_h_s2": torch.empty((B, SH2), **b),
+                "dW_A": torch.empty((SH2, D), **f), "dW_B": torch.empty((SH2, D), **f),
+                "dW_C": torch.empty((SH2, D), **f), "dW_O": torch.empty((D, SH2), **f)}
+    if workspace is None:
+        workspace = alloc_workspace(B, K, SH2, D, h_history.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = m2scan_bwd_bf16(
+        _check_bf16(h_history, "h_history", (B, K, SH2)), _check_bf16(h_s2, "h_s2", (B, SH2)),
+        _check(W_A, "W_A", (SH2, D)), _check(W_B, "W_B", (SH2, D)),
+        _check(W_C, "W_C", (SH2, D)), _check(W_O, "W_O", (D, SH2)), tw, _gate_ptr(gate_scale),
+        _check_bf16(d_h_enriched, "d_h_enriched", (B, SH2)), B, K, SH2, D,
+        _check_bf16(outs["d_h_history"], "d_h_history", (B, K, SH2)),
+        _check_bf16(outs["d_h_s2"], "d_h_s2", (B, SH2)), _check(outs["dW_A"], "dW_A", (SH2, D)),
+        _check(outs["dW_B"], "dW_B", (SH2, D)), _check(outs["dW_C"], "dW_C", (SH2, D)),
+        _check(outs["dW_O"], "dW_O", (D, SH2)), workspace.data_ptr(), ws_bytes, _stream(stream))
+    if st != M2SCAN_OK:
+        raise M2ScanError(st, "m2scan_bwd_bf16")
+    return outs

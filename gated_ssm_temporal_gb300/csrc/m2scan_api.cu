@@ -565,6 +565,64 @@ m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const flo
   return M2SCAN_OK;
 }
 
+m2scan_status m2scan_bwd_bf16(const void* h_history, const void* h_s2, const float* W_A,
+                              const float* W_B, const float* W_C, const float* W_O, float tw,
+                              const float* gate_scale, const void* d_h_enriched, int64_t B,
+                              int32_t K, int32_t SH2, int32_t D, void* d_h_history, void* d_h_s2,
+                              float* dW_A, float* dW_B, float* dW_C, float* dW_O, void* workspace,
+                              size_t workspace_bytes, m2scan_stream_t stream) {
+  t_last_launches = 0;
+  m2scan_status st = check_shape(B, K, SH2, D);
+  if (st != M2SCAN_OK) return st;
+  if (!W_A || !W_B || !W_C || !W_O || !dW_A || !dW_B || !dW_C || !dW_O) return M2SCAN_ERR_NULL;
+  if (B > 0 && (!h_history || !h_s2 || !d_h_enriched || !d_h_history || !d_h_s2))
+    return M2SCAN_ERR_NULL;
+  const void* ptrs[] = {h_history, h_s2, W_A, W_B, W_C, W_O, d_h_enriched, d_h_history,
+                        d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return M2SCAN_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(gate_scale) & 3u) != 0) return M2SCAN_ERR_ALIGN;
+  const size_t need = m2scan_bwd_workspace_bytes(B, K, SH2, D);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return M2SCAN_ERR_WORKSPACE;
+  const uint64_t nw = static_cast<uint64_t>(SH2) * D * 4;
+  const uint64_t nb = static_cast<uint64_t>(B) * SH2 * 2;  // bf16 rows
+  const Span outs[] = {span(d_h_history, nb * K), span(d_h_s2, nb), span(dW_A, nw),
+                       span(dW_B, nw), span(dW_C, nw), span(dW_O, nw), span(workspace, need)};
+  const Span ins[] = {span(h_history, nb * K), span(h_s2, nb), span(W_A, nw), span(W_B, nw),
+                      span(W_C, nw), span(W_O, nw), span(d_h_enriched, nb),
+                      span(gate_scale, gate_scale ? 4 : 0)};
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+    for (const Span& s : ins)
+      if (overlaps(outs[i], s)) return M2SCAN_ERR_ALIAS;
+    for (size_t k = i + 1; k < sizeof(outs) / sizeof(outs[0]); ++k)
+      if (overlaps(outs[i], outs[k])) return M2SCAN_ERR_ALIAS;
+  }
+  if (B == 0) {
+    float* dws[] = {dW_A, dW_B, dW_C, dW_O};
+    for (float* p : dws) {
+      cudaError_t e = cudaMemsetAsync(p, 0, nw, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return M2SCAN_OK;
+  }
+  int dev = 0;
+  if ((st = prepare_device(&dev)) != M2SCAN_OK) return st;
+  const size_t smem = generic_smem_bytes(true, K, SH2, D);
+  if (smem > static_cast<size_t>(g_max_smem[dev])) return M2SCAN_ERR_UNSUPPORTED;
+  const int grid = slots_for(B);
+  float* ws = static_cast<float*>(workspace);
+  GenericArgs ga{static_cast<const float*>(h_history), static_cast<const float*>(h_s2),
+                 static_cast<const float*>(d_h_enriched), W_A, W_B, W_C, W_O,
+                 static_cast<float*>(d_h_history), static_cast<float*>(d_h_s2), ws,
+                 B, K, SH2, D, tw, gate_scale};
+  cudaError_t e = launch_generic(true, ga, grid, smem, stream, true);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_reduce(ws, grid, SH2 * D, dW_A, dW_B, dW_C, dW_O, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = 2;
+  return M2SCAN_OK;
+}
+
 m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float* W_A,
                          const float* W_B, const float* W_C, const float* W_O, float tw,
                          const float* d_h_enriched, int64_t B, int32_t K, int32_t SH2,

@@ -6,14 +6,32 @@
 // owns the samples [c*B/P, (c+1)*B/P) and the weight-gradient slot c. Every
 // slot entry is owned by one fixed thread (entry e by thread e % 256), so the
 // partial sums are formed in a fixed order without atomics.
+//
+// T is the type of the activations (h_history, h_s2, dY in; the layer's
+// output or the input gradients out): float, or bfloat16 for the pages'
+// "bf16 inputs/outputs with fp32 accumulation" variant. Weights, weight
+// gradients and every product and sum are fp32 either way; a bf16 output is
+// the fp32 result rounded to nearest even.
+#include <cuda_bf16.h>
+
 #include "m2scan_device.cuh"
 #include "m2scan_internal.h"
 
 namespace m2scan {
 namespace {
 
-template <bool BWD>
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ void store_as(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_as(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+template <bool BWD, typename T>
 __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) {
+  const T* h_history = reinterpret_cast<const T*>(a.h_history);
+  const T* h_s2 = reinterpret_cast<const T*>(a.h_s2);
+  const T* g_in = reinterpret_cast<const T*>(a.g);
+  T* out0 = reinterpret_cast<T*>(a.out0);
+  T* out1 = reinterpret_cast<T*>(a.out1);
   extern __shared__ float4 smem_f4[];
   float* sm = reinterpret_cast<float*>(smem_f4);
   const int K = a.K, SH2 = a.SH2, D = a.D, TD = 2 * D;
@@ -33,10 +51,10 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
     for (int e = tid; e < 4 * n; e += kThreads) slot[e] = 0.f;
 
   for (long long b = b0; b < b1; ++b) {
-    const float* h = a.h_history + b * K * SH2;
+    const T* h = h_history + b * K * SH2;
     for (int j = tid; j < SH2; j += kThreads) {
-      sHs[j] = a.h_s2[b * SH2 + j];
-      if (BWD) sG[j] = a.g[b * SH2 + j];
+      sHs[j] = to_f32(h_s2[b * SH2 + j]);
+      if (BWD) sG[j] = to_f32(g_in[b * SH2 + j]);
     }
     __syncthreads();
     // projections A|B (one output per thread and step), C and d_ctx
@@ -44,9 +62,9 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
       const int t = e / TD, k = e - (e / TD) * TD;
       const float* W = k < D ? a.W_A : a.W_B;
       const int col = k < D ? k : k - D;
-      const float* hr = h + static_cast<size_t>(t) * SH2;
+      const T* hr = h + static_cast<size_t>(t) * SH2;
       float s = 0.f;
-      for (int j = 0; j < SH2; ++j) s = fmaf(hr[j], W[j * D + col], s);
+      for (int j = 0; j < SH2; ++j) s = fmaf(to_f32(hr[j]), W[j * D + col], s);
       sAB[e] = s;
     }
     for (int d = tid; d < D; d += kThreads) {
@@ -91,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
       for (int j = tid; j < SH2; j += kThreads) {
         float o = 0.f;
         for (int d = 0; d < D; ++d) o = fmaf(sCtx[d], a.W_O[static_cast<size_t>(d) * SH2 + j], o);
-        a.out0[b * SH2 + j] = fmaf(a.tw, o, sHs[j]);
+        store_as(out0 + b * SH2 + j, fmaf(a.tw, o, sHs[j]));
       }
     } else {
       for (int e = tid; e < K * SH2; e += kThreads) {
@@ -102,18 +120,18 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
           s = fmaf(pr[d], a.W_A[j * D + d], s);
           s = fmaf(pr[D + d], a.W_B[j * D + d], s);
         }
-        a.out0[(b * K + t) * SH2 + j] = s;
+        store_as(out0 + (b * K + t) * SH2 + j, s);
       }
       for (int j = tid; j < SH2; j += kThreads) {
         float s = sG[j];
         for (int d = 0; d < D; ++d) s = fmaf(sDC[d], a.W_C[j * D + d], s);
-        a.out1[b * SH2 + j] = s;
+        store_as(out1 + b * SH2 + j, s);
       }
       for (int e = tid; e < n; e += kThreads) {
         const int j = e / D, d = e - (e / D) * D;
         float sa = 0.f, sb = 0.f;
         for (int t = 0; t < K; ++t) {
-          const float hv = h[static_cast<size_t>(t) * SH2 + j];
+          const float hv = to_f32(h[static_cast<size_t>(t) * SH2 + j]);
           sa = fmaf(hv, sAB[t * TD + d], sa);
           sb = fmaf(hv, sAB[t * TD + D + d], sb);
         }
@@ -178,11 +196,18 @@ size_t generic_smem_bytes(bool bwd, int K, int SH2, int D) {
 }
 
 cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem,
-                           cudaStream_t stream) {
-  if (bwd)
-    generic_kernel<true><<<grid, kThreads, smem, stream>>>(a);
-  else
-    generic_kernel<false><<<grid, kThreads, smem, stream>>>(a);
+                           cudaStream_t stream, bool bf16) {
+  if (bf16) {
+    if (bwd)
+      generic_kernel<true, __nv_bfloat16><<<grid, kThreads, smem, stream>>>(a);
+    else
+      generic_kernel<false, __nv_bfloat16><<<grid, kThreads, smem, stream>>>(a);
+  } else {
+    if (bwd)
+      generic_kernel<true, float><<<grid, kThreads, smem, stream>>>(a);
+    else
+      generic_kernel<false, float><<<grid, kThreads, smem, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -195,12 +220,16 @@ cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float*
 }
 
 cudaError_t prepare_generic_kernels(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(generic_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(generic_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             max_smem);
-  return e;
+  const void* kernels[] = {reinterpret_cast<const void*>(generic_kernel<false, float>),
+                           reinterpret_cast<const void*>(generic_kernel<true, float>),
+                           reinterpret_cast<const void*>(generic_kernel<false, __nv_bfloat16>),
+                           reinterpret_cast<const void*>(generic_kernel<true, __nv_bfloat16>)};
+  for (const void* k : kernels) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace m2scan

@@ -83,15 +83,16 @@ def make_inputs(w: Workload) -> dict:
                 d_h_enriched=d_h_enriched, tw=float(w.tw))
 
 
-def algorithmic_bytes(B: int, K: int, SH2: int) -> dict:
-    """HBM bytes the layer must move per call (fp32, weights excluded).
+def algorithmic_bytes(B: int, K: int, SH2: int, elem: int = 4) -> dict:
+    """HBM bytes the layer must move per call (weights excluded), with
+    activations of ``elem`` bytes (4: fp32, 2: bf16).
 
-    forward reads h_history and h_s2 and writes h_enriched: 4*SH2*(K+2) per
+    forward reads h_history and h_s2 and writes h_enriched: elem*SH2*(K+2) per
     sample; backward reads h_history, h_s2 and d_h_enriched and writes
-    d_h_history and d_h_s2: 4*SH2*(2K+3) per sample.
+    d_h_history and d_h_s2: elem*SH2*(2K+3) per sample.
     """
-    fwd = 4 * SH2 * (K + 2) * B
-    bwd = 4 * SH2 * (2 * K + 3) * B
+    fwd = elem * SH2 * (K + 2) * B
+    bwd = elem * SH2 * (2 * K + 3) * B
     return dict(fwd=fwd, bwd=bwd, total=fwd + bwd)
 
 

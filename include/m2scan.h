@@ -153,6 +153,30 @@ m2scan_status m2scan_fwd_bf16(const void* h_history, const void* h_s2, const flo
                               int32_t D, void* h_enriched, m2scan_stream_t stream);
 
 /*
+ * Backward pass with bf16 activations, the counterpart of m2scan_fwd_bf16:
+ * h_history [B,K,SH2], h_s2 [B,SH2] and d_h_enriched [B,SH2] are bfloat16
+ * inputs, d_h_history [B,K,SH2] and d_h_s2 [B,SH2] bfloat16 outputs (the fp32
+ * results rounded to nearest even); weights and the weight gradients dW_A,
+ * dW_B, dW_C, dW_O are fp32 as for m2scan_bwd, and every product and sum is
+ * fp32 (the bf16 inputs are exact in fp32). gate_scale, workspace (at least
+ * m2scan_bwd_workspace_bytes(B, K, SH2, D)), the ownership, alignment and
+ * aliasing rules and the status codes are those of m2scan_bwd_ex, with the
+ * activation spans counted in 2-byte elements. Any shape m2scan_bwd accepts
+ * whose per-sample tile (4 * (2 * K * D + 2 * SH2 + 4 * D) bytes) fits the
+ * device's shared memory; larger ones return M2SCAN_ERR_UNSUPPORTED.
+ * It runs the per-sample generic kernel (no tensor-core kernel of the
+ * backward reads bf16 yet), then the fixed-order slot sum: two launches (none
+ * when B == 0, where the weight gradients are zeroed). Weight gradients are
+ * bit-identical run to run.
+ */
+m2scan_status m2scan_bwd_bf16(const void* h_history, const void* h_s2, const float* W_A,
+                              const float* W_B, const float* W_C, const float* W_O, float tw,
+                              const float* gate_scale, const void* d_h_enriched, int64_t B,
+                              int32_t K, int32_t SH2, int32_t D, void* d_h_history, void* d_h_s2,
+                              float* dW_A, float* dW_B, float* dW_C, float* dW_O, void* workspace,
+                              size_t workspace_bytes, m2scan_stream_t stream);
+
+/*
  * The layer with the pages' own output step ("Custom Kernel Optimization
  * Implementation Plan", Task 1 Step 3) in place of tw * (ctx . W_O): one
  * scalar context per sample blended into every feature with a per-feature

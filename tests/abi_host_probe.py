@@ -125,5 +125,26 @@ res["bf16_misaligned"] = g.m2scan_fwd_bf16(W[0] + 2, W[1], W[2], W[3], W[4], W[5
                                            256, 16, W[6], 0)
 res["bf16_alias"] = g.m2scan_fwd_bf16(W[0], W[1], W[2], W[3], W[4], W[5], 0.1, 0, 8, 8, 256, 16,
                                       W[0] + 1024, 0)
+def bwd_bf16(**kw):
+    ws = g.m2scan_bwd_workspace_bytes(B, K, SH2, D)
+    args = dict(h_history=W[0], h_s2=W[1], W_A=W[2], W_B=W[3], W_C=W[4], W_O=W[5], tw=0.5,
+                gate_scale=0, d_h_enriched=W[7], B=B, K=K, SH2=SH2, D=D, d_h_history=W[8],
+                d_h_s2=W[9], dW_A=W[10], dW_B=W[11], dW_C=W[12], dW_O=W[13], workspace=W[14],
+                workspace_bytes=ws, stream=0)
+    args.update(kw)
+    return g.m2scan_bwd_bf16(**args)
+
+
+res["bf16b_null_ws"] = bwd_bf16(workspace=0)
+res["bf16b_short_ws"] = bwd_bf16(workspace_bytes=g.m2scan_bwd_workspace_bytes(B, K, SH2, D) - 16)
+res["bf16b_null_dWC"] = bwd_bf16(dW_C=0)
+res["bf16b_null_g"] = bwd_bf16(d_h_enriched=0)
+res["bf16b_shape"] = bwd_bf16(SH2=6)
+res["bf16b_misaligned_h"] = bwd_bf16(h_history=W[0] + 2)
+res["bf16b_misaligned_gs"] = bwd_bf16(gate_scale=W[18] + 2)
+res["bf16b_alias_dhs2_hs2"] = bwd_bf16(d_h_s2=W[1] + 16)
+res["bf16b_alias_ws_dWA"] = bwd_bf16(workspace=W[10])
+res["bf16b_alias_gs_dh"] = bwd_bf16(gate_scale=W[8] + 4)
+
 res["status_str_ok"] = g.m2scan_status_str(0)
 print(json.dumps(res))

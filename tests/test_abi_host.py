@@ -62,6 +62,10 @@ NULL, SHAPE, ALIGN, ALIAS, WORKSPACE = 1, 2, 3, 4, 5
     ("bl_bwd_short_ws", WORKSPACE), ("bl_bwd_alias_dw_ws", ALIAS),
     ("bf16_B0_ok", 0), ("bf16_sh2_96", 6), ("bf16_d8", 6), ("bf16_misaligned", ALIGN),
     ("bf16_alias", ALIAS),
+    ("bf16b_null_ws", WORKSPACE), ("bf16b_short_ws", WORKSPACE), ("bf16b_null_dWC", NULL),
+    ("bf16b_null_g", NULL), ("bf16b_shape", SHAPE), ("bf16b_misaligned_h", ALIGN),
+    ("bf16b_misaligned_gs", ALIGN), ("bf16b_alias_dhs2_hs2", ALIAS), ("bf16b_alias_ws_dWA", ALIAS),
+    ("bf16b_alias_gs_dh", ALIAS),
 ])
 def test_host_validation(probe, key, expect):
     assert probe[key] == expect, (key, probe[key])
