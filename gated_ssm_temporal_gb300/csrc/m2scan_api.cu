@@ -297,7 +297,7 @@ m2scan_status m2scan_fwd_ex(const float* h_history, const float* h_s2, const flo
   } else {
     GenericArgs ga{h_history, h_s2, nullptr, W_A, W_B, W_C, W_O, h_enriched, nullptr, nullptr,
                    B, K, SH2, D, tw, gate_scale};
-    e = launch_generic(false, ga, grid, generic_smem_bytes(false, K, SH2, D), stream);
+    e = launch_generic(false, ga, grid, g_max_smem[dev], stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_launches = 1;
@@ -556,7 +556,7 @@ m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const flo
   } else {
     GenericArgs ga{h_history, h_s2, d_h_enriched, W_A, W_B, W_C, W_O, d_h_history, d_h_s2, ws,
                    B, K, SH2, D, tw, gate_scale};
-    e = launch_generic(true, ga, grid, generic_smem_bytes(true, K, SH2, D), stream);
+    e = launch_generic(true, ga, grid, g_max_smem[dev], stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   e = launch_reduce(ws, grid, SH2 * D, dW_A, dW_B, dW_C, dW_O, stream);
@@ -615,7 +615,7 @@ m2scan_status m2scan_bwd_bf16(const void* h_history, const void* h_s2, const flo
                  static_cast<const float*>(d_h_enriched), W_A, W_B, W_C, W_O,
                  static_cast<float*>(d_h_history), static_cast<float*>(d_h_s2), ws,
                  B, K, SH2, D, tw, gate_scale};
-  cudaError_t e = launch_generic(true, ga, grid, smem, stream, true);
+  cudaError_t e = launch_generic(true, ga, grid, g_max_smem[dev], stream, true);
   if (e != cudaSuccess) return cuda_fail(e);
   e = launch_reduce(ws, grid, SH2 * D, dW_A, dW_B, dW_C, dW_O, stream);
   if (e != cudaSuccess) return cuda_fail(e);

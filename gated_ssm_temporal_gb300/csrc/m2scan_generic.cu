@@ -7,6 +7,12 @@
 // slot entry is owned by one fixed thread (entry e by thread e % 256), so the
 // partial sums are formed in a fixed order without atomics.
 //
+// Staged form (GenericArgs::staged, chosen by the launcher when it fits the
+// device's shared memory): the four weight matrices, the sample's h_history
+// rows (as fp32) and the CTA's slot live in shared memory, and the slot is
+// written to global memory once, after the last sample. Every sum is formed
+// in the same order as in the unstaged form, so both give identical bits.
+//
 // T is the type of the activations (h_history, h_s2, dY in; the layer's
 // output or the input gradients out): float, or bfloat16 for the pages'
 // "bf16 inputs/outputs with fp32 accumulation" variant. Weights, weight
@@ -46,9 +52,37 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
   const int P = gridDim.x, cta = blockIdx.x;
   const long long b0 = a.B * cta / P, b1 = a.B * (cta + 1) / P;
   const int n = SH2 * D;
-  float* slot = BWD ? a.ws + static_cast<size_t>(cta) * 4 * n : nullptr;
+  const bool staged = a.staged != 0;
+  // staged only: h rows [K][SH2]; W_A, W_B, W_C [SH2][D] in rows of ldw = D + 1
+  // and W_O [D][SH2] in rows of ldo = SH2 + 1 (the padding keeps the loops
+  // that walk j across a warp free of bank conflicts); slot [4][n]
+  const int ldw = staged ? D + 1 : D, ldo = staged ? SH2 + 1 : SH2;
+  float* sH = sDC + D;
+  float* sWA = sH + static_cast<size_t>(K) * SH2;
+  const size_t nw = static_cast<size_t>(SH2) * (D + 1);  // D * (SH2 + 1) is the same less SH2 - D
+  float* sWB = sWA + nw;
+  float* sWC = sWB + nw;
+  float* sWO = sWC + nw;
+  float* sSlot = sWO + static_cast<size_t>(D) * (SH2 + 1);
+  const float* W_A = staged ? sWA : a.W_A;
+  const float* W_B = staged ? sWB : a.W_B;
+  const float* W_C = staged ? sWC : a.W_C;
+  const float* W_O = staged ? sWO : a.W_O;
+  float* gslot = BWD ? a.ws + static_cast<size_t>(cta) * 4 * n : nullptr;
+  float* slot = (BWD && staged) ? sSlot : gslot;
+  if (staged) {
+    for (int e = tid; e < n; e += kThreads) {
+      const int j = e / D, d = e - (e / D) * D;
+      sWA[j * ldw + d] = a.W_A[e];
+      sWB[j * ldw + d] = a.W_B[e];
+      sWC[j * ldw + d] = a.W_C[e];
+      const int dd = e / SH2, jj = e - (e / SH2) * SH2;
+      sWO[dd * ldo + jj] = a.W_O[e];
+    }
+  }
   if (BWD)
     for (int e = tid; e < 4 * n; e += kThreads) slot[e] = 0.f;
+  __syncthreads();
 
   for (long long b = b0; b < b1; ++b) {
     const T* h = h_history + b * K * SH2;
@@ -56,24 +90,31 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
       sHs[j] = to_f32(h_s2[b * SH2 + j]);
       if (BWD) sG[j] = to_f32(g_in[b * SH2 + j]);
     }
+    if (staged)
+      for (int e = tid; e < K * SH2; e += kThreads) sH[e] = to_f32(h[e]);
     __syncthreads();
     // projections A|B (one output per thread and step), C and d_ctx
     for (int e = tid; e < K * TD; e += kThreads) {
       const int t = e / TD, k = e - (e / TD) * TD;
-      const float* W = k < D ? a.W_A : a.W_B;
+      const float* W = k < D ? W_A : W_B;
       const int col = k < D ? k : k - D;
-      const T* hr = h + static_cast<size_t>(t) * SH2;
       float s = 0.f;
-      for (int j = 0; j < SH2; ++j) s = fmaf(to_f32(hr[j]), W[j * D + col], s);
+      if (staged) {
+        const float* hr = sH + static_cast<size_t>(t) * SH2;
+        for (int j = 0; j < SH2; ++j) s = fmaf(hr[j], W[j * ldw + col], s);
+      } else {
+        const T* hr = h + static_cast<size_t>(t) * SH2;
+        for (int j = 0; j < SH2; ++j) s = fmaf(to_f32(hr[j]), W[j * ldw + col], s);
+      }
       sAB[e] = s;
     }
     for (int d = tid; d < D; d += kThreads) {
       float c = 0.f;
-      for (int j = 0; j < SH2; ++j) c = fmaf(sHs[j], a.W_C[j * D + d], c);
+      for (int j = 0; j < SH2; ++j) c = fmaf(sHs[j], W_C[j * ldw + d], c);
       sC[d] = c;
       if (BWD) {
         float o = 0.f;
-        for (int j = 0; j < SH2; ++j) o = fmaf(sG[j], a.W_O[static_cast<size_t>(d) * SH2 + j], o);
+        for (int j = 0; j < SH2; ++j) o = fmaf(sG[j], W_O[static_cast<size_t>(d) * ldo + j], o);
         sDctx[d] = a.tw * o;
       }
     }
@@ -108,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
     if (!BWD) {
       for (int j = tid; j < SH2; j += kThreads) {
         float o = 0.f;
-        for (int d = 0; d < D; ++d) o = fmaf(sCtx[d], a.W_O[static_cast<size_t>(d) * SH2 + j], o);
+        for (int d = 0; d < D; ++d) o = fmaf(sCtx[d], W_O[static_cast<size_t>(d) * ldo + j], o);
         store_as(out0 + b * SH2 + j, fmaf(a.tw, o, sHs[j]));
       }
     } else {
@@ -117,21 +158,22 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
         const float* pr = sAB + t * TD;
         float s = 0.f;
         for (int d = 0; d < D; ++d) {
-          s = fmaf(pr[d], a.W_A[j * D + d], s);
-          s = fmaf(pr[D + d], a.W_B[j * D + d], s);
+          s = fmaf(pr[d], W_A[j * ldw + d], s);
+          s = fmaf(pr[D + d], W_B[j * ldw + d], s);
         }
         store_as(out0 + (b * K + t) * SH2 + j, s);
       }
       for (int j = tid; j < SH2; j += kThreads) {
         float s = sG[j];
-        for (int d = 0; d < D; ++d) s = fmaf(sDC[d], a.W_C[j * D + d], s);
+        for (int d = 0; d < D; ++d) s = fmaf(sDC[d], W_C[j * ldw + d], s);
         store_as(out1 + b * SH2 + j, s);
       }
       for (int e = tid; e < n; e += kThreads) {
         const int j = e / D, d = e - (e / D) * D;
         float sa = 0.f, sb = 0.f;
         for (int t = 0; t < K; ++t) {
-          const float hv = to_f32(h[static_cast<size_t>(t) * SH2 + j]);
+          const float hv = staged ? sH[static_cast<size_t>(t) * SH2 + j]
+                                  : to_f32(h[static_cast<size_t>(t) * SH2 + j]);
           sa = fmaf(hv, sAB[t * TD + d], sa);
           sb = fmaf(hv, sAB[t * TD + D + d], sb);
         }
@@ -146,6 +188,8 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
     }
     __syncthreads();
   }
+  if (BWD && staged)
+    for (int e = tid; e < 4 * n; e += kThreads) gslot[e] = sSlot[e];
 }
 
 // dW[e] = sum over slots p = 0..P-1 of ws[p][e], added in a fixed order:
@@ -195,8 +239,18 @@ size_t generic_smem_bytes(bool bwd, int K, int SH2, int D) {
   return sizeof(float) * (static_cast<size_t>(K) * 2 * D + 2 * static_cast<size_t>(SH2) + 4 * D);
 }
 
-cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem,
-                           cudaStream_t stream, bool bf16) {
+size_t generic_staged_smem_bytes(bool bwd, int K, int SH2, int D) {
+  const size_t sh = static_cast<size_t>(SH2), d = static_cast<size_t>(D);
+  return generic_smem_bytes(bwd, K, SH2, D) +
+         sizeof(float) * (static_cast<size_t>(K) * sh + 3 * sh * (d + 1) + d * (sh + 1) +
+                          (bwd ? 4 * sh * d : 0));
+}
+
+cudaError_t launch_generic(bool bwd, GenericArgs a, int grid, int max_smem, cudaStream_t stream,
+                           bool bf16) {
+  const size_t staged = generic_staged_smem_bytes(bwd, a.K, a.SH2, a.D);
+  a.staged = staged <= static_cast<size_t>(max_smem) ? 1 : 0;
+  const size_t smem = a.staged ? staged : generic_smem_bytes(bwd, a.K, a.SH2, a.D);
   if (bf16) {
     if (bwd)
       generic_kernel<true, __nv_bfloat16><<<grid, kThreads, smem, stream>>>(a);

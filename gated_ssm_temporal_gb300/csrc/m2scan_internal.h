@@ -79,6 +79,7 @@ struct GenericArgs {
   int D;
   float tw;
   const float* gate_scale;  // one float multiplying every gate, or null (1)
+  int staged = 0;           // set by launch_generic: weights, h rows and slot in shared memory
 };
 
 // Fast path shape limits (see m2scan.h).
@@ -119,9 +120,11 @@ cudaError_t prepare_fwd_bf16_kernels(int max_smem);
 // Warp-specialised tensor-core backward (D = 16).
 bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_bwd_tc(const FastArgs& a, int grid, cudaStream_t stream);
-// bf16: the activations (h_history, h_s2, g, out0, out1) are bfloat16.
-cudaError_t launch_generic(bool bwd, const GenericArgs& a, int grid, size_t smem,
-                           cudaStream_t stream, bool bf16 = false);
+// bf16: the activations (h_history, h_s2, g, out0, out1) are bfloat16. The
+// staged form is used when generic_staged_smem_bytes fits max_smem; the plain
+// form needs generic_smem_bytes <= max_smem (the caller checks that).
+cudaError_t launch_generic(bool bwd, GenericArgs a, int grid, int max_smem, cudaStream_t stream,
+                           bool bf16 = false);
 cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float* dW_B,
                           float* dW_C, float* dW_O, cudaStream_t stream);
 cudaError_t prepare_kernels(int max_smem_optin);
