@@ -13,7 +13,7 @@ order, the commits of one issuing thread in issue order. The run fails on
   buffer or accumulator set written while another role reads or writes it.
 
 The models follow the kernels' source (``fwd_tc16_kernel``,
-``bwd_tc_kernel``, ``fwd_bf16_kernel``): the same item order, barrier
+``bwd_tc_kernel``, ``fwd_bf16_kernel``, ``fwd_tc_kernel``): the same item order, barrier
 counts, ring sizes and wait parities. ``mutation`` plants a protocol mistake
 (a dropped wait) so that the tests can check the checker.
 """
@@ -85,9 +85,10 @@ def schedule(actors, bars, events, seed, limit=10 ** 6):
     assert not any(events.values()), "completions left over"
 
 
-def tiles(B, P, cta, K):
+def tiles(B, P, cta, K, S_max=None):
     """Sample counts of the CTA's tiles (the kernels' balanced split)."""
-    S_max = min(128 // K, 16)
+    if S_max is None:
+        S_max = min(128 // K, 16)
     cb0 = B * cta // P
     n_c = B * (cta + 1) // P - cb0
     T = (n_c + S_max - 1) // S_max
@@ -328,6 +329,95 @@ def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
     schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)
 
 
+def fwd_tc(B, P, cta, K, SH2, NST, seed, mutation=None, D=8):
+    """fwd_tc_kernel (D = 8 and 16 with the plain tf32 split): per tile the
+    NC chunks, then one item of h_s2 rows; the compute warps split each chunk
+    into one of two TMEM A buffers and free the stage themselves (the MMA
+    thread reads only TMEM and the weights); one accumulator set. The MMA
+    thread's wait on accempty is implied by the compute order (the next
+    tile's first A buffer is handed over after the read-back), so dropping
+    it is not a mistake this model can show."""
+    S_max = min(128 // K, 32, 256 // D)
+    S = tiles(B, P, cta, K, S_max)
+    T, NC = len(S), SH2 // 32
+    bars = {}
+    for s in range(NST):
+        bars["full%d" % s] = Bar("full", 1)
+        bars["empty%d" % s] = Bar("empty", 1)
+    for s in range(2):
+        bars["aready%d" % s] = Bar("aready", 1)
+        bars["afree%d" % s] = Bar("afree", 1)
+    bars["accfull"] = Bar("accfull", 1)
+    bars["accempty"] = Bar("accempty", 1)
+    events = {"tma": [], "mma": []}
+    st_read = [set() for _ in range(NST)]
+    a_read = [0, 0]
+    acc = {"w": 0, "r": False}
+    n_items = T * (NC + 1)
+
+    def producer():
+        for pn in range(n_items):
+            st, use = pn % NST, pn // NST
+            if use > 0:
+                yield W("empty%d" % st, use - 1)
+            assert not st_read[st], ("stage reloaded while read", st)
+            events["tma"].append(("full%d" % st, None))
+
+    def mma():
+        c = 0
+        for t in range(T):
+            if t > 0:
+                yield W("accempty", t - 1)
+            assert not acc["r"], "products into accumulators being read"
+            for q in range(NC):
+                yield W("aready%d" % (c & 1), c >> 1)
+                a_read[c & 1] += 1
+                acc["w"] += 1
+
+                def done(b=c & 1):
+                    a_read[b] -= 1
+                    acc["w"] -= 1
+                events["mma"].append(("afree%d" % (c & 1), done))
+                c += 1
+            events["mma"].append(("accfull", None))
+
+    def compute():
+        seq = c = 0
+        for t in range(T):
+            for q in range(NC):
+                st = seq % NST
+                yield W("full%d" % st, seq // NST)
+                if mutation == "early_empty":
+                    bars["empty%d" % st].arrive()
+                st_read[st].add(seq)
+                if c >= 2 and mutation != "no_afree_wait":
+                    yield W("afree%d" % (c & 1), (c - 2) >> 1)
+                assert a_read[c & 1] == 0, "A buffer written while read"
+                yield ("yield",)
+                st_read[st].discard(seq)
+                bars["aready%d" % (c & 1)].arrive()
+                if mutation != "early_empty":
+                    bars["empty%d" % st].arrive()
+                seq += 1
+                c += 1
+            if mutation != "no_accfull_wait":
+                yield W("accfull", t)
+            assert acc["w"] == 0, "accumulators read while written"
+            acc["r"] = True
+            yield ("yield",)
+            acc["r"] = False
+            bars["accempty"].arrive()
+            st = seq % NST
+            yield W("full%d" % st, seq // NST)
+            st_read[st].add(seq)
+            yield ("yield",)
+            st_read[st].discard(seq)
+            bars["empty%d" % st].arrive()
+            seq += 1
+
+    schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)
+
+
 # -------------------------------------------------------------- backward
 
 def bwd_tc(B, P, cta, K, SH2, NST, seed, mutation=None):
@@ -513,4 +603,4 @@ def bwd_tc(B, P, cta, K, SH2, NST, seed, mutation=None):
     schedule({"p": producer(), "m": main(), "r": corr(), "c": compute()}, bars, events, seed)
 
 
-MODELS = {"fwd_tc16": fwd_tc16, "fwd_bf16": fwd_bf16, "bwd_tc": bwd_tc}
+MODELS = {"fwd_tc16": fwd_tc16, "fwd_bf16": fwd_bf16, "bwd_tc": bwd_tc, "fwd_tc": fwd_tc}

@@ -13,7 +13,8 @@ P = 152
 # (B, K): the layer's workload, ragged splits, a CTA with one or no sample,
 # the narrowest and widest histories
 SHAPES = [(8192, 8), (65536, 8), (1000, 8), (300, 16), (152, 8), (20, 8), (700, 1), (400, 128), (333, 3)]
-WIDTHS = {"fwd_tc16": (256, 64, 32), "fwd_bf16": (256, 128, 64), "bwd_tc": (256, 64, 32)}
+WIDTHS = {"fwd_tc16": (256, 64, 32), "fwd_bf16": (256, 128, 64), "bwd_tc": (256, 64, 32),
+          "fwd_tc": (256, 64, 32)}
 
 
 @pytest.mark.parametrize("model", sorted(pm.MODELS))
@@ -54,6 +55,9 @@ MUTATIONS = [
     ("bwd_tc", "no_htfree_wait"),
     ("bwd_tc", "no_dhfree1_wait"),
     ("bwd_tc", "early_row_empty"),
+    ("fwd_tc", "no_afree_wait"),
+    ("fwd_tc", "no_accfull_wait"),
+    ("fwd_tc", "early_empty"),
 ]
 
 
