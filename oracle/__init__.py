@@ -52,9 +52,9 @@ def open_library(path: str):
     dp = ctypes.POINTER(ctypes.c_double)
     i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
     lib.m2o_scan_state.argtypes = [dp] * 5 + [i64, i32, i32, i32, dbl] + [dp] * 5
-    lib.m2o_forward.argtypes = [dp] * 6 + [dbl, i64, i32, i32, i32, dbl, i32, dp, i32]
+    lib.m2o_forward.argtypes = [dp] * 6 + [dbl, i64, i32, i32, i32, dbl, i32, dp, dp, i32]
     lib.m2o_backward.argtypes = ([dp] * 6 + [dbl, dp, i64, i32, i32, i32, dbl, i32]
-                                 + [dp] * 6 + [i32])
+                                 + [dp] * 9 + [i32])
     lib.m2o_bias_grad.argtypes = [dp, i64, i32, dp, i32, dp]
     for f in (lib.m2o_scan_state, lib.m2o_forward, lib.m2o_backward, lib.m2o_bias_grad):
         f.restype = ctypes.c_int
@@ -106,29 +106,36 @@ def scan_state(h_history, h_s2, W_A, W_B, W_C, lib=None, gate_scale=1.0):
 
 
 def forward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, n_threads=None, lib=None, gate_scale=1.0,
-            blend=False):
+            blend=False, abs_terms=False):
     """h_enriched [B,SH2] in float64; ``gate_scale`` multiplies every gate.
     ``blend``: the pages' output step, W_O is then the per-feature weight
-    vector w [SH2] (None: ones) and tw is ignored."""
+    vector w [SH2] (None: ones) and tw is ignored.
+    ``abs_terms``: return (h_enriched, the per-element sum of the absolute
+    values of the terms h_enriched adds up)."""
     h, hs, wa, wb, wc = map(_f64, (h_history, h_s2, W_A, W_B, W_C))
     B, K, SH2, D = _dims(h, wa)
     wo = _f64(np.ones(SH2) if W_O is None else W_O)
     out = np.empty((B, SH2))
+    aout = np.empty((B, SH2)) if abs_terms else None
     rc = _load(lib).m2o_forward(_ptr(h), _ptr(hs), _ptr(wa), _ptr(wb), _ptr(wc), _ptr(wo),
                              float(tw), B, K, SH2, D, float(gate_scale), 1 if blend else 0,
-                             _ptr(out),
+                             _ptr(out), _ptr(aout) if abs_terms else None,
                              n_threads or default_threads())
     if rc:
         raise RuntimeError("oracle forward failed (%d)" % rc)
-    return out
+    return (out, aout) if abs_terms else out
 
 
 def backward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, n_threads=None,
-             lib=None, gate_scale=1.0, blend=False):
+             lib=None, gate_scale=1.0, blend=False, abs_terms=False):
     """Returns dict of float64 arrays: d_h_history, d_h_s2, dW_A, dW_B, dW_C, dW_O.
     ``gate_scale`` multiplies every gate (a constant: it gets no gradient).
     ``blend``: the pages' output step (see ``forward``); dW_O is then the
-    gradient of the per-feature weights, [SH2]."""
+    gradient of the per-feature weights, [SH2].
+    ``abs_terms``: also return, under the keys ``dW_A_abs`` ... ``dW_O_abs``,
+    ``d_h_history_abs`` and ``d_h_s2_abs``, the per-element sums of the
+    absolute values of the terms each output adds up (the scale that bounds
+    the rounding error of an fp32 evaluation of those sums)."""
     h, hs, wa, wb, wc, g = map(_f64, (h_history, h_s2, W_A, W_B, W_C, d_h_enriched))
     B, K, SH2, D = _dims(h, wa)
     wo = _f64(np.ones(SH2) if W_O is None else W_O)
@@ -137,13 +144,22 @@ def backward(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, n_threads=No
         "dW_A": np.empty((SH2, D)), "dW_B": np.empty((SH2, D)),
         "dW_C": np.empty((SH2, D)), "dW_O": np.empty((SH2,) if blend else (D, SH2)),
     }
+    terms = np.zeros((4, SH2 * D)) if abs_terms else None
+    adh = np.empty((B, K, SH2)) if abs_terms else None
+    adhs = np.empty((B, SH2)) if abs_terms else None
     rc = _load(lib).m2o_backward(
         _ptr(h), _ptr(hs), _ptr(wa), _ptr(wb), _ptr(wc), _ptr(wo), float(tw), _ptr(g),
         B, K, SH2, D, float(gate_scale), 1 if blend else 0, _ptr(out["d_h_history"]), _ptr(out["d_h_s2"]), _ptr(out["dW_A"]),
         _ptr(out["dW_B"]), _ptr(out["dW_C"]), _ptr(out["dW_O"]),
-        n_threads or default_threads())
+        _ptr(terms) if abs_terms else None, _ptr(adh) if abs_terms else None,
+        _ptr(adhs) if abs_terms else None, n_threads or default_threads())
     if rc:
         raise RuntimeError("oracle backward failed (%d)" % rc)
+    if abs_terms:
+        for i, k in enumerate(("dW_A", "dW_B", "dW_C", "dW_O")):
+            out[k + "_abs"] = terms[i][:out[k].size].reshape(out[k].shape).copy()
+        out["d_h_history_abs"] = adh
+        out["d_h_s2_abs"] = adhs
     return out
 
 

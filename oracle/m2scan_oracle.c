@@ -50,6 +50,21 @@
  * then added in block order, so the result does not depend on the number of
  * threads that ran it.
  *
+ * Error scale of the weight gradients (test infrastructure, not part of the
+ * layer): each weight gradient is a sum of per-sample terms (h * dA, h * dBv,
+ * hs * dC, tw * ctx * g). When `abs_terms` is not NULL the backward also
+ * returns, per element, the sum of the absolute values of those same terms,
+ *   |dW_A|[j,s] = sum over b, t of |h[b,t,j] * dA[t,s]|   (likewise |dW_B|)
+ *   |dW_C|[j,s] = sum over b of |hs[b,j] * dC[s]|
+ *   |dW_O|[s,j] = sum over b of |tw * ctx[s] * g[j]|
+ * (blend form: sum over b of |g[j] * context / D|). The rounding error of any
+ * fp32 evaluation of a sum is bounded by a multiple of this quantity (the
+ * standard bound for floating-point summation), not by the sum itself.
+ * `abs_dh`, `abs_dhs2` (backward) and `abs_out` (forward) do the same for the
+ * per-sample outputs: sum over s of |dA*W_A| + |dBv*W_B|, |g| + sum over s of
+ * |dC*W_C| and |hs| + |tw| * sum over s of |ctx*W_O| (blend: |hs| +
+ * |w| * sum over s of |ctx| / D). NULL skips any of them.
+ *
  * Layouts (row-major, contiguous): h_history [B,K,SH2], h_s2 [B,SH2],
  * W_A, W_B, W_C [SH2,D], W_O [D,SH2], d_h_enriched and h_enriched [B,SH2].
  */
@@ -126,7 +141,7 @@ int m2o_scan_state(const double* h_history, const double* h_s2, const double* W_
 int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
                 const double* W_B, const double* W_C, const double* W_O, double tw,
                 int64_t B, int K, int SH2, int D, double gs, int blend, double* h_enriched,
-                int n_threads) {
+                double* abs_out, int n_threads) {
   if (B < 0 || K < 1 || SH2 < 1 || D < 1) return 1;
   if (n_threads < 1) n_threads = 1;
   int fail = 0;
@@ -148,16 +163,23 @@ int m2o_forward(const double* h_history, const double* h_s2, const double* W_A,
       if (blend) {
         double context = 0.0;
         for (int s = 0; s < D; s++) context += ctx[s];
+        double acontext = 0.0;
+        for (int s = 0; s < D; s++) acontext += fabs(ctx[s]);
         for (int j = 0; j < SH2; j++) {
           const double w = W_O ? W_O[j] : 1.0;
           h_enriched[b * SH2 + j] = hs[j] + w * context / D;
+          if (abs_out) abs_out[b * SH2 + j] = fabs(hs[j]) + fabs(w) * acontext / D;
         }
         continue;
       }
       for (int j = 0; j < SH2; j++) {
-        double o = 0.0;
-        for (int s = 0; s < D; s++) o += ctx[s] * W_O[(int64_t)s * SH2 + j];
+        double o = 0.0, ao = 0.0;
+        for (int s = 0; s < D; s++) {
+          o += ctx[s] * W_O[(int64_t)s * SH2 + j];
+          ao += fabs(ctx[s] * W_O[(int64_t)s * SH2 + j]);
+        }
         h_enriched[b * SH2 + j] = hs[j] + tw * o;
+        if (abs_out) abs_out[b * SH2 + j] = fabs(hs[j]) + fabs(tw) * ao;
       }
     }
     free(buf);
@@ -169,12 +191,14 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
                  const double* W_B, const double* W_C, const double* W_O, double tw,
                  const double* d_h_enriched, int64_t B, int K, int SH2, int D, double gs,
                  int blend, double* d_h_history, double* d_h_s2, double* dW_A, double* dW_B,
-                 double* dW_C, double* dW_O, int n_threads) {
+                 double* dW_C, double* dW_O, double* abs_terms, double* abs_dh,
+                 double* abs_dhs2, int n_threads) {
   if (B < 0 || K < 1 || SH2 < 1 || D < 1) return 1;
   if (n_threads < 1) n_threads = 1;
   const int64_t nw = (int64_t)SH2 * D; /* elements of each weight gradient */
-  /* per-block partial sums: [block][4][nw], order dW_A, dW_B, dW_C, dW_O */
-  double* part = (double*)calloc((size_t)M2O_BLOCKS * 4 * nw, sizeof(double));
+  /* per-block partial sums: [block][8][nw], order dW_A, dW_B, dW_C, dW_O, then
+   * the absolute-term sums of the same four */
+  double* part = (double*)calloc((size_t)M2O_BLOCKS * 8 * nw, sizeof(double));
   if (!part) return 2;
   int fail = 0;
 #pragma omp parallel num_threads(n_threads)
@@ -187,10 +211,14 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
 #pragma omp for schedule(dynamic, 1)
     for (int blk = 0; blk < M2O_BLOCKS; blk++) {
       if (!buf) continue;
-      double* pA = part + (int64_t)blk * 4 * nw;
+      double* pA = part + (int64_t)blk * 8 * nw;
       double* pB = pA + nw;
       double* pC = pB + nw;
       double* pO = pC + nw; /* stored [D,SH2] like W_O */
+      double* qA = pO + nw; /* absolute-term sums, same layouts */
+      double* qB = qA + nw;
+      double* qC = qB + nw;
+      double* qO = qC + nw;
       int64_t b0 = B * blk / M2O_BLOCKS, b1 = B * (blk + 1) / M2O_BLOCKS;
       double *A = buf, *Bv = A + K * D, *sig = Bv + K * D, *x = sig + K * D;
       double *dA = x + K * D, *dBv = dA + K * D;
@@ -209,6 +237,7 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
             const double w = W_O ? W_O[j] : 1.0;
             dcontext += g[j] * w / D;
             pO[j] += g[j] * context / D;
+            qO[j] += fabs(g[j] * context / D);
           }
           for (int s = 0; s < D; s++) {
             dctx[s] = dcontext;
@@ -219,7 +248,10 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
           double acc = 0.0;
           for (int j = 0; j < SH2; j++) acc += g[j] * W_O[(int64_t)s * SH2 + j];
           dctx[s] = tw * acc;
-          for (int j = 0; j < SH2; j++) pO[(int64_t)s * SH2 + j] += tw * ctx[s] * g[j];
+          for (int j = 0; j < SH2; j++) {
+            pO[(int64_t)s * SH2 + j] += tw * ctx[s] * g[j];
+            qO[(int64_t)s * SH2 + j] += fabs(tw * ctx[s] * g[j]);
+          }
           dC[s] = dctx[s] * x[(K - 1) * D + s];
         }
         /* reverse scan; the gate of step t is gs * sigmoid(A[t]) (same plan,
@@ -237,30 +269,43 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
         /* weight gradients */
         for (int j = 0; j < SH2; j++) {
           for (int s = 0; s < D; s++) {
-            double sa = 0.0, sb = 0.0;
+            double sa = 0.0, sb = 0.0, ua = 0.0, ub = 0.0;
             for (int t = 0; t < K; t++) {
               sa += h[(int64_t)t * SH2 + j] * dA[t * D + s];
               sb += h[(int64_t)t * SH2 + j] * dBv[t * D + s];
+              ua += fabs(h[(int64_t)t * SH2 + j] * dA[t * D + s]);
+              ub += fabs(h[(int64_t)t * SH2 + j] * dBv[t * D + s]);
             }
             pA[(int64_t)j * D + s] += sa;
             pB[(int64_t)j * D + s] += sb;
             pC[(int64_t)j * D + s] += hs[j] * dC[s];
+            qA[(int64_t)j * D + s] += ua;
+            qB[(int64_t)j * D + s] += ub;
+            qC[(int64_t)j * D + s] += fabs(hs[j] * dC[s]);
           }
         }
         /* input gradients */
         for (int t = 0; t < K; t++) {
           for (int j = 0; j < SH2; j++) {
-            double acc = 0.0;
-            for (int s = 0; s < D; s++)
+            double acc = 0.0, aacc = 0.0;
+            for (int s = 0; s < D; s++) {
               acc += dA[t * D + s] * W_A[(int64_t)j * D + s] +
                      dBv[t * D + s] * W_B[(int64_t)j * D + s];
+              aacc += fabs(dA[t * D + s] * W_A[(int64_t)j * D + s]) +
+                      fabs(dBv[t * D + s] * W_B[(int64_t)j * D + s]);
+            }
             d_h_history[(b * K + t) * SH2 + j] = acc;
+            if (abs_dh) abs_dh[(b * K + t) * SH2 + j] = aacc;
           }
         }
         for (int j = 0; j < SH2; j++) {
-          double acc = g[j];
-          for (int s = 0; s < D; s++) acc += dC[s] * W_C[(int64_t)j * D + s];
+          double acc = g[j], aacc = fabs(g[j]);
+          for (int s = 0; s < D; s++) {
+            acc += dC[s] * W_C[(int64_t)j * D + s];
+            aacc += fabs(dC[s] * W_C[(int64_t)j * D + s]);
+          }
           d_h_s2[b * SH2 + j] = acc;
+          if (abs_dhs2) abs_dhs2[b * SH2 + j] = aacc;
         }
       }
     }
@@ -269,17 +314,28 @@ int m2o_backward(const double* h_history, const double* h_s2, const double* W_A,
   /* combine the blocks in block order */
   for (int64_t e = 0; e < nw; e++) {
     double sa = 0.0, sb = 0.0, sc = 0.0, so = 0.0;
+    double ua = 0.0, ub = 0.0, uc = 0.0, uo = 0.0;
     for (int blk = 0; blk < M2O_BLOCKS; blk++) {
-      const double* p = part + (int64_t)blk * 4 * nw;
+      const double* p = part + (int64_t)blk * 8 * nw;
       sa += p[e];
       sb += p[nw + e];
       sc += p[2 * nw + e];
       so += p[3 * nw + e];
+      ua += p[4 * nw + e];
+      ub += p[5 * nw + e];
+      uc += p[6 * nw + e];
+      uo += p[7 * nw + e];
     }
     dW_A[e] = sa;
     dW_B[e] = sb;
     dW_C[e] = sc;
     if (!blend || e < SH2) dW_O[e] = so;
+    if (abs_terms) {
+      abs_terms[e] = ua;
+      abs_terms[nw + e] = ub;
+      abs_terms[2 * nw + e] = uc;
+      if (!blend || e < SH2) abs_terms[3 * nw + e] = uo;
+    }
   }
   free(part);
   return fail;

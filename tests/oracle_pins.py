@@ -19,6 +19,13 @@ raises AssertionError when the oracle disagrees with:
     into every feature with a weight w[j] and 1/D): central differences and
     torch autograd of all gradients including dw, the K=1 closed form, and
     w = 0 giving the identity on h_s2.
+  * for the per-element error scales (sums of the absolute values of the
+    terms each output adds up, which bound the rounding error of an fp32
+    evaluation): the same sums formed from torch float64 autograd's dA, dB,
+    dC, ctx, equality with the signed result when every term is
+    non-negative or there is a single term, additivity over samples,
+    invariance under a sign flip of dY and under a permutation of samples,
+    and the triangle inequality.
 ``tests/test_oracle_mutants.py`` plants mistakes in copies of the oracle and
 checks that these pins catch each one.
 """
@@ -362,7 +369,103 @@ def pin_blend(lib=None):
         close(gr[GRADS[p]], t[p].grad.numpy(), 1e-10, 1e-12, "blend autograd d%s" % p)
 
 
+ABS_KEYS = ("dW_A", "dW_B", "dW_C", "dW_O", "d_h_history", "d_h_s2")
+
+
+def bwd_abs(x, lib, **kw):
+    return bwd(x, lib, abs_terms=True, **kw)
+
+
+def pin_abs_terms_autograd(lib=None):
+    """Absolute-term sums against the same sums built from torch float64
+    autograd's intermediate gradients (dA, dB = dL/dB_t, dC = dL/dC) and
+    forward values (ctx)."""
+    import torch
+    for (B, K, SH2, D, seed) in [(4, 5, 7, 3, 20), (3, 1, 6, 2, 21)]:
+        x = rand_inputs(B, K, SH2, D, seed, wscale=3.0)
+        t = {k: torch.tensor(x[k], dtype=torch.float64, requires_grad=True) for k in PARAMS}
+        A = t["h_history"] @ t["W_A"]
+        Bv = t["h_history"] @ t["W_B"]
+        C = t["h_s2"] @ t["W_C"]
+        for v in (A, Bv, C):
+            v.retain_grad()
+        state = torch.zeros(B, D, dtype=torch.float64)
+        for k in range(K):
+            state = torch.sigmoid(A[:, k]) * state + Bv[:, k]
+        ctx = C * state
+        y = t["h_s2"] + x["tw"] * (ctx @ t["W_O"])
+        (y * torch.tensor(x["d_h_enriched"])).sum().backward()
+        h, hs, g = x["h_history"], x["h_s2"], x["d_h_enriched"]
+        dA, dB, dC = A.grad.numpy(), Bv.grad.numpy(), C.grad.numpy()
+        cx = ctx.detach().numpy()
+        exp = {
+            "dW_A": np.abs(h[:, :, :, None] * dA[:, :, None, :]).sum(axis=(0, 1)),
+            "dW_B": np.abs(h[:, :, :, None] * dB[:, :, None, :]).sum(axis=(0, 1)),
+            "dW_C": np.abs(hs[:, :, None] * dC[:, None, :]).sum(axis=0),
+            "dW_O": np.abs(x["tw"] * cx[:, :, None] * g[:, None, :]).sum(axis=0),
+            "d_h_history": (np.abs(dA[:, :, None, :] * x["W_A"][None, None]).sum(axis=3)
+                            + np.abs(dB[:, :, None, :] * x["W_B"][None, None]).sum(axis=3)),
+            "d_h_s2": np.abs(g) + np.abs(dC[:, None, :] * x["W_C"][None]).sum(axis=2),
+        }
+        r = bwd_abs(x, lib)
+        for k in ABS_KEYS:
+            close(r[k + "_abs"], exp[k], 1e-10, 1e-13, "autograd |terms| of %s" % k)
+        out, aout = fwd(x, lib, abs_terms=True)
+        close(aout, np.abs(hs) + abs(x["tw"]) * np.abs(cx[:, :, None] * x["W_O"][None]).sum(axis=1),
+              1e-10, 1e-13, "autograd |terms| of h_enriched")
+
+
+def pin_abs_terms_invariants(lib=None):
+    """Equalities and invariances every absolute-term sum must satisfy."""
+    # every term non-negative: inputs >= 0 and tw > 0 make every projection,
+    # state, gradient and product non-negative, so |sum| = sum of |terms|
+    x = rand_inputs(5, 4, 6, 3, 30)
+    for k in PARAMS + ["d_h_enriched"]:
+        x[k] = np.abs(x[k])
+    r = bwd_abs(x, lib)
+    for k in ABS_KEYS:
+        close(r[k + "_abs"], np.abs(r[k]), 1e-12, 0.0, "non-negative terms %s" % k)
+    out, aout = fwd(x, lib, abs_terms=True)
+    close(aout, np.abs(out), 1e-12, 0.0, "non-negative terms h_enriched")
+    # one sample, one step, one state, no residual: every sum has one term
+    x = rand_inputs(1, 1, 5, 1, 31)
+    r = bwd_abs(x, lib)
+    for k in ("dW_A", "dW_B", "dW_C", "dW_O", "d_h_history"):
+        close(r[k + "_abs"], np.abs(r[k]), 1e-14, 0.0, "single term %s" % k)
+    xz = dict(x)
+    xz["h_s2"] = np.zeros_like(x["h_s2"])
+    out, aout = fwd(xz, lib, abs_terms=True)
+    close(aout, np.abs(out), 1e-14, 0.0, "single term h_enriched")
+    # mixed signs: triangle inequality, additivity over samples, sign flip of
+    # dY, permutation of samples
+    x = rand_inputs(6, 5, 7, 3, 32, wscale=2.0)
+    r = bwd_abs(x, lib)
+    for k in ABS_KEYS:
+        assert np.all(np.abs(r[k]) <= r[k + "_abs"] * (1 + 1e-12) + 1e-300), "triangle %s" % k
+    part = []
+    for sl in (slice(0, 2), slice(2, 6)):
+        xs = {k: (v[sl] if k in ("h_history", "h_s2", "d_h_enriched") else v) for k, v in x.items()}
+        part.append(bwd_abs(xs, lib))
+    for k in ("dW_A", "dW_B", "dW_C", "dW_O"):
+        close(r[k + "_abs"], part[0][k + "_abs"] + part[1][k + "_abs"], 1e-12, 0.0,
+              "additivity over samples %s" % k)
+    for k in ("d_h_history", "d_h_s2"):
+        close(r[k + "_abs"], np.concatenate([part[0][k + "_abs"], part[1][k + "_abs"]]), 0.0, 0.0,
+              "per-sample %s" % k)
+    xf = dict(x)
+    xf["d_h_enriched"] = -x["d_h_enriched"]
+    rf = bwd_abs(xf, lib)
+    for k in ABS_KEYS:
+        close(rf[k + "_abs"], r[k + "_abs"], 1e-14, 0.0, "sign flip of dY %s" % k)
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    xp = {k: (v[perm] if k in ("h_history", "h_s2", "d_h_enriched") else v) for k, v in x.items()}
+    rp = bwd_abs(xp, lib)
+    for k in ("dW_A", "dW_B", "dW_C", "dW_O"):
+        close(rp[k + "_abs"], r[k + "_abs"], 1e-12, 0.0, "sample permutation %s" % k)
+
+
 ALL_PINS = [pin_finite_differences, pin_closed_form_scan, pin_reverse_closed_form, pin_k1,
             pin_k2, pin_saturated_gates, pin_tw_zero, pin_linearity, pin_torch_autograd,
             pin_golden_hand_example, pin_thread_count_invariance, pin_gate_scale_closed_form,
-            pin_gate_scale_gradients, pin_blend]
+            pin_gate_scale_gradients, pin_blend, pin_abs_terms_autograd,
+            pin_abs_terms_invariants]

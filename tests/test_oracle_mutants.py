@@ -51,11 +51,28 @@ MUTANTS = {
                        "pO[(int64_t)s * SH2 + j] += ctx[s] * g[j];"),
     "dhist_swapped_weights": ("acc += dA[t * D + s] * W_A[(int64_t)j * D + s] +",
                               "acc += dA[t * D + s] * W_B[(int64_t)j * D + s] +"),
-    "dhs2_no_residual": ("double acc = g[j];", "double acc = 0.0;"),
+    "dhs2_no_residual": ("double acc = g[j], aacc", "double acc = 0.0, aacc"),
     "dWC_uses_dctx": ("pC[(int64_t)j * D + s] += hs[j] * dC[s];",
                       "pC[(int64_t)j * D + s] += hs[j] * dctx[s];"),
     "combine_drops_last_block": ("for (int blk = 0; blk < M2O_BLOCKS; blk++) {\n      const",
                                  "for (int blk = 0; blk < M2O_BLOCKS - 1; blk++) {\n      const"),
+    # the per-element error scales (sums of |terms|)
+    "abs_of_sum_over_t": ("ua += fabs(h[(int64_t)t * SH2 + j] * dA[t * D + s]);",
+                          "ua = fabs(sa);"),
+    "abs_dWB_uses_dA": ("ub += fabs(h[(int64_t)t * SH2 + j] * dBv[t * D + s]);",
+                        "ub += fabs(h[(int64_t)t * SH2 + j] * dA[t * D + s]);"),
+    "abs_dWO_missing_tw": ("qO[(int64_t)s * SH2 + j] += fabs(tw * ctx[s] * g[j]);",
+                           "qO[(int64_t)s * SH2 + j] += fabs(ctx[s] * g[j]);"),
+    "abs_dWC_signed": ("qC[(int64_t)j * D + s] += fabs(hs[j] * dC[s]);",
+                       "qC[(int64_t)j * D + s] += hs[j] * dC[s];"),
+    "abs_dh_drops_B_term": ("fabs(dBv[t * D + s] * W_B[(int64_t)j * D + s]);",
+                            "0.0 * fabs(dBv[t * D + s] * W_B[(int64_t)j * D + s]);"),
+    "abs_dhs2_no_residual": ("double acc = g[j], aacc = fabs(g[j]);",
+                             "double acc = g[j], aacc = 0.0;"),
+    "abs_out_no_residual": ("abs_out[b * SH2 + j] = fabs(hs[j]) + fabs(tw) * ao;",
+                            "abs_out[b * SH2 + j] = fabs(tw) * ao;"),
+    "abs_combine_drops_last_block": ("ua += p[4 * nw + e];",
+                                     "ua += (blk < M2O_BLOCKS - 1) ? p[4 * nw + e] : 0.0;"),
 }
 
 
