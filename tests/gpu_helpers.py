@@ -5,6 +5,7 @@ import gated_ssm_temporal_gb300 as g
 from gated_ssm_temporal_gb300 import build as gbuild
 
 OUTPUTS = ("d_h_history", "d_h_s2", "dW_A", "dW_B", "dW_C", "dW_O")
+NAMES_ALL = ("h_enriched",) + OUTPUTS
 
 
 def ensure_built():
@@ -43,10 +44,26 @@ def run_all(x, force_generic=False):
     return out
 
 
-def oracle_all(x):
+def oracle_all(x, **kw):
+    """The oracle's outputs and, under ``<name>_abs``, the sums of the absolute
+    values of each output's terms (the error scale of the parity bound)."""
     import oracle
-    ref = {"h_enriched": oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"],
-                                        x["W_C"], x["W_O"], x["tw"])}
+    y, ya = oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"], x["W_O"],
+                           x["tw"], abs_terms=True, **kw)
+    ref = {"h_enriched": y, "h_enriched_abs": ya}
     ref.update(oracle.backward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"],
-                               x["W_O"], x["tw"], x["d_h_enriched"]))
+                               x["W_O"], x["tw"], x["d_h_enriched"], abs_terms=True, **kw))
     return ref
+
+
+def shape_of(x):
+    B, K, SH2 = x["h_history"].shape
+    return int(B), int(K), int(SH2), int(x["W_A"].shape[1])
+
+
+def runs_wide(x, force_generic=False):
+    """Whether the backward of these shapes runs the wide-state family (38
+    sample ranges for the weight gradients instead of 152 slots)."""
+    ensure_built()
+    B, K, SH2, D = shape_of(x)
+    return not force_generic and g.m2scan_path_for(K, SH2, D) == 3

@@ -7,8 +7,8 @@ import pytest
 import oracle
 import gated_ssm_temporal_gb300 as g
 from gated_ssm_temporal_gb300.workloads import Workload, make_inputs
-from gpu_helpers import ensure_built, to_dev
-from tolerance import assert_parity
+from gpu_helpers import ensure_built, runs_wide, shape_of, to_dev
+from tolerance import assert_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -46,18 +46,20 @@ def test_blend_parity(B, K, SH2, D, generic, with_w, gs):
     x = make_inputs(Workload("blend", B, K, SH2, D, 1.0, B + 3 * K + D))
     w = np.random.default_rng(B).standard_normal(SH2) if with_w else None
     got = run(x, w, gs, generic)
-    kw = dict(blend=True, gate_scale=1.0 if gs is None else gs)
-    ref = {"h_enriched": oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"],
-                                        w, 1.0, **kw)}
+    kw = dict(blend=True, gate_scale=1.0 if gs is None else gs, abs_terms=True)
+    y, ya = oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"], w, 1.0, **kw)
+    ref = {"h_enriched": y, "h_enriched_abs": ya}
     ref.update(oracle.backward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"], w, 1.0,
                                x["d_h_enriched"], **kw))
-    for n in ("h_enriched", "d_h_history", "d_h_s2", "dW_A", "dW_B", "dW_C"):
-        assert_parity(n, got[n], ref[n])
+    names = ["h_enriched", "d_h_history", "d_h_s2", "dW_A", "dW_B", "dW_C"]
     if with_w:
-        # the weights' gradient is a sum over the batch, like dW_O
-        assert_parity("dW_O", got["d_temporal_weight"], ref["dW_O"])
+        # the weights' gradient is a sum over the batch, like dW_O, folded over the states
+        got["dw"] = got["d_temporal_weight"]
+        names.append("dw")
     else:
         assert "d_temporal_weight" not in got
+    assert_outputs(got, ref, shape_of(x), names, wide=runs_wide(x, generic),
+                   key_map={"dw": "dW_O"})
 
 
 def test_blend_empty_batch_zero_fills_the_weight_gradient():

@@ -4,11 +4,10 @@ shape of every kernel family (needs a GB300)."""
 import numpy as np
 import pytest
 
-import oracle
 import gated_ssm_temporal_gb300 as g
 from gated_ssm_temporal_gb300.workloads import Workload, make_inputs
-from gpu_helpers import OUTPUTS, ensure_built, to_dev
-from tolerance import assert_parity
+from gpu_helpers import OUTPUTS, ensure_built, oracle_all, runs_wide, shape_of, to_dev
+from tolerance import assert_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -43,27 +42,24 @@ def run(x, gs, force_generic=False):
 
 
 def reference(x, gs):
-    ref = {"h_enriched": oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"],
-                                        x["W_O"], x["tw"], gate_scale=gs)}
-    ref.update(oracle.backward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"],
-                               x["W_O"], x["tw"], x["d_h_enriched"], gate_scale=gs))
-    return ref
+    return oracle_all(x, gate_scale=gs)
+
+
+NAMES = ("h_enriched",) + OUTPUTS
 
 
 @pytest.mark.parametrize("B,K,SH2,D,generic", SHAPES)
 def test_gate_multiplier_parity(B, K, SH2, D, generic):
     x = make_inputs(Workload("gate", B, K, SH2, D, 0.3, B + K + D))
     got, ref = run(x, 0.85, generic), reference(x, 0.85)
-    for n in ref:
-        assert_parity(n, got[n], ref[n])
+    assert_outputs(got, ref, shape_of(x), NAMES, wide=runs_wide(x, generic))
 
 
 def test_gate_multiplier_zero_keeps_only_the_last_step():
     # g = 0: x_{K-1} = B_{K-1}; W_A then gets no gradient at all
     x = make_inputs(Workload("gate0", 64, 8, 256, 16, 0.3, 5))
     got, ref = run(x, 0.0), reference(x, 0.0)
-    for n in ref:
-        assert_parity(n, got[n], ref[n])
+    assert_outputs(got, ref, shape_of(x), NAMES)
     assert np.all(got["dW_A"] == 0.0)
 
 
