@@ -43,7 +43,7 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="pages")
@@ -191,19 +191,48 @@ def kernel_sources_sha() -> str:
 
 
 def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+    """DRAM bytes per launch from the committed ncu summary, if it matches this
+    source: (reads + writes, the record) or (None, None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)[kernel]
         if t.get("kernel_sha") == kernel_sources_sha():
-            return float(t["dram_bytes_per_launch"])
+            return float(t["dram_bytes_per_launch"]), t
     except (OSError, KeyError, ValueError):
         pass
-    return None
+    return None, None
 
 
-def cpu_baseline(x, seconds: float):
-    """The fp64 oracle on this host's cores, repeated on the workload batch for ~seconds."""
+def traffic_fields(kernel: str, alg_read: float, alg_write: float) -> dict:
+    """roofline.traffic and the fields that say what it counts. DRAM writes are
+    counted when L2 evicts them: output lines still dirty in L2 when the kernel
+    ends are written back during the next kernel, so a one-launch capture can
+    show fewer write bytes than the kernel stored. Reads are complete."""
+    total, rec = recorded_traffic(kernel)
+    out = {"traffic": total, "traffic_algorithmic_read": alg_read,
+           "traffic_algorithmic_write": alg_write}
+    if rec is None:
+        out["traffic_note"] = "no capture of the current kernel sources"
+        return out
+    rd, wr = float(rec["dram_bytes_read"]), float(rec["dram_bytes_write"])
+    out.update({"traffic_read": rd, "traffic_write_evicted": wr,
+                "traffic_read_over_algorithmic": rd / alg_read if alg_read else None,
+                "traffic_write_left_in_l2": max(0.0, alg_write - wr),
+                "traffic_note": "traffic = DRAM reads + DRAM writes seen during the launch; "
+                                "writes still dirty in L2 at its end reach DRAM later and are "
+                                "not counted (traffic_write_left_in_l2 = algorithmic writes - "
+                                "evicted writes)"})
+    if "l2_write_bytes_from_sm" in rec:
+        out["traffic_l2_write_from_sm"] = float(rec["l2_write_bytes_from_sm"])
+    return out
+
+
+def cpu_baseline(x, seconds: float, gpu_out=None, act_bound=None):
+    """The fp64 oracle on this host's cores, repeated on the workload batch for
+    ~seconds. ``gpu_out``: the outputs of the last timed GPU step, which are
+    then checked against the oracle's result of the same inputs (``x`` holds
+    the values the GPU read); ``act_bound``: relative bound of the activation
+    outputs (None: the layer's fp32 criterion)."""
     import oracle
     threads = oracle.default_threads()
     B = x["h_history"].shape[0]
@@ -217,9 +246,47 @@ def cpu_baseline(x, seconds: float):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": "%d passes of fwd+bwd over the full %d-sample batch (%.1f s)"
-                      % (done // B, B, el)}
+    res = {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+           "sample": "%d passes of fwd+bwd over the full %d-sample batch (%.1f s)"
+                     % (done // B, B, el)}
+    if gpu_out is not None:
+        res["output_check"] = check_outputs(x, gpu_out, act_bound)
+    return res
+
+
+def check_outputs(x, gpu_out, act_bound=None):
+    """Every output of the last timed step against the oracle, with the parity
+    criteria of the tests (tests/tolerance.py): activation outputs element by
+    element, weight gradients on the bound from their sums of |terms|."""
+    import numpy as np
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import tolerance
+    import oracle
+    y, ya = oracle.forward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"], x["W_O"],
+                           x["tw"], abs_terms=True)
+    ref = {"h_enriched": y}
+    ref.update(oracle.backward(x["h_history"], x["h_s2"], x["W_A"], x["W_B"], x["W_C"],
+                               x["W_O"], x["tw"], x["d_h_enriched"], abs_terms=True))
+    B, K, SH2 = x["h_history"].shape
+    D = x["W_A"].shape[1]
+    out = {}
+    ok = True
+    for n, got in gpu_out.items():
+        got = np.asarray(got, dtype=np.float64)
+        if n in ("dW_A", "dW_B", "dW_C", "dW_O"):
+            r = tolerance.compare(n, got, ref[n], ref[n + "_abs"],
+                                  tolerance.coefficient(n, B, K, SH2, D))
+        elif act_bound is not None:
+            err = np.abs(got - ref[n])
+            bound = act_bound * np.abs(ref[n]) + tolerance.ATOL
+            r = {"n_fail": int((err > bound).sum()),
+                 "max_err_over_bound": float((err / bound).max()) if err.size else 0.0}
+        else:
+            r = tolerance.compare(n, got, ref[n])
+        ok = ok and r["n_fail"] == 0
+        out[n] = {"n_fail": r["n_fail"], "max_err_over_bound": r["max_err_over_bound"]}
+    out["pass"] = ok
+    return out
 
 
 # -------------------------------------------------------------- native arm
@@ -302,10 +369,19 @@ def run_native(args, rank, world, local):
     barrier(dist, local)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop(gpus=list(range(max(world, 1)))) if rank == 0 else None
-    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
-    bwd_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / n
-    fwd_ms, bwd_ms = max_over_ranks(dist, [fwd_ms, bwd_ms], device=dev)
-    step_ms = fwd_ms + bwd_ms
+    fwd_t = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_t = [e[2].elapsed_time(e[3]) for e in ev]
+    step_t = [a + b for a, b in zip(fwd_t, bwd_t)]
+    # medians of the per-step event times (the means are reported beside them)
+    fwd_ms, bwd_ms, step_ms, fwd_mean, bwd_mean = max_over_ranks(
+        dist, [statistics.median(fwd_t), statistics.median(bwd_t), statistics.median(step_t),
+               sum(fwd_t) / n, sum(bwd_t) / n], device=dev)
+    # the last timed step's outputs, for the check against the oracle
+    last_out = None
+    if rank == 0 and not args.no_cpu_baseline:
+        last_out = {"h_enriched": y.float().cpu().numpy()}
+        last_out.update({k: v.float().cpu().numpy() for k, v in outs.items()})
+    flags_timed = g.m2scan_read_device_flags()
     value = whole_job_throughput(B, world, step_ms / 1e3)
 
     # end to end: every step copies its inputs in from pinned host memory and
@@ -366,31 +442,41 @@ def run_native(args, rank, world, local):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     (e2e_ms,) = max_over_ranks(dist, [e2e_ms], device=dev)
+    flags_e2e = g.m2scan_read_device_flags()
+    (flags_any,) = max_over_ranks(dist, [float(flags_timed | flags_e2e)], device=dev)
 
     if rank != 0:
         return
-    ab = algorithmic_bytes(B, K, SH2, elem=2 if bf16 else 4)
+    elem = 2 if bf16 else 4
+    ab = algorithmic_bytes(B, K, SH2, elem=elem)
     peak, peak_src = measured_peaks()
     achieved = ab["bwd"] / (bwd_ms / 1e3) / 1e9
-    traffic = recorded_traffic("m2scan_bwd_bf16" if bf16 else "m2scan_bwd")
-    bwd_kernel = ("m2scan_bwd_bf16 (per-sample generic kernel + slot reduction)" if bf16 else
-                  "m2scan_bwd (fused backward + slot reduction)")
+    bwd_kernel = ("m2scan_bwd_bf16" if bf16 else "m2scan_bwd (fused backward + slot reduction)")
+    bwd_write = elem * SH2 * (K + 1) * B  # d_h_history and d_h_s2
+    traffic = traffic_fields("m2scan_bwd_bf16" if bf16 else "m2scan_bwd", ab["bwd"] - bwd_write,
+                             bwd_write)
     line = {
         "metric": metric_for(w) + (" with bf16 activations" if bf16 else ""), "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
+        "data": "synthetic",
         "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g per rank" % (w.name, B, K, SH2, D,
                                                                              w.tw),
                    "B": B, "K": K, "SH2": SH2, "D": D, "parallelism": "replicas x%d" % world,
                    "activations": args.dtype,
+                   "arithmetic": ("bf16 tensor-core operands (exact products), fp32 sums"
+                                  if bf16 else "fp32 (3 x TF32 tensor-core products)"),
                    "l2": "flushed (512 MiB write) before every timed fwd and every timed bwd"},
-        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "timing": "median of the per-step CUDA-event times (fwd, bwd and their sum)",
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_ms_mean": fwd_mean, "bwd_ms_mean": bwd_mean,
         "hbm_gbs": ab["total"] / (step_ms / 1e3) / 1e9,
         "hbm_frac_of_measured": ab["total"] / (step_ms / 1e3) / 1e9 / peak,
-        "roofline": {"kernel": bwd_kernel, "bound": "hbm",
-                     "achieved": achieved, "peak": peak, "peak_source": peak_src + " hbm_gbs burst",
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "algorithmic_bytes": ab["bwd"]},
+        "roofline": dict({"kernel": bwd_kernel, "bound": "hbm",
+                          "achieved": achieved, "peak": peak,
+                          "peak_source": peak_src + " hbm_gbs burst",
+                          "unit": "GB/s", "frac": achieved / peak,
+                          "algorithmic_bytes": ab["bwd"]}, **traffic),
+        "device_flags": int(flags_any),
         "e2e": {"value": whole_job_throughput(B, world, e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_before,
@@ -399,8 +485,18 @@ def run_native(args, rank, world, local):
         "pages_h100_context_ms": {"fwd": 22.0, "bwd": 1567.0},
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(x, args.cpu_seconds)
+        xo = dict(x)
+        if bf16:  # the oracle sees the values the GPU read
+            for k in acts:
+                xo[k] = d[k].float().cpu().numpy()
+        line["cpu_baseline"] = cpu_baseline(xo, args.cpu_seconds, last_out,
+                                            act_bound=2.0 ** -8 if bf16 else None)
+    if flags_any:
+        # a kernel gave up on a barrier wait: its results and times are garbage
+        line["invalid"] = "device error flags %d: a kernel gave up waiting" % int(flags_any)
     print(json.dumps(line), flush=True)
+    if flags_any or not line.get("cpu_baseline", {}).get("output_check", {"pass": True})["pass"]:
+        sys.exit(3)
 
 
 # ------------------------------------------------------------ reference arm
@@ -562,7 +658,7 @@ def run_bias_native(args, rank, world, local):
         "roofline": {"kernel": "m2scan_bias_grad (partial sums + ordered final sum)",
                      "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_source": peak_src + " hbm_gbs burst", "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name)[0],
                      "algorithmic_bytes": nbytes},
         "e2e": {"value": nbytes * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": C * 4, "ms_per_step": e2e_ms},

@@ -80,6 +80,8 @@ def load_library(path: str | None = None):
         lib.m2scan_path_for.restype = ctypes.c_int
         lib.m2scan_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.m2scan_read_device_flags.restype = ctypes.c_int
+        lib.m2scan_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
+        lib.m2scan_selftest_wait_timeout.restype = ctypes.c_int
         lib.m2scan_last_launch_count.argtypes = []
         lib.m2scan_last_launch_count.restype = ctypes.c_int
         lib.m2scan_bias_grad_workspace_bytes.argtypes = [i64, i32]
@@ -180,6 +182,11 @@ def m2scan_read_device_flags():
     if st != M2SCAN_OK:
         raise M2ScanError(st, "m2scan_read_device_flags")
     return flags.value
+
+
+def m2scan_selftest_wait_timeout(limit_ns, out, stream=0):
+    """Launches the wait-limit self-test; ``out`` is a device pointer to three uint64."""
+    return load_library().m2scan_selftest_wait_timeout(limit_ns, out, stream)
 
 
 def m2scan_last_launch_count():

@@ -142,7 +142,8 @@ int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_
     if (!bwd && fwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (bwd && bwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (fast_plan(bwd, K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
-    if (wide_path_ok(K, SH2, D)) return 3;
+    // (the wide-state kernels address rows with 32-bit TMA coordinates)
+    if (wide_path_ok(K, SH2, D) && B * K < (1ll << 31)) return 3;
   }
   if (generic_smem_bytes(bwd, K, SH2, D) <= static_cast<size_t>(max_smem)) return 2;
   return 0;
@@ -156,6 +157,19 @@ CUresult encode_map(CUtensorMap* m, const float* ptr, int rank, const cuuint64_t
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
+
+}  // namespace
+
+CUresult m2scan::encode_tensor_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+                                   const cuuint64_t* strides, const cuuint32_t* box,
+                                   CUtensorMapSwizzle swizzle) {
+  const cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(ptr), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+namespace {
 
 // bf16 h_history [SH2, K, B] (box [64, K, S_max]) and h_s2 [SH2, B] (box
 // [64, S_max]): 64 bf16 = one 128-byte swizzled row per box row.
@@ -241,6 +255,21 @@ size_t m2scan_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D) 
   return wide > slots ? wide : slots;
 }
 
+m2scan_status m2scan_selftest_wait_timeout(uint64_t limit_ns, uint64_t* out,
+                                           m2scan_stream_t stream) {
+  if (!out) return M2SCAN_ERR_NULL;
+  if (!aligned16(out)) return M2SCAN_ERR_ALIGN;
+  if (limit_ns < 1000ull || limit_ns > 100000000ull) return M2SCAN_ERR_SHAPE;
+  int dev = 0;
+  m2scan_status st = prepare_device(&dev);
+  if (st != M2SCAN_OK) return st;
+  const cudaError_t e = launch_wait_timeout_selftest(
+      g_err_ptr[dev], limit_ns, reinterpret_cast<unsigned long long*>(out), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = 1;
+  return M2SCAN_OK;
+}
+
 m2scan_status m2scan_read_device_flags(uint32_t* flags) {
   if (!flags) return M2SCAN_ERR_NULL;
   int dev = 0;
@@ -293,7 +322,7 @@ m2scan_status m2scan_fwd_ex(const float* h_history, const float* h_s2, const flo
                    : launch_fast(false, D, fa, grid, stream);
   } else if (path == 3) {
     e = launch_wide_fwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, B, K, SH2, h_enriched,
-                        gate_scale, stream);
+                        gate_scale, g_err_ptr[dev], stream);
   } else {
     GenericArgs ga{h_history, h_s2, nullptr, W_A, W_B, W_C, W_O, h_enriched, nullptr, nullptr,
                    B, K, SH2, D, tw, gate_scale};
@@ -549,7 +578,8 @@ m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const flo
   } else if (path == 3) {
     int n = 0;
     e = launch_wide_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2, d_h_history,
-                        d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, gate_scale, stream, &n);
+                        d_h_s2, dW_A, dW_B, dW_C, dW_O, workspace, gate_scale, g_err_ptr[dev], stream,
+                        &n);
     t_last_launches = n;
     if (e != cudaSuccess) return cuda_fail(e);
     return M2SCAN_OK;

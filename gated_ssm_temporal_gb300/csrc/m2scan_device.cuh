@@ -103,14 +103,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // any wait of any kernel has given up (the bit is set), every later wait that
 // has to spin gives up at its next check instead of waiting out its own
 // limit, so a broken hand-off ends the kernel in about one limit.
-__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+// `limit_ns` is kWaitLimitNs everywhere except in the library's self-test of
+// this give-up path, which waits on a barrier nobody arrives on.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, unsigned* err,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((i & 15u) == 0u) {
       if ((*reinterpret_cast<volatile unsigned*>(err) & kErrWaitTimeout) != 0u) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         atomicOr(err, kErrWaitTimeout);
         return false;
       }

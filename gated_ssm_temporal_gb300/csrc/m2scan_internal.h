@@ -91,19 +91,20 @@ bool tc_path_ok(bool bwd, int D);
 size_t generic_smem_bytes(bool bwd, int K, int SH2, int D);
 
 cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream);
-// FP32 kernels for wide states (D = 64, SH2 % 128 == 0, K <= 128).
+// Tensor-core kernels for wide states (D = 64, SH2 % 128 == 0, K <= 128).
 bool wide_path_ok(int K, int SH2, int D);
+int wide_ranges(int64_t B);
 size_t wide_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2);
 cudaError_t launch_wide_fwd(const float* h_history, const float* h_s2, const float* W_A,
                             const float* W_B, const float* W_C, const float* W_O, float tw, int64_t B,
-                            int K, int SH2, float* h_enriched, const float* gate_scale,
+                            int K, int SH2, float* h_enriched, const float* gate_scale, unsigned* err,
                             cudaStream_t stream);
 cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const float* W_A,
                             const float* W_B, const float* W_C, const float* W_O, float tw,
                             const float* g, int64_t B, int K, int SH2, float* d_h_history,
                             float* d_h_s2, float* dW_A, float* dW_B, float* dW_C, float* dW_O,
-                            void* workspace, const float* gate_scale, cudaStream_t stream,
-                            int* n_launches);
+                            void* workspace, const float* gate_scale, unsigned* err,
+                            cudaStream_t stream, int* n_launches);
 cudaError_t prepare_wide_kernels();
 // Warp-specialised tensor-core forward (D in {8, 16}).
 bool fwd_tc_plan(int K, int SH2, int D, FastArgs* a);
@@ -139,5 +140,14 @@ cudaError_t launch_colsum(const float* dy, long long N, int C, float* db, int ac
                           float* part, cudaStream_t stream, int* n_launches);
 
 unsigned* device_error_word();  // device address of the error word (current device)
+
+// TMA descriptor of a 2-D or 3-D fp32 tensor with the given swizzle (driver
+// entry point looked up at set-up; L2 promotion 256 B, zero fill out of bounds).
+CUresult encode_tensor_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+                           const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Self-test of the bounded barrier wait (one CTA; see m2scan_selftest.cu).
+cudaError_t launch_wait_timeout_selftest(unsigned* err, unsigned long long limit_ns,
+                                         unsigned long long* out, cudaStream_t stream);
 
 }  // namespace m2scan

@@ -42,6 +42,12 @@
  *     fixed sample-to-slot assignment and the slots are added in slot order
  *     (the deterministic two-phase reduction of "Phase 3 Kernel Optimization
  *     Implementation Plan", Task 2), with no floating-point atomics.
+ *   - The library looks up, once per device, the device addresses of its
+ *     static device variables and sets its kernels' shared-memory limits,
+ *     and keeps both for the life of the process. cudaDeviceReset (or
+ *     anything else that destroys the device's primary context) while the
+ *     library is in use is not supported: later calls would use addresses
+ *     from the destroyed context.
  *   - Supported shapes: B >= 0, K >= 1, SH2 >= 4 with SH2 % 4 == 0, D >= 1,
  *     and per-sample scratch of 4*K*2*D bytes within shared memory (the
  *     fallback path): K * D <= 16384. A fused fast path is used when D is 4,
@@ -86,10 +92,9 @@ m2scan_status m2scan_fwd(const float* h_history, const float* h_s2, const float*
 /*
  * Bytes of device workspace m2scan_bwd needs for these shapes: the per-slot
  * partial sums of the four weight gradients (min(B,152) slots of 4*SH2*D
- * floats); for the wide-state shapes (D = 64, SH2 % 128 == 0, K <= 128) the
- * larger of that and min(B,38) slots plus dA|dB (B*K*2D floats) and
- * [dC | ctx] (B*2D floats). Depends on the shapes only. Returns 0 for invalid
- * shapes.
+ * floats); for the wide-state shapes (D = 64, SH2 % 128 == 0, K <= 128,
+ * B*K < 2^31) those slots plus dA|dB (B*K*2D floats) and [dC | ctx] (B*2D
+ * floats). Depends on the shapes only. Returns 0 for invalid shapes.
  */
 size_t m2scan_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D);
 
@@ -281,8 +286,8 @@ int m2scan_last_cuda_error(void);
 int m2scan_set_force_generic(int force);
 
 /* Which kernel family m2scan_fwd/m2scan_bwd would launch for these shapes:
- * 1 = fused fast path, 2 = generic fallback, 3 = wide-state FP32 kernels
- * (D = 64, SH2 % 128 == 0, K <= 128), 0 = unsupported shape. */
+ * 1 = fused fast path, 2 = generic fallback, 3 = wide-state tensor-core
+ * kernels (D = 64, SH2 % 128 == 0, K <= 128), 0 = unsupported shape. */
 int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
 
 /*
@@ -294,6 +299,23 @@ int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
  * Returns M2SCAN_OK and stores the flags in *flags.
  */
 m2scan_status m2scan_read_device_flags(uint32_t* flags);
+
+/*
+ * Self-test of the time limit on the kernels' barrier waits (no counterpart
+ * on the pages; it exercises the failure path that m2scan_read_device_flags
+ * reports). Launches one small kernel that waits twice, with a limit of
+ * `limit_ns` nanoseconds (1 us to 100 ms), on a shared-memory barrier that
+ * nothing ever arrives on. The first wait gives up after the limit and sets
+ * bit 0 of the device error flags; the second then gives up at its first
+ * check of that bit. Nothing faults or hangs. `out` is a DEVICE pointer to
+ * three uint64 values (16-byte aligned): the nanoseconds each wait took and a
+ * mask (bit 0 / bit 1: the first / second wait gave up). Asynchronous on
+ * `stream`. Afterwards bit 0 of the flags is set, so kernels that would have
+ * to wait give up at once: read (and so clear) the flags with
+ * m2scan_read_device_flags before launching anything else.
+ */
+m2scan_status m2scan_selftest_wait_timeout(uint64_t limit_ns, uint64_t* out,
+                                           m2scan_stream_t stream);
 
 /* Number of CUDA kernels launched by the most recent successful call of
  * m2scan_fwd, m2scan_bwd (or their _ex forms) or m2scan_bias_grad on the
