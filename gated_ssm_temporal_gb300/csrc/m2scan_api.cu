@@ -77,6 +77,7 @@ m2scan_status prepare_device(int* dev_out) {
   if ((e = prepare_fwd_tc16_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_fwd_bf16_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_wide_kernels()) != cudaSuccess) return cuda_fail(e);
+  if ((e = prepare_bwd_bf16_kernels()) != cudaSuccess) return cuda_fail(e);
   void* p = nullptr;
   if ((e = cudaGetSymbolAddress(&p, g_m2scan_err_word)) != cudaSuccess) return cuda_fail(e);
   if (!g_encode) {
@@ -162,9 +163,9 @@ CUresult encode_map(CUtensorMap* m, const float* ptr, int rank, const cuuint64_t
 
 CUresult m2scan::encode_tensor_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
                                    const cuuint64_t* strides, const cuuint32_t* box,
-                                   CUtensorMapSwizzle swizzle) {
+                                   CUtensorMapSwizzle swizzle, CUtensorMapDataType type) {
   const cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(ptr), dims, strides, box,
+  return g_encode(m, type, rank, const_cast<void*>(ptr), dims, strides, box,
                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
@@ -637,10 +638,34 @@ m2scan_status m2scan_bwd_bf16(const void* h_history, const void* h_s2, const flo
   }
   int dev = 0;
   if ((st = prepare_device(&dev)) != M2SCAN_OK) return st;
-  const size_t smem = generic_smem_bytes(true, K, SH2, D);
-  if (smem > static_cast<size_t>(g_max_smem[dev])) return M2SCAN_ERR_UNSUPPORTED;
   const int grid = slots_for(B);
   float* ws = static_cast<float*>(workspace);
+  FastArgs fa{};
+  if (!g_force_generic.load() && bwd_bf16_tc_plan(B, K, SH2, D, &fa) &&
+      fa.smem_bytes <= g_max_smem[dev]) {
+    // the tensor-core kernel: 2-D bf16 tensor maps, 128-byte swizzle
+    const cuuint64_t sh = static_cast<cuuint64_t>(SH2);
+    const cuuint64_t dh[2] = {sh, static_cast<cuuint64_t>(B) * K}, ds[2] = {sh, static_cast<cuuint64_t>(B)};
+    const cuuint64_t str[1] = {sh * 2};
+    const cuuint32_t bh[2] = {64, 128}, bs[2] = {64, static_cast<cuuint32_t>(fa.S_max)};
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (encode_tensor_map(&fa.tm_h, h_history, 2, dh, str, bh, sw, bf) != CUDA_SUCCESS ||
+        encode_tensor_map(&fa.tm_hs, h_s2, 2, ds, str, bs, sw, bf) != CUDA_SUCCESS ||
+        encode_tensor_map(&fa.tm_g, d_h_enriched, 2, ds, str, bs, sw, bf) != CUDA_SUCCESS)
+      return M2SCAN_ERR_UNSUPPORTED;
+    fa.W_A = W_A; fa.W_B = W_B; fa.W_C = W_C; fa.W_O = W_O;
+    fa.out0 = static_cast<float*>(d_h_history); fa.out1 = static_cast<float*>(d_h_s2);
+    fa.ws = ws; fa.gate_scale = gate_scale; fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw;
+    cudaError_t e = launch_bwd_bf16_tc(fa, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_reduce(ws, grid, SH2 * D, dW_A, dW_B, dW_C, dW_O, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_last_launches = 2;
+    return M2SCAN_OK;
+  }
+  const size_t smem = generic_smem_bytes(true, K, SH2, D);
+  if (smem > static_cast<size_t>(g_max_smem[dev])) return M2SCAN_ERR_UNSUPPORTED;
   GenericArgs ga{static_cast<const float*>(h_history), static_cast<const float*>(h_s2),
                  static_cast<const float*>(d_h_enriched), W_A, W_B, W_C, W_O,
                  static_cast<float*>(d_h_history), static_cast<float*>(d_h_s2), ws,

@@ -144,7 +144,16 @@ unsigned* device_error_word();  // device address of the error word (current dev
 // TMA descriptor of a 2-D or 3-D fp32 tensor with the given swizzle (driver
 // entry point looked up at set-up; L2 promotion 256 B, zero fill out of bounds).
 CUresult encode_tensor_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-                           const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle);
+                           const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle,
+                           CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+
+// Tensor-core backward with bf16 activations (D = 16, SH2 % 64 == 0,
+// SH2 <= 256, K <= 128, B * K < 2^31). tm_h = h_history as [B*K rows][SH2]
+// bf16 (box 64 x 128 rows), tm_hs / tm_g = h_s2 / d_h_enriched [B][SH2] bf16
+// (box 64 x S_max), all 128-byte swizzle; ws = the weight-gradient slots.
+bool bwd_bf16_tc_plan(int64_t B, int K, int SH2, int D, FastArgs* a);
+cudaError_t launch_bwd_bf16_tc(const FastArgs& a, int grid, cudaStream_t stream);
+cudaError_t prepare_bwd_bf16_kernels();
 
 // Self-test of the bounded barrier wait (one CTA; see m2scan_selftest.cu).
 cudaError_t launch_wait_timeout_selftest(unsigned* err, unsigned long long limit_ns,
