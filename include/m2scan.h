@@ -169,10 +169,12 @@ m2scan_status m2scan_fwd_bf16(const void* h_history, const void* h_s2, const flo
  * activation spans counted in 2-byte elements. Any shape m2scan_bwd accepts
  * whose per-sample tile (4 * (2 * K * D + 2 * SH2 + 4 * D) bytes) fits the
  * device's shared memory; larger ones return M2SCAN_ERR_UNSUPPORTED.
- * It runs the per-sample generic kernel (no tensor-core kernel of the
- * backward reads bf16 yet), then the fixed-order slot sum: two launches (none
- * when B == 0, where the weight gradients are zeroed). Weight gradients are
- * bit-identical run to run.
+ * For D = 16, SH2 % 64 == 0, SH2 <= 256, K <= 128 (and B * K < 2^31) it
+ * runs a tensor-core kernel (bf16 products of the exact bf16 activations with
+ * the fp32 factors split into three bf16 parts, fp32 accumulation); other
+ * shapes run the per-sample generic kernel. Then the fixed-order slot sum:
+ * two launches (none when B == 0, where the weight gradients are zeroed).
+ * Weight gradients are bit-identical run to run.
  */
 m2scan_status m2scan_bwd_bf16(const void* h_history, const void* h_s2, const float* W_A,
                               const float* W_B, const float* W_C, const float* W_O, float tw,
