@@ -179,17 +179,54 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
     fence_barrier_init();
   }
   if (warp == kMma) tmem_alloc(&bb->tslot, 512);
+  // the producer requests the first stages (they need no weights) before the
+  // weights are staged, so that both latencies overlap
+  Ring pr;
+  int pn = 0, ptile = 0, ppass = 0, pq = 0;  // producer: stages issued; position of the next
+  auto produce_one = [&]() {
+    const long long tb0 = tile_start(ptile);
+    const int row0 = static_cast<int>(tb0 * K);
+    if (pn >= kNst) bounded_wait(&bb->empty[pr.i], pr.ph ^ 1u, a.err);
+    unsigned char* sp = base + kOffRing + pr.i * kStageB;
+    uint64_t* bar = &bb->full[pr.i];
+    mbar_arrive_expect_tx(bar, kHBox + 2u * static_cast<uint32_t>(S_max) * 128u);
+    tma_load_2d(sp, &a.tm_h, kBlk * pq, row0, bar);
+    tma_load_2d(sp + kHBox, &a.tm_hs, kBlk * pq, static_cast<int>(tb0), bar);
+    tma_load_2d(sp + kHBox + 2048, &a.tm_g, kBlk * pq, static_cast<int>(tb0), bar);
+    pr.next();
+    ++pn;
+    if (++pq == NB) {
+      pq = 0;
+      if (++ppass == 2) {
+        ppass = 0;
+        ++ptile;
+      }
+    }
+  };
+  if (tid == kProd * 32)
+    for (int i = 0; i < kNst && ptile < T; ++i) produce_one();
   // ---- weights, thread = feature j: the three bf16 parts of [W_A|W_B] row j
   // (pass 1: rows p * 32 + c of block j / 64), [W0 | W1] row j (d_h), and W_C^T,
-  // W_O as fp32 rows for the FMA pipe
+  // W_O as fp32 rows for the FMA pipe. Every global load is issued first.
   if (warp < kCW) {
     const int j = tid;
     if (j < SH2) {
+      float4 wr[8], wcr[4];
+      float wor[kD];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        wr[i] = __ldg(reinterpret_cast<const float4*>(a.W_A + j * kD) + i);
+        wr[4 + i] = __ldg(reinterpret_cast<const float4*>(a.W_B + j * kD) + i);
+        wcr[i] = __ldg(reinterpret_cast<const float4*>(a.W_C + j * kD) + i);
+      }
+#pragma unroll
+      for (int c = 0; c < kD; ++c) wor[c] = __ldg(a.W_O + c * SH2 + j);
       const int q = j / kBlk, jj = j % kBlk;
       unsigned char* wp = sWp + q * 96 * 128;
-#pragma unroll 4
+#pragma unroll
       for (int c = 0; c < kTD; ++c) {
-        const float w = c < kD ? __ldg(a.W_A + j * kD + c) : __ldg(a.W_B + j * kD + c - kD);
+        const float4 v4 = wr[c >> 2];
+        const float w = (c & 3) == 0 ? v4.x : (c & 3) == 1 ? v4.y : (c & 3) == 2 ? v4.z : v4.w;
         float p0, p1, p2;
         bf_parts(w, p0, p1, p2);
         put_bf(wp, bf_off(c, jj), p0);
@@ -200,8 +237,9 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
       }
 #pragma unroll
       for (int c = 0; c < kD; ++c) {
-        sWct[c * SH2P + j] = __ldg(a.W_C + j * kD + c);
-        sWo[c * SH2P + j] = __ldg(a.W_O + c * SH2 + j);
+        const float4 v4 = wcr[c >> 2];
+        sWct[c * SH2P + j] = (c & 3) == 0 ? v4.x : (c & 3) == 1 ? v4.y : (c & 3) == 2 ? v4.z : v4.w;
+        sWo[c * SH2P + j] = wor[c];
       }
     }
   }
@@ -213,27 +251,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
 
   if (warp == kProd) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      Ring r;
-      int n = 0;
-      const uint32_t bytes = kHBox + 2u * static_cast<uint32_t>(S_max) * 128u;
-      for (int t = 0; t < T; ++t) {
-        const long long tb0 = tile_start(t);
-        const int row0 = static_cast<int>(tb0 * K);
-        for (int pass = 0; pass < 2; ++pass)
-          for (int q = 0; q < NB; ++q) {
-            if (n >= kNst) bounded_wait(&bb->empty[r.i], r.ph ^ 1u, a.err);
-            unsigned char* sp = base + kOffRing + r.i * kStageB;
-            uint64_t* bar = &bb->full[r.i];
-            mbar_arrive_expect_tx(bar, bytes);
-            tma_load_2d(sp, &a.tm_h, kBlk * q, row0, bar);
-            tma_load_2d(sp + kHBox, &a.tm_hs, kBlk * q, static_cast<int>(tb0), bar);
-            tma_load_2d(sp + kHBox + 2048, &a.tm_g, kBlk * q, static_cast<int>(tb0), bar);
-            r.next();
-            ++n;
-          }
-      }
-    }
+    if (lane == 0)
+      while (ptile < T) produce_one();
   } else if (warp == kMma) {
     // --------------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -295,7 +314,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
     const int row = 32 * q4 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     const float gsc = load_gate_scale(a.gate_scale);
-    const int ss = tid >> 4, sd = tid & 15;  // (sample, state) of the dots and the scan
+    const int ss = tid >> 4, sd = tid & 15;  // (sample, state) of the scan
+    const int jp = (tid >> 4) & 3, sq = tid >> 6;  // dots: 16-column part, sample quad
     const int jj = tid & 63, cq = tid >> 6;  // column in a block, state / sample quad of the items
     float wcacc[kMaxNB][4], woacc[kMaxNB][4];  // dW_C[j][4cq + e], dW_O[4cq + e][j] partial sums
 #pragma unroll
@@ -308,8 +328,9 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
       const int S_t = static_cast<int>(tile_start(t + 1) - tb0);
       const int R_t = S_t * K;
       const long long row0 = tb0 * K;
-      // ======================= pass 1: C and d_ctx of (sample ss, state sd)
-      float cv = 0.f, gv = 0.f;
+      // ===== pass 1: C and d_ctx; thread = (state sd, samples 4 sq .. 4 sq + 3,
+      // columns 16 jp .. 16 jp + 15 of each block): a weight row serves 4 samples
+      float cacc[4] = {0.f, 0.f, 0.f, 0.f}, gacc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int q = 0; q < NB; ++q) {
         bounded_wait(&bb->full[r.i], r.ph, a.err);
         const unsigned char* sp = base + kOffRing + r.i * kStageB;
@@ -318,25 +339,46 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
         const float* wc = sWct + sd * SH2P + kBlk * q;
         const float* wo = sWo + sd * SH2P + kBlk * q;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const uint4 hv = *reinterpret_cast<const uint4*>(hs + bf_off(ss, 8 * c8));
-          const uint4 g4 = *reinterpret_cast<const uint4*>(gs + bf_off(ss, 8 * c8));
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const int c8 = 2 * jp + h8;
           const float4 w0 = lds4(wc + 8 * c8), w1 = lds4(wc + 8 * c8 + 4);
           const float4 o0 = lds4(wo + 8 * c8), o1 = lds4(wo + 8 * c8 + 4);
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
           const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
           const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            cv = fmaf(__uint_as_float(hw[e] << 16), wv[2 * e], cv);
-            cv = fmaf(__uint_as_float(hw[e] & 0xFFFF0000u), wv[2 * e + 1], cv);
-            gv = fmaf(__uint_as_float(gw[e] << 16), ov[2 * e], gv);
-            gv = fmaf(__uint_as_float(gw[e] & 0xFFFF0000u), ov[2 * e + 1], gv);
+          for (int i = 0; i < 4; ++i) {
+            const uint4 hv = *reinterpret_cast<const uint4*>(hs + bf_off(4 * sq + i, 8 * c8));
+            const uint4 g4 = *reinterpret_cast<const uint4*>(gs + bf_off(4 * sq + i, 8 * c8));
+            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              cacc[i] = fmaf(__uint_as_float(hw[e] << 16), wv[2 * e], cacc[i]);
+              cacc[i] = fmaf(__uint_as_float(hw[e] & 0xFFFF0000u), wv[2 * e + 1], cacc[i]);
+              gacc[i] = fmaf(__uint_as_float(gw[e] << 16), ov[2 * e], gacc[i]);
+              gacc[i] = fmaf(__uint_as_float(gw[e] & 0xFFFF0000u), ov[2 * e + 1], gacc[i]);
+            }
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bb->empty[r.i]);
         r.next();
+      }
+      // the four column parts added in order (A|B's buffer is free until the
+      // read-back below)
+      float cv, gv;
+      {
+        float* red = sAB;  // [4 jp][16 s][16 d], C then d_ctx
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          red[(jp * 16 + 4 * sq + i) * kD + sd] = cacc[i];
+          red[1024 + (jp * 16 + 4 * sq + i) * kD + sd] = gacc[i];
+        }
+        named_sync(1, kCT);
+        cv = (red[ss * kD + sd] + red[(16 + ss) * kD + sd]) +
+             (red[(32 + ss) * kD + sd] + red[(48 + ss) * kD + sd]);
+        gv = (red[1024 + ss * kD + sd] + red[1024 + (16 + ss) * kD + sd]) +
+             (red[1024 + (32 + ss) * kD + sd] + red[1024 + (48 + ss) * kD + sd]);
+        named_sync(1, kCT);
       }
       const float dctx = a.tw * gv;
       // =========================== projections: TMEM -> A|B (three parts added)
@@ -375,26 +417,64 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
         sDC[ss * kD + sd] = dctx * x;
         sCtx[ss * kD + sd] = cv * x;
         float dx = dctx * cv;
-        for (int u = K - 1; u >= 0; --u) {
-          const int rr = rb + u;
-          float sg, dsg;
-          sigmoid_and_slope(ab(rr, sd), sg, dsg);
-          sg *= gsc;
-          dsg *= gsc;
-          const float xprev = u > 0 ? ab(rr - 1, kD + sd) : 0.f;
-          const float dA = dx * xprev * dsg, dB = dx;
-          dx *= sg;
-          float p0, p1, p2;
-          bf_parts(dA, p0, p1, p2);
-          put_t(sd, rr, p0);
-          put_t(kTD + sd, rr, p0);
-          put_t(2 * kTD + sd, rr, p1);
-          put_t(3 * kTD + sd, rr, p2);
-          bf_parts(dB, p0, p1, p2);
-          put_t(kD + sd, rr, p0);
-          put_t(kTD + kD + sd, rr, p0);
-          put_t(2 * kTD + kD + sd, rr, p1);
-          put_t(3 * kTD + kD + sd, rr, p2);
+        if ((K & 7) == 0) {
+          // K a multiple of 8: a group of 8 steps is 8 consecutive tile rows
+          // (16 bytes of a part row), written at once per part row
+          const int prow[8] = {sd, kTD + sd, 2 * kTD + sd, 3 * kTD + sd,
+                               kD + sd, kTD + kD + sd, 2 * kTD + kD + sd, 3 * kTD + kD + sd};
+          for (int g = K / 8 - 1; g >= 0; --g) {
+            uint32_t pk[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pk[i][0] = pk[i][1] = pk[i][2] = pk[i][3] = 0u;
+#pragma unroll
+            for (int uu = 7; uu >= 0; --uu) {
+              const int rr = rb + 8 * g + uu;
+              float sg, dsg;
+              sigmoid_and_slope(ab(rr, sd), sg, dsg);
+              sg *= gsc;
+              dsg *= gsc;
+              const float xprev = (8 * g + uu) > 0 ? ab(rr - 1, kD + sd) : 0.f;
+              const float dA = dx * xprev * dsg, dB = dx;
+              dx *= sg;
+              float v[8];
+              bf_parts(dA, v[0], v[2], v[3]);
+              bf_parts(dB, v[4], v[6], v[7]);
+              v[1] = v[0];
+              v[5] = v[4];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+                pk[i][uu >> 1] |= (uu & 1) ? b << 16 : b;
+              }
+            }
+            const int r0 = rb + 8 * g;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(sT + kHBox * (r0 >> 6) + bf_off(prow[i], r0 & 63)) =
+                  make_uint4(pk[i][0], pk[i][1], pk[i][2], pk[i][3]);
+          }
+        } else {
+          for (int u = K - 1; u >= 0; --u) {
+            const int rr = rb + u;
+            float sg, dsg;
+            sigmoid_and_slope(ab(rr, sd), sg, dsg);
+            sg *= gsc;
+            dsg *= gsc;
+            const float xprev = u > 0 ? ab(rr - 1, kD + sd) : 0.f;
+            const float dA = dx * xprev * dsg, dB = dx;
+            dx *= sg;
+            float p0, p1, p2;
+            bf_parts(dA, p0, p1, p2);
+            put_t(sd, rr, p0);
+            put_t(kTD + sd, rr, p0);
+            put_t(2 * kTD + sd, rr, p1);
+            put_t(3 * kTD + sd, rr, p2);
+            bf_parts(dB, p0, p1, p2);
+            put_t(kD + sd, rr, p0);
+            put_t(kTD + kD + sd, rr, p0);
+            put_t(2 * kTD + kD + sd, rr, p1);
+            put_t(3 * kTD + kD + sd, rr, p2);
+          }
         }
       }
       if (R_t < 128) {  // rows past the tile: zero (the dW products read them)
@@ -439,7 +519,13 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
             if (s < S_t) {
               float o = bfv(gs, bf_off(s, jj));
 #pragma unroll
-              for (int c = 0; c < kD; ++c) o = fmaf(sDC[s * kD + c], wcj[c], o);
+              for (int c4 = 0; c4 < kD / 4; ++c4) {
+                const float4 dc = lds4(sDC + s * kD + 4 * c4);
+                o = fmaf(dc.x, wcj[4 * c4], o);
+                o = fmaf(dc.y, wcj[4 * c4 + 1], o);
+                o = fmaf(dc.z, wcj[4 * c4 + 2], o);
+                o = fmaf(dc.w, wcj[4 * c4 + 3], o);
+              }
               reinterpret_cast<__nv_bfloat16*>(a.out1)[(tb0 + s) * SH2 + j] = __float2bfloat16_rn(o);
             }
           }
