@@ -104,6 +104,27 @@ def test_bwd_shapes(B, K, SH2, D):
     run_bwd_and_check(make_inputs(Workload("bf16b", B, K, SH2, D, 0.3, B + K + D, 2.0)))
 
 
+@pytest.mark.parametrize("B,K,SH2", [(2000, 8, 64), (3000, 3, 192), (777, 128, 128),
+                                     (461, 8, 256), (5000, 1, 256), (1234, 24, 128)])
+def test_bwd_tensor_core_shapes(B, K, SH2):
+    # D = 16 runs the tensor-core kernel: one to four 64-column blocks, tiles
+    # of 1 to 16 samples (K = 128 down to 1), K % 8 == 0 (the packed dA|dB
+    # stores) and not, ragged tile splits (B = 461: three or four tiles per CTA)
+    run_bwd_and_check(make_inputs(Workload("bf16tc", B, K, SH2, 16, 0.3, B + K + SH2, 2.0)))
+
+
+@pytest.mark.parametrize("sign", [-1.0, 1.0])
+def test_bwd_saturated_gates(sign):
+    x = make_inputs(Workload("bf16sat", 300, 8, 256, 16, 0.3, 31))
+    x["h_history"][:, :, 0] = 1.0
+    x["W_A"][0, :] = 50.0 * sign
+    run_bwd_and_check(x)
+
+
+def test_bwd_heavy_tailed_history():
+    run_bwd_and_check(make_inputs(Workload("bf16ht", 500, 8, 256, 16, 0.1, 32, 1.0, 10.0)))
+
+
 def test_bwd_gate_multiplier():
     run_bwd_and_check(make_inputs(Workload("bf16bg", 500, 8, 256, 16, 0.3, 5)), gs=0.85)
 
