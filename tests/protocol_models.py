@@ -13,9 +13,12 @@ order, the commits of one issuing thread in issue order. The run fails on
   buffer or accumulator set written while another role reads or writes it.
 
 The models follow the kernels' source (``fwd_tc16_kernel``,
-``bwd_tc_kernel``, ``fwd_bf16_kernel``, ``fwd_tc_kernel``): the same item order, barrier
-counts, ring sizes and wait parities. ``mutation`` plants a protocol mistake
-(a dropped wait) so that the tests can check the checker.
+``bwd_tc_kernel``, ``fwd_bf16_kernel``, ``fwd_tc_kernel``, ``wide_tc_kernel``
+forward and backward, ``wide_tc_dw_kernel``, ``bwd_bf16_tc_kernel``): the same
+item order, barrier counts, ring sizes and wait parities. ``mutation`` plants
+a protocol mistake (a dropped wait, an early release) so that the tests can
+check the checker. Where a kernel's compute warps arrive one per warp, the
+model's single compute role arrives once on a barrier of count 1.
 """
 import random
 
@@ -603,4 +606,386 @@ def bwd_tc(B, P, cta, K, SH2, NST, seed, mutation=None):
     schedule({"p": producer(), "m": main(), "r": corr(), "c": compute()}, bars, events, seed)
 
 
-MODELS = {"fwd_tc16": fwd_tc16, "fwd_bf16": fwd_bf16, "bwd_tc": bwd_tc, "fwd_tc": fwd_tc}
+# ------------------------------------------------- wide-state tile kernels
+
+class Tmem:
+    """Tensor-memory regions of 128 columns: MMA writers and readers in flight,
+    compute readers and writers, checked against each other."""
+
+    def __init__(self, n):
+        self.mw, self.mr = [0] * n, [0] * n
+        self.cr, self.cw = [0] * n, [0] * n
+
+    def mma(self, writes, reads, what):
+        for r in writes:
+            assert self.cr[r] == 0 and self.cw[r] == 0, ("%s writes a region compute uses" % what, r)
+        for r in reads:
+            assert self.cw[r] == 0, ("%s reads a region compute writes" % what, r)
+        for r in writes:
+            self.mw[r] += 1
+        for r in reads:
+            self.mr[r] += 1
+
+        def done():
+            for r in writes:
+                self.mw[r] -= 1
+            for r in reads:
+                self.mr[r] -= 1
+        return done
+
+    def compute(self, regions, write, what):
+        for r in regions:
+            assert self.mw[r] == 0, ("%s while the MMA writes it" % what, r)
+            if write:
+                assert self.mr[r] == 0, ("%s while the MMA reads it" % what, r)
+        for r in regions:
+            (self.cw if write else self.cr)[r] += 1
+
+    def release(self, regions, write):
+        for r in regions:
+            (self.cw if write else self.cr)[r] -= 1
+
+
+def wide_tiles(B, P, cta, K):
+    """Tiles of the wide-state tile kernels: 128-row tiles of S_max samples
+    handed out round-robin over min(n_tiles, P) CTAs."""
+    S_max = min(128 // K, 16)
+    n_tiles = -(-B // S_max)
+    grid = min(n_tiles, P)
+    if cta >= grid:
+        return []
+    return [min(S_max, B - t * S_max) for t in range(cta, n_tiles, grid)]
+
+
+def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
+    """wide_tc_kernel: per tile NQ = SH2/32 chunk stages (backward: then 2 NB
+    stages of d_h weight tiles), a producer, one MMA thread and the compute
+    warps. Remainder buffer cq & 1 (shared with the A|B buffer); projections
+    into TMEM regions 0-3 (chunk q into q mod 4); backward: d_h blocks into
+    regions 0 and 1 in turn, dA|dB in regions 2 and 3."""
+    S = wide_tiles(B, P, cta, K)
+    T, NQ, NB = len(S), SH2 // 32, SH2 // 128
+    bars = {"acc_full": Bar("acc_full", 1), "acc_free": Bar("acc_free", 1),
+            "dab_ready": Bar("dab_ready", 1)}
+    for s in range(NST):
+        bars["full%d" % s] = Bar("full", 1)
+        bars["empty%d" % s] = Bar("empty", 1)
+        bars["split%d" % s] = Bar("split", 1)
+    for b in range(2):
+        bars["dh_full%d" % b] = Bar("dh_full", 1)
+        bars["dh_free%d" % b] = Bar("dh_free", 1)
+    events = {"tma": [], "mma": []}
+    st_read = [set() for _ in range(NST)]
+    lo_read, lo_write, ab_use = [0, 0], [0, 0], [0]
+    tm = Tmem(4)
+    per_tile = NQ + (2 * NB if bwd else 0)
+
+    def producer():
+        for pn in range(T * per_tile):
+            st = pn % NST
+            if pn >= NST:
+                yield W("empty%d" % st, pn // NST - 1)
+            assert not st_read[st], ("stage reloaded while read", st)
+            events["tma"].append(("full%d" % st, None))
+
+    def mma():
+        cq = 0
+        uses = [0, 0]
+        for t in range(T):
+            if bwd:
+                if mutation != "no_dh_free_wait":
+                    for b in range(2):
+                        if uses[b]:
+                            yield W("dh_free%d" % b, uses[b] - 1)
+            elif t > 0 and mutation != "no_acc_free_wait":
+                yield W("acc_free", t - 1)
+            for q in range(NQ):
+                st = cq % NST
+                yield W("full%d" % st, cq // NST)
+                yield W("split%d" % st, cq // NST)
+                assert lo_write[cq & 1] == 0 and ab_use[0] == 0, "remainder buffer read while written"
+                st_read[st].add(("m", cq))
+                lo_read[cq & 1] += 1
+                fin = tm.mma([q & 3], [], "projection")
+
+                def done(st=st, cq=cq, fin=fin):
+                    st_read[st].discard(("m", cq))
+                    lo_read[cq & 1] -= 1
+                    fin()
+                events["mma"].append(("empty%d" % st, done))
+                cq += 1
+            events["mma"].append(("acc_full", None))
+            if not bwd:
+                continue
+            if mutation != "no_dab_ready_wait":
+                yield W("dab_ready", t)
+            for nb in range(NB):
+                b = nb & 1
+                if uses[b] and mutation != "no_dh_free_wait":
+                    yield W("dh_free%d" % b, uses[b] - 1)
+                uses[b] += 1
+                for half in range(2):
+                    st = cq % NST
+                    yield W("full%d" % st, cq // NST)
+                    yield W("split%d" % st, cq // NST)
+                    assert lo_write[cq & 1] == 0 and ab_use[0] == 0, "remainder buffer read while written"
+                    st_read[st].add(("m", cq))
+                    lo_read[cq & 1] += 1
+                    fin = tm.mma([b], [2, 3], "d_h")
+
+                    def done(st=st, cq=cq, fin=fin):
+                        st_read[st].discard(("m", cq))
+                        lo_read[cq & 1] -= 1
+                        fin()
+                    events["mma"].append(("empty%d" % st, done))
+                    cq += 1
+                events["mma"].append(("dh_full%d" % b, None))
+
+    def compute():
+        cq = 0
+        reads = [0, 0]
+
+        def stage():
+            nonlocal cq
+            st = cq % NST
+            yield W("full%d" % st, cq // NST)
+            if cq >= 2 and mutation != "no_lo_wait":
+                yield W("empty%d" % ((cq - 2) % NST), (cq - 2) // NST)
+            assert lo_read[cq & 1] == 0, "remainder buffer written while read"
+            st_read[st].add(("c", cq))
+            lo_write[cq & 1] += 1
+            if mutation == "early_split":
+                bars["split%d" % st].arrive()
+            yield ("yield",)
+            lo_write[cq & 1] -= 1
+            st_read[st].discard(("c", cq))
+            if mutation != "early_split":
+                bars["split%d" % st].arrive()
+            cq += 1
+
+        def readback(nb):
+            b = nb & 1
+            if mutation != "no_dh_full_wait":
+                yield W("dh_full%d" % b, reads[b])
+            reads[b] += 1
+            tm.compute([b], False, "d_h read back")
+            yield ("yield",)
+            tm.release([b], False)
+            bars["dh_free%d" % b].arrive()
+
+        for t in range(T):
+            for q in range(NQ):
+                yield from stage()
+            if mutation != "no_acc_full_wait":
+                yield W("acc_full", t)
+            # partial sums of C / d_ctx, then A|B, in the buffer the remainders share
+            assert lo_read == [0, 0], "A|B buffer written while remainders are read"
+            ab_use[0] += 1
+            tm.compute([0, 1, 2, 3], False, "projections read back")
+            yield ("yield",)
+            tm.release([0, 1, 2, 3], False)
+            if not bwd:
+                bars["acc_free"].arrive()
+            yield ("yield",)  # scan (and output)
+            if bwd:
+                tm.compute([2, 3], True, "dA|dB into TMEM")
+                yield ("yield",)
+                tm.release([2, 3], True)
+                bars["dab_ready"].arrive()
+                ab_use[0] -= 1
+                for nb in range(NB):
+                    for half in range(2):
+                        yield from stage()
+                    if nb >= 1:
+                        yield from readback(nb - 1)
+                yield from readback(NB - 1)
+            else:
+                ab_use[0] -= 1
+
+    schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)
+
+
+def wide_tc_bwd(B, P, cta, K, SH2, NST, seed, mutation=None):
+    return wide_tc(B, P, cta, K, SH2, NST, seed, mutation, bwd=True)
+
+
+def wide_tc_dw(B, P, cta, K, SH2, NST, seed, mutation=None):
+    """wide_tc_dw_kernel for the range of job (cta mod 3 nb) = dW_A|dW_B: NC
+    stages of 32 rows, a producer, one MMA thread, the compute warps (the
+    remainders, then the read-back of the accumulators once every product is
+    done)."""
+    Pr = min(B, 152)
+    p = cta % Pr
+    rows = (B * (p + 1) // Pr - B * p // Pr) * K
+    NC = -(-rows // 32)
+    bars = {"done": Bar("done", 1)}
+    for s in range(NST):
+        bars["full%d" % s] = Bar("full", 1)
+        bars["empty%d" % s] = Bar("empty", 1)
+        bars["split%d" % s] = Bar("split", 1)
+    events = {"tma": [], "mma": []}
+    st_read = [set() for _ in range(NST)]
+    st_write = [0] * NST
+    tm = Tmem(1)
+
+    def producer():
+        for c in range(NC):
+            st = c % NST
+            if c >= NST:
+                yield W("empty%d" % st, c // NST - 1)
+            assert not st_read[st] and not st_write[st], ("stage reloaded while used", st)
+            events["tma"].append(("full%d" % st, None))
+
+    def mma():
+        for c in range(NC):
+            st = c % NST
+            yield W("full%d" % st, c // NST)
+            if mutation != "no_split_wait":
+                yield W("split%d" % st, c // NST)
+            assert st_write[st] == 0, "operands read while their remainders are written"
+            st_read[st].add(("m", c))
+            fin = tm.mma([0], [], "dW")
+
+            def done(st=st, c=c, fin=fin):
+                st_read[st].discard(("m", c))
+                fin()
+            events["mma"].append(("empty%d" % st, done))
+        events["mma"].append(("done", None))
+
+    def compute():
+        for c in range(NC):
+            st = c % NST
+            yield W("full%d" % st, c // NST)
+            st_write[st] += 1
+            if mutation == "early_split":
+                bars["split%d" % st].arrive()
+            yield ("yield",)
+            st_write[st] -= 1
+            if mutation != "early_split":
+                bars["split%d" % st].arrive()
+        if mutation != "no_done_wait":
+            yield W("done", 0)
+        tm.compute([0], False, "dW read back")
+        yield ("yield",)
+        tm.release([0], False)
+
+    schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)
+
+
+# --------------------------------------------------- bf16 backward kernel
+
+def bwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
+    """bwd_bf16_tc_kernel: per tile NB = SH2/64 pass-1 stages then NB stages of
+    the tile's h blocks again; a stage is freed by the MMA commit and the
+    compute warps (empty: count 2 here). TMEM region X (projections, then
+    d_h) is read back by the compute warps; T (dA|dB parts, shared memory) is
+    written by the compute warps and read by the d_h and dW products."""
+    S = tiles(B, P, cta, K)
+    T_, NB = len(S), SH2 // 64
+    bars = {"acc_full": Bar("acc_full", 1), "t_ready": Bar("t_ready", 1),
+            "dh_full": Bar("dh_full", 1), "dh_free": Bar("dh_free", 1), "dw_done": Bar("dw_done", 1)}
+    for s in range(NST):
+        bars["full%d" % s] = Bar("full", 1)
+        bars["empty%d" % s] = Bar("empty", 2)
+    events = {"tma": [], "mma": []}
+    st_read = [set() for _ in range(NST)]
+    tm = Tmem(2)  # 0: X (projections, d_h), 1: the dW accumulators
+    t_read, t_write = [0], [0]
+
+    def producer():
+        for pn in range(T_ * 2 * NB):
+            st = pn % NST
+            if pn >= NST:
+                yield W("empty%d" % st, pn // NST - 1)
+            assert not st_read[st], ("stage reloaded while read", st)
+            events["tma"].append(("full%d" % st, None))
+
+    def mma():
+        n = 0
+        for t in range(T_):
+            if t > 0 and mutation != "no_dh_free_wait":
+                yield W("dh_free", t - 1)
+            for q in range(NB):
+                st = n % NST
+                yield W("full%d" % st, n // NST)
+                st_read[st].add(("m", n))
+                fin = tm.mma([0], [], "projection")
+
+                def done(st=st, n=n, fin=fin):
+                    st_read[st].discard(("m", n))
+                    fin()
+                events["mma"].append(("empty%d" % st, done))
+                n += 1
+            events["mma"].append(("acc_full", None))
+            if mutation != "no_t_ready_wait":
+                yield W("t_ready", t)
+            assert t_write[0] == 0, "T read while written"
+            t_read[0] += 1
+            fin = tm.mma([0], [], "d_h")
+
+            def dh_done(fin=fin):
+                t_read[0] -= 1
+                fin()
+            events["mma"].append(("dh_full", dh_done))
+            for q in range(NB):
+                st = n % NST
+                yield W("full%d" % st, n // NST)
+                assert t_write[0] == 0, "T read while written"
+                st_read[st].add(("m", n))
+                t_read[0] += 1
+                fin = tm.mma([1], [], "dW")
+
+                def done(st=st, n=n, fin=fin):
+                    st_read[st].discard(("m", n))
+                    t_read[0] -= 1
+                    fin()
+                events["mma"].append(("empty%d" % st, done))
+                n += 1
+        events["mma"].append(("dw_done", None))
+
+    def compute():
+        n = 0
+
+        def stage():
+            nonlocal n
+            st = n % NST
+            yield W("full%d" % st, n // NST)
+            st_read[st].add(("c", n))
+            if mutation == "early_empty":
+                bars["empty%d" % st].arrive()
+            yield ("yield",)
+            st_read[st].discard(("c", n))
+            if mutation != "early_empty":
+                bars["empty%d" % st].arrive()
+            n += 1
+
+        for t in range(T_):
+            for q in range(NB):
+                yield from stage()
+            yield W("acc_full", t)
+            tm.compute([0], False, "projections read back")
+            yield ("yield",)
+            tm.release([0], False)
+            assert t_read[0] == 0, "T written while read"
+            t_write[0] += 1
+            yield ("yield",)  # scan: dA|dB parts into T
+            t_write[0] -= 1
+            bars["t_ready"].arrive()
+            for q in range(NB):
+                yield from stage()
+            if mutation != "no_dh_full_wait":
+                yield W("dh_full", t)
+            tm.compute([0], False, "d_h read back")
+            yield ("yield",)
+            tm.release([0], False)
+            bars["dh_free"].arrive()
+        yield W("dw_done", 0)
+        tm.compute([1], False, "dW read back")
+        tm.release([1], False)
+
+    schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)
+
+
+MODELS = {"fwd_tc16": fwd_tc16, "fwd_bf16": fwd_bf16, "bwd_tc": bwd_tc, "fwd_tc": fwd_tc,
+          "wide_tc_fwd": wide_tc, "wide_tc_bwd": wide_tc_bwd, "wide_tc_dw": wide_tc_dw,
+          "bwd_bf16": bwd_bf16}

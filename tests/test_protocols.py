@@ -14,7 +14,8 @@ P = 152
 # the narrowest and widest histories
 SHAPES = [(8192, 8), (65536, 8), (1000, 8), (300, 16), (152, 8), (20, 8), (700, 1), (400, 128), (333, 3)]
 WIDTHS = {"fwd_tc16": (256, 64, 32), "fwd_bf16": (256, 128, 64), "bwd_tc": (256, 64, 32),
-          "fwd_tc": (256, 64, 32)}
+          "fwd_tc": (256, 64, 32), "wide_tc_fwd": (512, 256, 128), "wide_tc_bwd": (512, 384, 128),
+          "wide_tc_dw": (512, 128), "bwd_bf16": (256, 192, 64)}
 
 
 @pytest.mark.parametrize("model", sorted(pm.MODELS))
@@ -58,6 +59,19 @@ MUTATIONS = [
     ("fwd_tc", "no_afree_wait"),
     ("fwd_tc", "no_accfull_wait"),
     ("fwd_tc", "early_empty"),
+    ("wide_tc_fwd", "no_lo_wait"),
+    ("wide_tc_fwd", "no_acc_full_wait"),
+    ("wide_tc_fwd", "early_split"),
+    ("wide_tc_bwd", "no_lo_wait"),
+    ("wide_tc_bwd", "early_split"),
+    ("wide_tc_bwd", "no_dh_full_wait"),
+    ("wide_tc_dw", "no_split_wait"),
+    ("wide_tc_dw", "early_split"),
+    ("wide_tc_dw", "no_done_wait"),
+    ("bwd_bf16", "no_dh_free_wait"),
+    ("bwd_bf16", "no_t_ready_wait"),
+    ("bwd_bf16", "early_empty"),
+    ("bwd_bf16", "no_dh_full_wait"),
 ]
 
 
@@ -71,3 +85,22 @@ def test_planted_protocol_mistake_is_caught(model, mutation):
             except (AssertionError, RuntimeError):
                 return
     pytest.fail("%s: %s not detected" % (model, mutation))
+
+
+# Waits the kernels keep as second guards although another wait implies
+# them: dropping one must stay harmless on the whole grid. In the wide-state
+# tile kernels the compute warps split the next stage only after reading the
+# accumulators back (forward acc_free), after writing dA|dB into TMEM
+# (dab_ready) and after reading the previous d_h block back (dh_free), and
+# the MMA thread waits for every split.
+IMPLIED = [("wide_tc_fwd", "no_acc_free_wait"), ("wide_tc_bwd", "no_dab_ready_wait"),
+           ("wide_tc_bwd", "no_dh_free_wait")]
+
+
+@pytest.mark.parametrize("model,mutation", IMPLIED)
+def test_implied_wait_is_redundant(model, mutation):
+    f = pm.MODELS[model]
+    for (B, K), SH2, NST, cta in itertools.product(SHAPES, WIDTHS[model], (2, 4), (0, 77)):
+        for seed in range(3):
+            f(B, P, cta, K, SH2, NST, seed, mutation=mutation)
+
