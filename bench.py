@@ -3,8 +3,9 @@
 
 One step = m2scan_fwd + m2scan_bwd over one batch of the 8192-sample workload
 (K=8, SH2=256, D=16, fp32), inputs resident in HBM. L2 is flushed (a 512 MiB
-write) before every timed forward and every timed backward, outside the
-timed intervals, so both read their inputs from HBM. Each rank times K steps
+write, then a 512 MiB read of another buffer, so that the write's dirty lines
+are back in HBM too) before every timed forward and every timed backward,
+outside the timed intervals, so both read their inputs from HBM. Each rank times K steps
 with CUDA events on its stream; the line reports the maximum over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
@@ -34,6 +35,24 @@ if ROOT not in sys.path:
 METRIC = "fwd+bwd samples/s (B=8192, K=8, SH2=256, D=16)"
 UNIT = "samples/s"
 FLUSH_BYTES = 512 << 20
+L2_NOTE = ("flushed before every timed call: a 512 MiB write, then a 512 MiB read of another "
+           "buffer (no dirty flush lines left for the timed call to write back)")
+
+
+class L2Flush:
+    """Evicts L2 (129 MB): writes a 512 MiB buffer, then reads another of the
+    same size, so that the timed call finds neither its inputs nor dirty
+    lines of the flush in L2."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.w = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+        self.r = torch.ones(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+        self.sink = torch.empty((), device=dev, dtype=torch.float32)
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=(0,), out=self.sink)
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
                "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -324,7 +343,7 @@ def run_native(args, rank, world, local):
     y = torch.empty((B, SH2), device=dev, dtype=act_dtype)
     outs = alloc_outs()
     ws = g.alloc_workspace(B, K, SH2, D, dev)
-    flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
     fwd_call = g.fwd_bf16 if bf16 else g.fwd
     bwd_call = g.bwd_bf16 if bf16 else g.bwd
@@ -338,9 +357,9 @@ def run_native(args, rank, world, local):
                  d["d_h_enriched"], outs=outs, workspace=ws, stream=stream)
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         fwd()
-        flush.zero_()
+        flush()
         bwd()
     torch.cuda.synchronize()
 
@@ -355,12 +374,12 @@ def run_native(args, rank, world, local):
     launches_before = 0
     wall0 = time.perf_counter()
     for i in range(n):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         fwd()
         launches_before += g.m2scan_last_launch_count()
         ev[i][1].record(stream)
-        flush.zero_()
+        flush()
         ev[i][2].record(stream)
         bwd()
         launches_before += g.m2scan_last_launch_count()
@@ -466,7 +485,7 @@ def run_native(args, rank, world, local):
                    "activations": args.dtype,
                    "arithmetic": ("bf16 tensor-core operands (exact products), fp32 sums"
                                   if bf16 else "fp32 (3 x TF32 tensor-core products)"),
-                   "l2": "flushed (512 MiB write) before every timed fwd and every timed bwd"},
+                   "l2": L2_NOTE},
         "timing": "median of the per-step CUDA-event times (fwd, bwd and their sum)",
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_ms_mean": fwd_mean, "bwd_ms_mean": bwd_mean,
         "hbm_gbs": ab["total"] / (step_ms / 1e3) / 1e9,
@@ -575,14 +594,14 @@ def run_bias_native(args, rank, world, local):
     dy = torch.from_numpy(dy_h).to(dev)
     db = torch.empty((C,), device=dev)
     ws = torch.empty((max(1, g.m2scan_bias_grad_workspace_bytes(N, C) // 4),), device=dev)
-    flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
 
     def call(src, dst):
         g.bias_grad(src, dst, workspace=ws, stream=stream)
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         call(dy, db)
     torch.cuda.synchronize()
     n = args.steps
@@ -596,7 +615,7 @@ def run_bias_native(args, rank, world, local):
     launches = 0
     wall0 = time.perf_counter()
     for i in range(n):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         call(dy, db)
         launches += g.m2scan_last_launch_count()
@@ -654,7 +673,7 @@ def run_bias_native(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "%s: N=%d C=%d per rank" % (w.name, N, C), "N": N, "C": C,
                    "parallelism": "replicas x%d" % world,
-                   "l2": "flushed (512 MiB write) before every timed call"},
+                   "l2": L2_NOTE},
         "roofline": {"kernel": "m2scan_bias_grad (partial sums + ordered final sum)",
                      "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_source": peak_src + " hbm_gbs burst", "unit": "GB/s",

@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   int trace_n = 0;
   (void)trace_n;
   if (tid == 0) TRACE_AT(0, 1);
+  if (tid == 0) TRACE_CTA(0);
   const int K = a.K, SH2 = a.SH2, S_max = a.S_max, NST = a.n_stages;
   const uint32_t stage_bytes = static_cast<uint32_t>(a.stage_bytes);
   const int NC = SH2 / kChunk;
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   if (tid == 0) TRACE_AT(0, 2);
+  if (tid == 0) TRACE_CTA(1);
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -919,6 +921,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) TRACE_CTA(2);
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 

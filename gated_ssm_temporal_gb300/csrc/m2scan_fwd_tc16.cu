@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   const int K = a.K, SH2 = a.SH2, S_max = a.S_max, NST = a.n_stages;
   int trace_n = 0;
   (void)trace_n;
+  if (tid == 0) TRACE_CTA(0);
   const uint32_t stage_bytes = static_cast<uint32_t>(a.stage_bytes);
   const int NC = SH2 / kChunk;
   const long long B = a.B;
@@ -552,6 +553,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) TRACE_CTA(2);
   if (warp == kMmaWarp) tmem_dealloc(tmem, 2 * kSetCols);
 }
 

@@ -133,27 +133,6 @@ struct DwBars {
   uint32_t tslot;
 };
 
-// Instruction descriptor of kind::tf32 with either operand MN-major.
-__host__ __device__ constexpr uint32_t idesc_tf32_mn(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
-         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// Shared-memory descriptor of an MN-major tf32 operand in the layout TMA
-// writes with 128-byte swizzle and 32-byte atoms: rows of 128 bytes (32
-// elements along M or N) one per K index, groups of 4 rows 512 bytes apart
-// (SBO), 32-element blocks along M/N `lbo` bytes apart, layout type 1.
-// The next 8 K indices (one MMA step) start 1024 bytes further.
-__device__ __forceinline__ uint64_t desc_mn32(uint32_t saddr, uint32_t lbo) {
-  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((512u >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(1u) << 61;
-  return d;
-}
-
 // Element (r, c) of the [128][128] float A|B buffer: float4 slots XOR-ed with
 // the row, so that a warp's 32 rows at one column and 32 columns of one row
 // both spread over the banks.
