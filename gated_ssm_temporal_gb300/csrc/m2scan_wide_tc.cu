@@ -164,6 +164,31 @@ __device__ __forceinline__ void split_buf(float* hi, float* lo, int n4, int t, i
   }
 }
 
+// The same for two [128 x 128 B] boxes at once (h and the weights of a
+// stage) with a compile-time share per thread: every load is issued before
+// the first store, so a thread has all eight 16-byte pieces in flight.
+template <int kThr>
+__device__ __forceinline__ void split_two_boxes(float* hi0, float* lo0, float* hi1, float* lo1, int t) {
+  constexpr int kPer = static_cast<int>(kBox / 16) / kThr;  // float4 pieces of one box per thread
+  static_assert(kPer * kThr == static_cast<int>(kBox / 16), "box not divisible by the thread count");
+  float4 v[2 * kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    v[u] = reinterpret_cast<const float4*>(hi0)[t + u * kThr];
+    v[kPer + u] = reinterpret_cast<const float4*>(hi1)[t + u * kThr];
+  }
+#pragma unroll
+  for (int u = 0; u < 2 * kPer; ++u) {
+    const float4 x = v[u];
+    const float4 h = make_float4(tf32_rn(x.x), tf32_rn(x.y), tf32_rn(x.z), tf32_rn(x.w));
+    float* hi = u < kPer ? hi0 : hi1;
+    float* lo = u < kPer ? lo0 : lo1;
+    const int i = t + (u % kPer) * kThr;
+    reinterpret_cast<float4*>(hi)[i] = h;
+    reinterpret_cast<float4*>(lo)[i] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+  }
+}
+
 // Position in a ring of n barriers: index and the parity of its current use.
 struct Ring {
   int i = 0;
@@ -379,8 +404,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
         bounded_wait(&bb->full[r.i], r.ph, a.err);
         float* sp = reinterpret_cast<float*>(base + r.i * kStage);
         float* lo = lo_buffer();
-        split_buf(sp, lo, kBox / 16, tid, kCT, true);                                 // h
-        split_buf(sp + kBox / 4, lo + kBox / 4, kBox / 16, tid, kCT, true);           // W_A|W_B
+        split_two_boxes<kCT>(sp, lo, sp + kBox / 4, lo + kBox / 4, tid);  // h, W_A|W_B
         {
           const float* hs = sp + 2 * kBox / 4;
           const float* gv = hs + 512;
@@ -574,8 +598,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
             bounded_wait(&bb->full[r.i], r.ph, a.err);
             float* sp = reinterpret_cast<float*>(base + r.i * kStage);
             float* lo = lo_buffer();
-            split_buf(sp, lo, kBox / 16, tid, kCT, true);
-            split_buf(sp + kBox / 4, lo + kBox / 4, kBox / 16, tid, kCT, true);
+            split_two_boxes<kCT>(sp, lo, sp + kBox / 4, lo + kBox / 4, tid);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bb->split[r.i]);
@@ -590,16 +613,27 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
           float4 w[16];
 #pragma unroll
           for (int qq = 0; qq < 16; ++qq) w[qq] = ldg4w(a.W_C + static_cast<size_t>(j) * kWD + 4 * qq);
-          for (int s = 0; s < S_t; ++s) {
-            float o = __ldg(a.g + (b0 + s) * SH2 + j);
+          // two samples at a time: their dY loads go out together and their
+          // sums are independent chains
+          const float* gp = a.g + b0 * SH2 + j;
+          float* o1p = a.out1 + b0 * SH2 + j;
+          for (int s = 0; s < S_t; s += 2) {
+            const bool two = s + 1 < S_t;
+            float o = __ldg(gp + static_cast<size_t>(s) * SH2);
+            float p = two ? __ldg(gp + static_cast<size_t>(s + 1) * SH2) : 0.f;
 #pragma unroll
             for (int qq = 0; qq < 16; ++qq) {
               o = fmaf(sX[(4 * qq + 0) * kWSmax + s], w[qq].x, o);
+              p = fmaf(sX[(4 * qq + 0) * kWSmax + s + 1], w[qq].x, p);
               o = fmaf(sX[(4 * qq + 1) * kWSmax + s], w[qq].y, o);
+              p = fmaf(sX[(4 * qq + 1) * kWSmax + s + 1], w[qq].y, p);
               o = fmaf(sX[(4 * qq + 2) * kWSmax + s], w[qq].z, o);
+              p = fmaf(sX[(4 * qq + 2) * kWSmax + s + 1], w[qq].z, p);
               o = fmaf(sX[(4 * qq + 3) * kWSmax + s], w[qq].w, o);
+              p = fmaf(sX[(4 * qq + 3) * kWSmax + s + 1], w[qq].w, p);
             }
-            a.out1[(b0 + s) * SH2 + j] = o;
+            o1p[static_cast<size_t>(s) * SH2] = o;
+            if (two) o1p[static_cast<size_t>(s + 1) * SH2] = p;
           }
         }
         readback(NB - 1);
