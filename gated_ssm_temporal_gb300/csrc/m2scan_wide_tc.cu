@@ -395,12 +395,32 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
           if (kk < KPP) {
             const int k = kp * KPP + kk;
             wcr[kk] = ldg4w(a.W_C + static_cast<size_t>(k0 + k) * kWD + 4 * dq);
-            if (BWD)
-              wor[kk] = make_float4(__ldg(a.W_O + static_cast<size_t>(4 * dq) * SH2 + k0 + k),
-                                    __ldg(a.W_O + static_cast<size_t>(4 * dq + 1) * SH2 + k0 + k),
-                                    __ldg(a.W_O + static_cast<size_t>(4 * dq + 2) * SH2 + k0 + k),
-                                    __ldg(a.W_O + static_cast<size_t>(4 * dq + 3) * SH2 + k0 + k));
           }
+        if (BWD) {
+          // W_O rows 4 dq .. 4 dq + 3 over this thread's KPP consecutive
+          // columns: 16-byte loads along each row (8-byte when KPP = 2), then
+          // regrouped by column
+          float ow[4][8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float* rowp = a.W_O + static_cast<size_t>(4 * dq + i) * SH2 + k0 + kp * KPP;
+            if (KPP >= 4) {
+#pragma unroll
+              for (int c = 0; c < 8; c += 4)
+                if (c < KPP) {
+                  const float4 v = ldg4w(rowp + c);
+                  ow[i][c] = v.x; ow[i][c + 1] = v.y; ow[i][c + 2] = v.z; ow[i][c + 3] = v.w;
+                }
+            } else {
+              const float2 v = __ldg(reinterpret_cast<const float2*>(rowp));
+              ow[i][0] = v.x;
+              ow[i][1] = v.y;
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            if (kk < KPP) wor[kk] = make_float4(ow[0][kk], ow[1][kk], ow[2][kk], ow[3][kk]);
+        }
         bounded_wait(&bb->full[r.i], r.ph, a.err);
         float* sp = reinterpret_cast<float*>(base + r.i * kStage);
         float* lo = lo_buffer();
@@ -493,34 +513,60 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
       }
       named_sync(1, kCT);
       // ===================================================== scan per (s, d)
-      for (int p = tid; p < S_t * kWD; p += kCT) {
-        const int s = p >> 6, d = p & 63, rb = s * K;
-        float x = 0.f;
-        for (int u = 0; u < K; ++u) {  // backward: B_t is replaced by x_t
-          float* pb = sAB + ab_idx(rb + u, kWD + d);
-          x = fmaf(gsc * sigmoid_fast(sAB[ab_idx(rb + u, d)]), x, *pb);
-          if (BWD) *pb = x;
+      // two (sample, state) pairs per thread side by side (p0 and p0 + kCT):
+      // each pair's arithmetic is unchanged, the two chains overlap
+      for (int p0 = tid; p0 < S_t * kWD; p0 += 2 * kCT) {
+        const bool two = p0 + kCT < S_t * kWD;
+        int ss[2], dd[2], rbb[2];
+        float xx[2] = {0.f, 0.f};
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int p = p0 + jj * kCT;
+          ss[jj] = p >> 6;
+          dd[jj] = p & 63;
+          rbb[jj] = ss[jj] * K;
         }
-        const float Cv = sC[s * kWD + d];
-        if (!BWD) {
-          sX[d * kWSmax + s] = Cv * x;
-        } else {
-          const float dctx = sDctx[s * kWD + d];
-          const float dC = dctx * x;
-          sX[d * kWSmax + s] = dC;
-          a.cc[(b0 + s) * kWN + d] = dC;
-          a.cc[(b0 + s) * kWN + kWD + d] = Cv * x;
-          float dx = dctx * Cv;
+        for (int u = 0; u < K; ++u) {  // backward: B_t is replaced by x_t
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            if (jj == 1 && !two) break;
+            float* pb = sAB + ab_idx(rbb[jj] + u, kWD + dd[jj]);
+            xx[jj] = fmaf(gsc * sigmoid_fast(sAB[ab_idx(rbb[jj] + u, dd[jj])]), xx[jj], *pb);
+            if (BWD) *pb = xx[jj];
+          }
+        }
+        float dxx[2] = {0.f, 0.f};
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          if (jj == 1 && !two) break;
+          const int s = ss[jj], d = dd[jj];
+          const float Cv = sC[s * kWD + d];
+          if (!BWD) {
+            sX[d * kWSmax + s] = Cv * xx[jj];
+          } else {
+            const float dctx = sDctx[s * kWD + d];
+            const float dC = dctx * xx[jj];
+            sX[d * kWSmax + s] = dC;
+            a.cc[(b0 + s) * kWN + d] = dC;
+            a.cc[(b0 + s) * kWN + kWD + d] = Cv * xx[jj];
+            dxx[jj] = dctx * Cv;
+          }
+        }
+        if (BWD) {
           for (int u = K - 1; u >= 0; --u) {
-            const int rr = rb + u;
-            float sg, dsg;
-            sigmoid_and_slope(sAB[ab_idx(rr, d)], sg, dsg);
-            sg *= gsc;
-            dsg *= gsc;
-            const float xprev = u > 0 ? sAB[ab_idx(rr - 1, kWD + d)] : 0.f;
-            sAB[ab_idx(rr, d)] = dx * xprev * dsg;
-            sAB[ab_idx(rr, kWD + d)] = dx;
-            dx *= sg;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              if (jj == 1 && !two) break;
+              const int rr = rbb[jj] + u, d = dd[jj];
+              float sg, dsg;
+              sigmoid_and_slope(sAB[ab_idx(rr, d)], sg, dsg);
+              sg *= gsc;
+              dsg *= gsc;
+              const float xprev = u > 0 ? sAB[ab_idx(rr - 1, kWD + d)] : 0.f;
+              sAB[ab_idx(rr, d)] = dxx[jj] * xprev * dsg;
+              sAB[ab_idx(rr, kWD + d)] = dxx[jj];
+              dxx[jj] *= sg;
+            }
           }
         }
       }
@@ -623,14 +669,19 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
             float p = two ? __ldg(gp + static_cast<size_t>(s + 1) * SH2) : 0.f;
 #pragma unroll
             for (int qq = 0; qq < 16; ++qq) {
-              o = fmaf(sX[(4 * qq + 0) * kWSmax + s], w[qq].x, o);
-              p = fmaf(sX[(4 * qq + 0) * kWSmax + s + 1], w[qq].x, p);
-              o = fmaf(sX[(4 * qq + 1) * kWSmax + s], w[qq].y, o);
-              p = fmaf(sX[(4 * qq + 1) * kWSmax + s + 1], w[qq].y, p);
-              o = fmaf(sX[(4 * qq + 2) * kWSmax + s], w[qq].z, o);
-              p = fmaf(sX[(4 * qq + 2) * kWSmax + s + 1], w[qq].z, p);
-              o = fmaf(sX[(4 * qq + 3) * kWSmax + s], w[qq].w, o);
-              p = fmaf(sX[(4 * qq + 3) * kWSmax + s + 1], w[qq].w, p);
+              // s is even: samples s and s + 1 of a state in one 8-byte read
+              const float2 x0 = *reinterpret_cast<const float2*>(sX + (4 * qq + 0) * kWSmax + s);
+              const float2 x1 = *reinterpret_cast<const float2*>(sX + (4 * qq + 1) * kWSmax + s);
+              const float2 x2 = *reinterpret_cast<const float2*>(sX + (4 * qq + 2) * kWSmax + s);
+              const float2 x3 = *reinterpret_cast<const float2*>(sX + (4 * qq + 3) * kWSmax + s);
+              o = fmaf(x0.x, w[qq].x, o);
+              p = fmaf(x0.y, w[qq].x, p);
+              o = fmaf(x1.x, w[qq].y, o);
+              p = fmaf(x1.y, w[qq].y, p);
+              o = fmaf(x2.x, w[qq].z, o);
+              p = fmaf(x2.y, w[qq].z, p);
+              o = fmaf(x3.x, w[qq].w, o);
+              p = fmaf(x3.y, w[qq].w, p);
             }
             o1p[static_cast<size_t>(s) * SH2] = o;
             if (two) o1p[static_cast<size_t>(s + 1) * SH2] = p;
