@@ -600,6 +600,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_bf16_tc_kernel(const __grid_
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) signal_dependent_launch();
   if (warp == kMma) tmem_dealloc(tmem, 512);
 }
 

@@ -921,6 +921,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) signal_dependent_launch();
   if (tid == 0) TRACE_CTA(2);
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }

@@ -40,6 +40,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Lets the next kernel of the stream, when it was launched as a programmatic
+// dependent (the weight-gradient slot sum), be scheduled once every CTA of
+// this grid has signalled or exited. It orders no memory: the dependent
+// still waits for this grid to complete (griddepcontrol.wait) before it
+// reads anything this grid wrote. Called by one thread after the CTA's last
+// barrier, so the dependent's CTAs take SMs only as this grid's CTAs leave.
+__device__ __forceinline__ void signal_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)

@@ -708,6 +708,10 @@ __global__ void __launch_bounds__(kThreads, 1) fast_kernel(const __grid_constant
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem_acc, a.tmem_cols);
   }
+  if constexpr (BWD) {
+    __syncthreads();
+    if (tid == 0) signal_dependent_launch();
+  }
 }
 
 }  // namespace

@@ -190,6 +190,10 @@ __global__ void __launch_bounds__(kThreads) generic_kernel(const GenericArgs a) 
   }
   if (BWD && staged)
     for (int e = tid; e < 4 * n; e += kThreads) gslot[e] = sSlot[e];
+  if (BWD) {
+    __syncthreads();
+    if (tid == 0) signal_dependent_launch();
+  }
 }
 
 // dW[e] = sum over slots p = 0..P-1 of ws[p][e], added in a fixed order:
@@ -199,6 +203,9 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const float* __restric
                                                           int n, float* dW_A, float* dW_B,
                                                           float* dW_C, float* dW_O) {
   __shared__ float4 red[8][32];
+  // launched as a programmatic dependent of the kernel that wrote the slots:
+  // nothing is read before that grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
   const long long total = 4ll * n;
   const long long e0 = static_cast<long long>(blockIdx.x) * 128 + 4 * lane;
@@ -269,8 +276,21 @@ cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float*
                           float* dW_C, float* dW_O, cudaStream_t stream) {
   const long long total = 4ll * n;
   const int grid = static_cast<int>((total + 127) / 128);
-  reduce_kernel<<<grid, kThreads, 0, stream>>>(ws, slots, n, dW_A, dW_B, dW_C, dW_O);
-  return cudaGetLastError();
+  // A programmatic dependent of the slot-writing kernel: its launch is
+  // prepared while that kernel's last CTAs finish (they signal after their
+  // final barrier), and its griddepcontrol.wait keeps every read behind the
+  // completion of that kernel. Backward call at B = 8192, K = 8, SH2 = 256:
+  // 81.9 -> 77.8 us against a plain launch.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_kernel, ws, slots, n, dW_A, dW_B, dW_C, dW_O);
 }
 
 cudaError_t prepare_generic_kernels(int max_smem) {

@@ -854,6 +854,7 @@ __global__ void __launch_bounds__(kDwThreads, 1) wide_tc_dw_kernel(const __grid_
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) signal_dependent_launch();
   if (warp == mma_warp) tmem_dealloc(tmem, 512);
 }
 
