@@ -385,11 +385,12 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
 #pragma unroll
         for (int j = 0; j < 4; ++j) cacc[i][j] = gacc[i][j] = 0.f;
       // ============================================ projection chunks
-      for (int q = 0; q < NQ; ++q) {
-        // this chunk's W_C (and W_O) values first: their latency runs under
-        // the remainder work
+      // W_C (and W_O) values of chunk q for this thread's dots; those of
+      // chunk q + 1 are loaded as soon as chunk q's dots have used them, so
+      // their latency runs under the next chunk's wait and remainder work
+      float4 wcr[8], wor[8];
+      auto load_chunk_weights = [&](int q) {
         const int k0 = 32 * q;
-        float4 wcr[8], wor[8];
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (kk < KPP) {
@@ -421,6 +422,10 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
           for (int kk = 0; kk < 8; ++kk)
             if (kk < KPP) wor[kk] = make_float4(ow[0][kk], ow[1][kk], ow[2][kk], ow[3][kk]);
         }
+      };
+      if (!BWD) load_chunk_weights(0);
+      for (int q = 0; q < NQ; ++q) {
+        if (BWD) load_chunk_weights(q);
         bounded_wait(&bb->full[r.i], r.ph, a.err);
         float* sp = reinterpret_cast<float*>(base + r.i * kStage);
         float* lo = lo_buffer();
@@ -448,6 +453,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
             }
           }
         }
+        if (!BWD && q + 1 < NQ) load_chunk_weights(q + 1);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bb->split[r.i]);
@@ -663,28 +669,39 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
           // sums are independent chains
           const float* gp = a.g + b0 * SH2 + j;
           float* o1p = a.out1 + b0 * SH2 + j;
-          for (int s = 0; s < S_t; s += 2) {
-            const bool two = s + 1 < S_t;
-            float o = __ldg(gp + static_cast<size_t>(s) * SH2);
-            float p = two ? __ldg(gp + static_cast<size_t>(s + 1) * SH2) : 0.f;
+          for (int s = 0; s < S_t; s += 4) {
+            const int ns = min(4, S_t - s);
+            float o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) o[u] = u < ns ? __ldg(gp + static_cast<size_t>(s + u) * SH2) : 0.f;
 #pragma unroll
             for (int qq = 0; qq < 16; ++qq) {
-              // s is even: samples s and s + 1 of a state in one 8-byte read
-              const float2 x0 = *reinterpret_cast<const float2*>(sX + (4 * qq + 0) * kWSmax + s);
-              const float2 x1 = *reinterpret_cast<const float2*>(sX + (4 * qq + 1) * kWSmax + s);
-              const float2 x2 = *reinterpret_cast<const float2*>(sX + (4 * qq + 2) * kWSmax + s);
-              const float2 x3 = *reinterpret_cast<const float2*>(sX + (4 * qq + 3) * kWSmax + s);
-              o = fmaf(x0.x, w[qq].x, o);
-              p = fmaf(x0.y, w[qq].x, p);
-              o = fmaf(x1.x, w[qq].y, o);
-              p = fmaf(x1.y, w[qq].y, p);
-              o = fmaf(x2.x, w[qq].z, o);
-              p = fmaf(x2.y, w[qq].z, p);
-              o = fmaf(x3.x, w[qq].w, o);
-              p = fmaf(x3.y, w[qq].w, p);
+              // s is a multiple of 4: samples s .. s + 3 of a state in one
+              // 16-byte read (entries past S_t are read, their sums dropped)
+              const float4 x0 = *reinterpret_cast<const float4*>(sX + (4 * qq + 0) * kWSmax + s);
+              const float4 x1 = *reinterpret_cast<const float4*>(sX + (4 * qq + 1) * kWSmax + s);
+              const float4 x2 = *reinterpret_cast<const float4*>(sX + (4 * qq + 2) * kWSmax + s);
+              const float4 x3 = *reinterpret_cast<const float4*>(sX + (4 * qq + 3) * kWSmax + s);
+              o[0] = fmaf(x0.x, w[qq].x, o[0]);
+              o[1] = fmaf(x0.y, w[qq].x, o[1]);
+              o[2] = fmaf(x0.z, w[qq].x, o[2]);
+              o[3] = fmaf(x0.w, w[qq].x, o[3]);
+              o[0] = fmaf(x1.x, w[qq].y, o[0]);
+              o[1] = fmaf(x1.y, w[qq].y, o[1]);
+              o[2] = fmaf(x1.z, w[qq].y, o[2]);
+              o[3] = fmaf(x1.w, w[qq].y, o[3]);
+              o[0] = fmaf(x2.x, w[qq].z, o[0]);
+              o[1] = fmaf(x2.y, w[qq].z, o[1]);
+              o[2] = fmaf(x2.z, w[qq].z, o[2]);
+              o[3] = fmaf(x2.w, w[qq].z, o[3]);
+              o[0] = fmaf(x3.x, w[qq].w, o[0]);
+              o[1] = fmaf(x3.y, w[qq].w, o[1]);
+              o[2] = fmaf(x3.z, w[qq].w, o[2]);
+              o[3] = fmaf(x3.w, w[qq].w, o[3]);
             }
-            o1p[static_cast<size_t>(s) * SH2] = o;
-            if (two) o1p[static_cast<size_t>(s + 1) * SH2] = p;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (u < ns) o1p[static_cast<size_t>(s + u) * SH2] = o[u];
           }
         }
         readback(NB - 1);
