@@ -23,8 +23,9 @@
 //       dx x_{t-1} sigmoid'(A_t), dx <- dx sigmoid(A_t)); dA|dB split into tf32
 //       part and remainder in TMEM (A operand) for d_h_history =
 //       dA|dB . [W_A|W_B]^T on the tensor cores (four 128-column blocks, two
-//       accumulators in turn); d_h_s2 = dY + dC . W_C^T on the FMA pipe. dA|dB
-//       and [dC | ctx] go to the workspace.
+//       accumulators in turn). dA|dB and [dC | ctx] go to the workspace.
+//   wide_dhs2_kernel       d_h_s2 = dY + dC . W_C^T over the whole batch on
+//       the FMA pipe, from the dC the tile kernel left in the workspace.
 //   wide_tc_dw_kernel      the weight gradients as products over the batch:
 //       dW_A|dW_B = h^T . dA|dB over all rows, dW_C = h_s2^T . dC and
 //       dW_O^T = dY^T . ctx (times tw) over all samples. CTA (job, p) sums the
@@ -85,11 +86,9 @@ constexpr uint32_t kDwSmem = kDwOffBar + 128 + 1024;
 struct alignas(128) WideTcArgs {
   CUtensorMap tm_h, tm_wa, tm_wb, tm_wak, tm_wbk, tm_hs, tm_g;
   const float* h_s2;
-  const float* g;  // d_h_enriched (backward)
   const float* W_C;
   const float* W_O;
   float* out0;     // forward: h_enriched; backward: d_h_history
-  float* out1;     // backward: d_h_s2
   float* dab;      // backward: dA|dB [B*K][128]
   float* cc;       // backward: [dC | ctx] [B][128]
   const float* gate_scale;
@@ -659,51 +658,6 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
           }
           if (nb >= 1) readback(nb - 1);
         }
-        // d_h_s2 = dY + dC . W_C^T: thread = column j (its W_C row in
-        // registers) x every sample of the tile
-        for (int j = tid; j < SH2; j += kCT) {
-          float4 w[16];
-#pragma unroll
-          for (int qq = 0; qq < 16; ++qq) w[qq] = ldg4w(a.W_C + static_cast<size_t>(j) * kWD + 4 * qq);
-          // two samples at a time: their dY loads go out together and their
-          // sums are independent chains
-          const float* gp = a.g + b0 * SH2 + j;
-          float* o1p = a.out1 + b0 * SH2 + j;
-          for (int s = 0; s < S_t; s += 4) {
-            const int ns = min(4, S_t - s);
-            float o[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) o[u] = u < ns ? __ldg(gp + static_cast<size_t>(s + u) * SH2) : 0.f;
-#pragma unroll
-            for (int qq = 0; qq < 16; ++qq) {
-              // s is a multiple of 4: samples s .. s + 3 of a state in one
-              // 16-byte read (entries past S_t are read, their sums dropped)
-              const float4 x0 = *reinterpret_cast<const float4*>(sX + (4 * qq + 0) * kWSmax + s);
-              const float4 x1 = *reinterpret_cast<const float4*>(sX + (4 * qq + 1) * kWSmax + s);
-              const float4 x2 = *reinterpret_cast<const float4*>(sX + (4 * qq + 2) * kWSmax + s);
-              const float4 x3 = *reinterpret_cast<const float4*>(sX + (4 * qq + 3) * kWSmax + s);
-              o[0] = fmaf(x0.x, w[qq].x, o[0]);
-              o[1] = fmaf(x0.y, w[qq].x, o[1]);
-              o[2] = fmaf(x0.z, w[qq].x, o[2]);
-              o[3] = fmaf(x0.w, w[qq].x, o[3]);
-              o[0] = fmaf(x1.x, w[qq].y, o[0]);
-              o[1] = fmaf(x1.y, w[qq].y, o[1]);
-              o[2] = fmaf(x1.z, w[qq].y, o[2]);
-              o[3] = fmaf(x1.w, w[qq].y, o[3]);
-              o[0] = fmaf(x2.x, w[qq].z, o[0]);
-              o[1] = fmaf(x2.y, w[qq].z, o[1]);
-              o[2] = fmaf(x2.z, w[qq].z, o[2]);
-              o[3] = fmaf(x2.w, w[qq].z, o[3]);
-              o[0] = fmaf(x3.x, w[qq].w, o[0]);
-              o[1] = fmaf(x3.y, w[qq].w, o[1]);
-              o[2] = fmaf(x3.z, w[qq].w, o[2]);
-              o[3] = fmaf(x3.w, w[qq].w, o[3]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (u < ns) o1p[static_cast<size_t>(s + u) * SH2] = o[u];
-          }
-        }
         readback(NB - 1);
       }
       named_sync(1, kCT);  // sC, sDctx, sX and sAB are reused by the next tile
@@ -875,6 +829,77 @@ __global__ void __launch_bounds__(kDwThreads, 1) wide_tc_dw_kernel(const __grid_
   if (warp == mma_warp) tmem_dealloc(tmem, 512);
 }
 
+// d_h_s2 = dY + dC . W_C^T ("Custom Kernel Optimization Implementation Plan",
+// Task 2: the input gradient of the C projection) over the whole batch. CTA =
+// 64 samples x 64 columns, thread = 4 samples x 4 columns; dC (columns 0..63
+// of the workspace's [dC | ctx] rows) and the CTA's 64 rows of W_C are staged
+// transposed in shared memory (34 KB), so that for each state d a thread
+// reads its 4 dC values and 4 W_C values as one 16-byte piece each. Every
+// output starts from dY and adds its 64 products in state order with fused
+// multiply-adds.
+constexpr int kHsS = 64, kHsJ = 64, kHsThreads = 256;
+constexpr int kHsPadS = kHsS + 4, kHsPadJ = kHsJ + 4;  // row strides, 16-byte multiples
+
+__global__ void __launch_bounds__(kHsThreads) wide_dhs2_kernel(const float* __restrict__ g,
+                                                                const float* __restrict__ cc,
+                                                                const float* __restrict__ W_C,
+                                                                float* __restrict__ out, long long B,
+                                                                int SH2) {
+  __shared__ __align__(16) float sdc[kWD * kHsPadS];  // dC^T [d][s]
+  __shared__ __align__(16) float swc[kWD * kHsPadJ];  // W_C^T [d][j]
+  const int tid = threadIdx.x;
+  const long long s0 = static_cast<long long>(blockIdx.x) * kHsS;
+  const int j0 = blockIdx.y * kHsJ;
+  const int ns = static_cast<int>(min(static_cast<long long>(kHsS), B - s0));
+  // staging: consecutive threads take consecutive samples (or columns), so
+  // the transposed stores fall in distinct banks
+  for (int i = tid; i < kHsS * (kWD / 4); i += kHsThreads) {
+    const int sl = i % kHsS, d4 = i / kHsS;
+    const float4 v = sl < ns ? ldg4w(cc + (s0 + sl) * kWN + 4 * d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    sdc[(4 * d4 + 0) * kHsPadS + sl] = v.x;
+    sdc[(4 * d4 + 1) * kHsPadS + sl] = v.y;
+    sdc[(4 * d4 + 2) * kHsPadS + sl] = v.z;
+    sdc[(4 * d4 + 3) * kHsPadS + sl] = v.w;
+  }
+  for (int i = tid; i < kHsJ * (kWD / 4); i += kHsThreads) {
+    const int jl = i % kHsJ, d4 = i / kHsJ;
+    const float4 v = ldg4w(W_C + static_cast<size_t>(j0 + jl) * kWD + 4 * d4);
+    swc[(4 * d4 + 0) * kHsPadJ + jl] = v.x;
+    swc[(4 * d4 + 1) * kHsPadJ + jl] = v.y;
+    swc[(4 * d4 + 2) * kHsPadJ + jl] = v.z;
+    swc[(4 * d4 + 3) * kHsPadJ + jl] = v.w;
+  }
+  // this thread's outputs start from dY: samples 4 sg .. 4 sg + 3, columns
+  // 4 cg .. 4 cg + 3 (a warp reads a 256-byte row piece of two samples)
+  const int cg = tid & 15, sg = tid >> 4;
+  float o[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int sl = 4 * sg + i;
+    const float4 a0 = sl < ns ? ldg4w(g + (s0 + sl) * SH2 + j0 + 4 * cg) : make_float4(0.f, 0.f, 0.f, 0.f);
+    o[i][0] = a0.x; o[i][1] = a0.y; o[i][2] = a0.z; o[i][3] = a0.w;
+  }
+  __syncthreads();
+#pragma unroll 8
+  for (int d = 0; d < kWD; ++d) {
+    const float4 x = *reinterpret_cast<const float4*>(sdc + d * kHsPadS + 4 * sg);
+    const float4 w = *reinterpret_cast<const float4*>(swc + d * kHsPadJ + 4 * cg);
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    const float ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[i][c] = fmaf(xs[i], ws[c], o[i][c]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int sl = 4 * sg + i;
+    if (sl < ns)
+      *reinterpret_cast<float4*>(out + (s0 + sl) * SH2 + j0 + 4 * cg) =
+          make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+  }
+}
+
 }  // namespace
 
 bool wide_path_ok(int K, int SH2, int D) {
@@ -942,8 +967,8 @@ cudaError_t launch_wide_fwd(const float* h_history, const float* h_s2, const flo
   return cudaGetLastError();
 }
 
-// The tile kernel, the weight-gradient products and the slot reduction: the
-// number of launches goes to *n.
+// The tile kernel, d_h_s2, the weight-gradient products and the slot
+// reduction: the number of launches goes to *n.
 cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const float* W_A,
                             const float* W_B, const float* W_C, const float* W_O, float tw,
                             const float* g, int64_t B, int K, int SH2, float* d_h_history,
@@ -959,12 +984,16 @@ cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const flo
   float* slots = ws;
   float* dab = ws + static_cast<size_t>(P) * 4 * static_cast<size_t>(SH2) * kWD;
   float* cc = dab + static_cast<size_t>(B) * K * kWN;
-  w.h_s2 = h_s2; w.g = g; w.W_C = W_C; w.W_O = W_O; w.out0 = d_h_history; w.out1 = d_h_s2;
+  w.h_s2 = h_s2; w.W_C = W_C; w.W_O = W_O; w.out0 = d_h_history;
   w.dab = dab; w.cc = cc; w.gate_scale = gate_scale; w.err = err;
   w.B = B; w.K = K; w.SH2 = SH2; w.tw = tw;
   wide_tc_kernel<true><<<wide_grid(B, w.S_max), kTileThreads, kTileSmem, stream>>>(w);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  ++*n;
+  const dim3 hs_grid(static_cast<unsigned>((B + kHsS - 1) / kHsS), static_cast<unsigned>(SH2 / kHsJ));
+  wide_dhs2_kernel<<<hs_grid, kHsThreads, 0, stream>>>(g, cc, W_C, d_h_s2, B, SH2);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n;
   WideDwArgs dw{};
   {
