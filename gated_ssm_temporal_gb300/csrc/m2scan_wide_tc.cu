@@ -831,72 +831,95 @@ __global__ void __launch_bounds__(kDwThreads, 1) wide_tc_dw_kernel(const __grid_
 
 // d_h_s2 = dY + dC . W_C^T ("Custom Kernel Optimization Implementation Plan",
 // Task 2: the input gradient of the C projection) over the whole batch. CTA =
-// 64 samples x 64 columns, thread = 4 samples x 4 columns; dC (columns 0..63
-// of the workspace's [dC | ctx] rows) and the CTA's 64 rows of W_C are staged
-// transposed in shared memory (34 KB), so that for each state d a thread
-// reads its 4 dC values and 4 W_C values as one 16-byte piece each. Every
-// output starts from dY and adds its 64 products in state order with fused
-// multiply-adds.
-constexpr int kHsS = 64, kHsJ = 64, kHsThreads = 256;
+// 128 samples x 128 columns, thread = 8 samples x 8 columns (4 in each
+// 64-column half, so that a warp's W_C reads are contiguous); dC (columns 0..63
+// of the workspace's [dC | ctx] rows) and the CTA's 128 rows of W_C are staged
+// transposed in shared memory (68 KB), so that for each state d a thread reads
+// its 8 dC values and 8 W_C values as two 16-byte pieces each and does 64
+// multiply-adds with them. Every output starts from dY and adds its 64
+// products in state order with fused multiply-adds.
+constexpr int kHsS = 128, kHsJ = 128, kHsThreads = 256;
 constexpr int kHsPadS = kHsS + 4, kHsPadJ = kHsJ + 4;  // row strides, 16-byte multiples
+constexpr uint32_t kHsSmem = (kWD * kHsPadS + kWD * kHsPadJ) * 4;
 
 __global__ void __launch_bounds__(kHsThreads) wide_dhs2_kernel(const float* __restrict__ g,
                                                                 const float* __restrict__ cc,
                                                                 const float* __restrict__ W_C,
                                                                 float* __restrict__ out, long long B,
                                                                 int SH2) {
-  __shared__ __align__(16) float sdc[kWD * kHsPadS];  // dC^T [d][s]
-  __shared__ __align__(16) float swc[kWD * kHsPadJ];  // W_C^T [d][j]
+  extern __shared__ __align__(16) float hs_smem[];
+  float* sdc = hs_smem;                  // dC^T [d][s]
+  float* swc = hs_smem + kWD * kHsPadS;  // W_C^T [d][j]
   const int tid = threadIdx.x;
   const long long s0 = static_cast<long long>(blockIdx.x) * kHsS;
   const int j0 = blockIdx.y * kHsJ;
   const int ns = static_cast<int>(min(static_cast<long long>(kHsS), B - s0));
-  // staging: consecutive threads take consecutive samples (or columns), so
-  // the transposed stores fall in distinct banks
-  for (int i = tid; i < kHsS * (kWD / 4); i += kHsThreads) {
-    const int sl = i % kHsS, d4 = i / kHsS;
-    const float4 v = sl < ns ? ldg4w(cc + (s0 + sl) * kWN + 4 * d4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    sdc[(4 * d4 + 0) * kHsPadS + sl] = v.x;
-    sdc[(4 * d4 + 1) * kHsPadS + sl] = v.y;
-    sdc[(4 * d4 + 2) * kHsPadS + sl] = v.z;
-    sdc[(4 * d4 + 3) * kHsPadS + sl] = v.w;
-  }
-  for (int i = tid; i < kHsJ * (kWD / 4); i += kHsThreads) {
-    const int jl = i % kHsJ, d4 = i / kHsJ;
-    const float4 v = ldg4w(W_C + static_cast<size_t>(j0 + jl) * kWD + 4 * d4);
-    swc[(4 * d4 + 0) * kHsPadJ + jl] = v.x;
-    swc[(4 * d4 + 1) * kHsPadJ + jl] = v.y;
-    swc[(4 * d4 + 2) * kHsPadJ + jl] = v.z;
-    swc[(4 * d4 + 3) * kHsPadJ + jl] = v.w;
-  }
-  // this thread's outputs start from dY: samples 4 sg .. 4 sg + 3, columns
-  // 4 cg .. 4 cg + 3 (a warp reads a 256-byte row piece of two samples)
+  // this thread's outputs start from dY: samples 8 sg .. 8 sg + 7, columns
+  // 4 cg .. 4 cg + 3 and 64 + 4 cg .. 64 + 4 cg + 3 (a warp reads two 256-byte
+  // row pieces of two samples); requested first, their latency runs under
+  // the staging below
   const int cg = tid & 15, sg = tid >> 4;
-  float o[4][4];
+  float o[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int sl = 4 * sg + i;
-    const float4 a0 = sl < ns ? ldg4w(g + (s0 + sl) * SH2 + j0 + 4 * cg) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < 8; ++i) {
+    const int sl = 8 * sg + i;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    if (sl < ns) {
+      const float* gp = g + (s0 + sl) * SH2 + j0 + 4 * cg;
+      a0 = ldg4w(gp);
+      a1 = ldg4w(gp + kHsJ / 2);
+    }
     o[i][0] = a0.x; o[i][1] = a0.y; o[i][2] = a0.z; o[i][3] = a0.w;
+    o[i][4] = a1.x; o[i][5] = a1.y; o[i][6] = a1.z; o[i][7] = a1.w;
+  }
+  // staging: consecutive threads take consecutive samples (or columns), so
+  // the transposed stores fall in distinct banks; each pass issues all its
+  // loads before its first store
+  constexpr int kPer = kHsS * (kWD / 4) / kHsThreads;  // float4 per thread and matrix
+  static_assert(kHsS == kHsJ && kPer * kHsThreads == kHsS * (kWD / 4), "staging split");
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    float4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + u * kHsThreads, r = i % kHsS, d4 = i / kHsS;
+      if (m == 0)
+        v[u] = r < ns ? ldg4w(cc + (s0 + r) * kWN + 4 * d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        v[u] = ldg4w(W_C + static_cast<size_t>(j0 + r) * kWD + 4 * d4);
+    }
+    float* dst = m == 0 ? sdc : swc;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + u * kHsThreads, r = i % kHsS, d4 = i / kHsS;
+      dst[(4 * d4 + 0) * kHsPadS + r] = v[u].x;
+      dst[(4 * d4 + 1) * kHsPadS + r] = v[u].y;
+      dst[(4 * d4 + 2) * kHsPadS + r] = v[u].z;
+      dst[(4 * d4 + 3) * kHsPadS + r] = v[u].w;
+    }
   }
   __syncthreads();
-#pragma unroll 8
+#pragma unroll 2
   for (int d = 0; d < kWD; ++d) {
-    const float4 x = *reinterpret_cast<const float4*>(sdc + d * kHsPadS + 4 * sg);
-    const float4 w = *reinterpret_cast<const float4*>(swc + d * kHsPadJ + 4 * cg);
-    const float xs[4] = {x.x, x.y, x.z, x.w};
-    const float ws[4] = {w.x, w.y, w.z, w.w};
+    const float4 x0 = *reinterpret_cast<const float4*>(sdc + d * kHsPadS + 8 * sg);
+    const float4 x1 = *reinterpret_cast<const float4*>(sdc + d * kHsPadS + 8 * sg + 4);
+    const float4 w0 = *reinterpret_cast<const float4*>(swc + d * kHsPadJ + 4 * cg);
+    const float4 w1 = *reinterpret_cast<const float4*>(swc + d * kHsPadJ + kHsJ / 2 + 4 * cg);
+    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const float ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) o[i][c] = fmaf(xs[i], ws[c], o[i][c]);
+      for (int c = 0; c < 8; ++c) o[i][c] = fmaf(xs[i], ws[c], o[i][c]);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int sl = 4 * sg + i;
-    if (sl < ns)
-      *reinterpret_cast<float4*>(out + (s0 + sl) * SH2 + j0 + 4 * cg) =
-          make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+  for (int i = 0; i < 8; ++i) {
+    const int sl = 8 * sg + i;
+    if (sl < ns) {
+      float* op = out + (s0 + sl) * SH2 + j0 + 4 * cg;
+      *reinterpret_cast<float4*>(op) = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+      *reinterpret_cast<float4*>(op + kHsJ / 2) = make_float4(o[i][4], o[i][5], o[i][6], o[i][7]);
+    }
   }
 }
 
@@ -992,7 +1015,7 @@ cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const flo
   if (e != cudaSuccess) return e;
   ++*n;
   const dim3 hs_grid(static_cast<unsigned>((B + kHsS - 1) / kHsS), static_cast<unsigned>(SH2 / kHsJ));
-  wide_dhs2_kernel<<<hs_grid, kHsThreads, 0, stream>>>(g, cc, W_C, d_h_s2, B, SH2);
+  wide_dhs2_kernel<<<hs_grid, kHsThreads, kHsSmem, stream>>>(g, cc, W_C, d_h_s2, B, SH2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n;
   WideDwArgs dw{};
@@ -1029,6 +1052,9 @@ cudaError_t prepare_wide_kernels() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(wide_tc_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kDwSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(wide_dhs2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kHsSmem));
   return e;
 }
 
