@@ -13,12 +13,12 @@
 // swizzle with 32-byte atoms, as TMA lays them out) and the weight-gradient
 // products read h_history, h_s2, dY, dA|dB and [dC | ctx] MN-major too.
 //
-//   wide_tc_kernel<false>  forward, per 128-row tile (S = 128 / K samples,
+//   wide_tc_kernel<false, KPP>  forward, per 128-row tile (S = 128 / K samples,
 //       S <= 16): A|B = h_history . [W_A|W_B] on the tensor cores (32-column
 //       chunks of SH2 through a ring of two stages); C = h_s2 . W_C on the FMA
 //       pipe during the chunks; the scan x_t = sigmoid(A_t) x_{t-1} + B_t,
 //       ctx = C x_{K-1} and h_enriched = h_s2 + tw ctx . W_O.
-//   wide_tc_kernel<true>   backward, per tile: the same projections and
+//   wide_tc_kernel<true, KPP>   backward, per tile: the same projections and
 //       d_ctx = tw dY . W_O^T; replay and reverse scan (dB_t = dx, dA_t =
 //       dx x_{t-1} sigmoid'(A_t), dx <- dx sigmoid(A_t)); dA|dB split into tf32
 //       part and remainder in TMEM (A operand) for d_h_history =
@@ -200,7 +200,10 @@ struct Ring {
   }
 };
 
-template <bool BWD>
+// KPP: chunk columns per thread in the C / d_ctx dots, fixed by the samples
+// per tile (S_max > 8: 8; S_max > 4: 4; else 2), so that the per-thread
+// weight arrays are exactly as large as they are used.
+template <bool BWD, int KPP>
 __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_constant__ WideTcArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -361,8 +364,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     const float gsc = load_gate_scale(a.gate_scale);
     // C / d_ctx partial dots: thread = (state quad dq, sample quad sq, k part kp)
-    const int NSQ = S_max > 8 ? 4 : (S_max > 4 ? 2 : 1);
-    const int NKP = 16 / NSQ, KPP = 32 / NKP;
+    constexpr int NKP = 32 / KPP, NSQ = 16 / NKP;
     const int dq = tid & 15, sq = (tid >> 4) % NSQ, kp = (tid >> 4) / NSQ;
     Ring r;
     int lt = 0, cq = 0;     // cq: stages consumed (the remainder buffer is cq & 1)
@@ -387,30 +389,28 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
       // W_C (and W_O) values of chunk q for this thread's dots; those of
       // chunk q + 1 are loaded as soon as chunk q's dots have used them, so
       // their latency runs under the next chunk's wait and remainder work
-      float4 wcr[8], wor[8];
+      float4 wcr[KPP], wor[KPP];
       auto load_chunk_weights = [&](int q) {
         const int k0 = 32 * q;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          if (kk < KPP) {
-            const int k = kp * KPP + kk;
-            wcr[kk] = ldg4w(a.W_C + static_cast<size_t>(k0 + k) * kWD + 4 * dq);
-          }
+        for (int kk = 0; kk < KPP; ++kk) {
+          const int k = kp * KPP + kk;
+          wcr[kk] = ldg4w(a.W_C + static_cast<size_t>(k0 + k) * kWD + 4 * dq);
+        }
         if (BWD) {
           // W_O rows 4 dq .. 4 dq + 3 over this thread's KPP consecutive
           // columns: 16-byte loads along each row (8-byte when KPP = 2), then
           // regrouped by column
-          float ow[4][8];
+          float ow[4][KPP];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float* rowp = a.W_O + static_cast<size_t>(4 * dq + i) * SH2 + k0 + kp * KPP;
-            if (KPP >= 4) {
+            if constexpr (KPP >= 4) {
 #pragma unroll
-              for (int c = 0; c < 8; c += 4)
-                if (c < KPP) {
-                  const float4 v = ldg4w(rowp + c);
-                  ow[i][c] = v.x; ow[i][c + 1] = v.y; ow[i][c + 2] = v.z; ow[i][c + 3] = v.w;
-                }
+              for (int c = 0; c < KPP; c += 4) {
+                const float4 v = ldg4w(rowp + c);
+                ow[i][c] = v.x; ow[i][c + 1] = v.y; ow[i][c + 2] = v.z; ow[i][c + 3] = v.w;
+              }
             } else {
               const float2 v = __ldg(reinterpret_cast<const float2*>(rowp));
               ow[i][0] = v.x;
@@ -418,13 +418,11 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
             }
           }
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            if (kk < KPP) wor[kk] = make_float4(ow[0][kk], ow[1][kk], ow[2][kk], ow[3][kk]);
+          for (int kk = 0; kk < KPP; ++kk) wor[kk] = make_float4(ow[0][kk], ow[1][kk], ow[2][kk], ow[3][kk]);
         }
       };
-      if (!BWD) load_chunk_weights(0);
+      load_chunk_weights(0);
       for (int q = 0; q < NQ; ++q) {
-        if (BWD) load_chunk_weights(q);
         bounded_wait(&bb->full[r.i], r.ph, a.err);
         float* sp = reinterpret_cast<float*>(base + r.i * kStage);
         float* lo = lo_buffer();
@@ -433,8 +431,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
           const float* hs = sp + 2 * kBox / 4;
           const float* gv = hs + 512;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            if (kk >= KPP) break;
+          for (int kk = 0; kk < KPP; ++kk) {
             const int k = kp * KPP + kk;
             const float w4[4] = {wcr[kk].x, wcr[kk].y, wcr[kk].z, wcr[kk].w};
             const float o4[4] = {wor[kk].x, wor[kk].y, wor[kk].z, wor[kk].w};
@@ -452,7 +449,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
             }
           }
         }
-        if (!BWD && q + 1 < NQ) load_chunk_weights(q + 1);
+        if (q + 1 < NQ) load_chunk_weights(q + 1);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bb->split[r.i]);
@@ -972,6 +969,18 @@ static bool wide_tile_maps(WideTcArgs* w, const float* h_history, const float* h
   return true;
 }
 
+// Chunk columns per thread of the C / d_ctx dots for S_max samples per tile.
+static int wide_kpp(int S_max) { return S_max > 8 ? 8 : (S_max > 4 ? 4 : 2); }
+
+template <bool BWD>
+static void launch_wide_tile(const WideTcArgs& w, int grid, cudaStream_t stream) {
+  switch (wide_kpp(w.S_max)) {
+    case 8: wide_tc_kernel<BWD, 8><<<grid, kTileThreads, kTileSmem, stream>>>(w); break;
+    case 4: wide_tc_kernel<BWD, 4><<<grid, kTileThreads, kTileSmem, stream>>>(w); break;
+    default: wide_tc_kernel<BWD, 2><<<grid, kTileThreads, kTileSmem, stream>>>(w); break;
+  }
+}
+
 static int wide_grid(int64_t B, int S_max) {
   const long long n_tiles = (B + S_max - 1) / S_max;
   return static_cast<int>(n_tiles < kMaxSlots ? n_tiles : kMaxSlots);
@@ -986,7 +995,7 @@ cudaError_t launch_wide_fwd(const float* h_history, const float* h_s2, const flo
   if (!wide_tile_maps(&w, h_history, h_s2, nullptr, W_A, W_B, B, K, SH2)) return cudaErrorInvalidValue;
   w.h_s2 = h_s2; w.W_C = W_C; w.W_O = W_O; w.out0 = h_enriched;
   w.gate_scale = gate_scale; w.err = err; w.B = B; w.K = K; w.SH2 = SH2; w.tw = tw;
-  wide_tc_kernel<false><<<wide_grid(B, w.S_max), kTileThreads, kTileSmem, stream>>>(w);
+  launch_wide_tile<false>(w, wide_grid(B, w.S_max), stream);
   return cudaGetLastError();
 }
 
@@ -1010,7 +1019,7 @@ cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const flo
   w.h_s2 = h_s2; w.W_C = W_C; w.W_O = W_O; w.out0 = d_h_history;
   w.dab = dab; w.cc = cc; w.gate_scale = gate_scale; w.err = err;
   w.B = B; w.K = K; w.SH2 = SH2; w.tw = tw;
-  wide_tc_kernel<true><<<wide_grid(B, w.S_max), kTileThreads, kTileSmem, stream>>>(w);
+  launch_wide_tile<true>(w, wide_grid(B, w.S_max), stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*n;
@@ -1044,11 +1053,14 @@ cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const flo
 }
 
 cudaError_t prepare_wide_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(wide_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kTileSmem));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(wide_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kTileSmem));
+  const void* tiles[] = {
+      reinterpret_cast<const void*>(wide_tc_kernel<false, 2>), reinterpret_cast<const void*>(wide_tc_kernel<false, 4>),
+      reinterpret_cast<const void*>(wide_tc_kernel<false, 8>), reinterpret_cast<const void*>(wide_tc_kernel<true, 2>),
+      reinterpret_cast<const void*>(wide_tc_kernel<true, 4>), reinterpret_cast<const void*>(wide_tc_kernel<true, 8>)};
+  cudaError_t e = cudaSuccess;
+  for (const void* k : tiles)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kTileSmem));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(wide_tc_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kDwSmem));
