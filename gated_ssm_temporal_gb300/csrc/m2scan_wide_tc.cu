@@ -769,8 +769,14 @@ __global__ void __launch_bounds__(kDwThreads, 1) wide_tc_dw_kernel(const __grid_
         }
         named_sync(1, kDwCW * 32);
       }
-      split_buf(sp, sp + kBox / 4, kBox / 16, ct, kDwCW * 32, true);
-      split_buf(sp + 2 * kBox / 4, sp + 2 * kBox / 4 + 1024 * NA, NA * 256, ct, kDwCW * 32, true);
+      if (NA == 4) {
+        // both operands are full [128 x 128 B] boxes: every load of a thread
+        // is issued before its first store
+        split_two_boxes<kDwCW * 32>(sp, sp + kBox / 4, sp + 2 * kBox / 4, sp + 3 * kBox / 4, ct);
+      } else {
+        split_buf(sp, sp + kBox / 4, kBox / 16, ct, kDwCW * 32, true);
+        split_buf(sp + 2 * kBox / 4, sp + 2 * kBox / 4 + 1024 * NA, NA * 256, ct, kDwCW * 32, true);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bb->split[r.i]);
