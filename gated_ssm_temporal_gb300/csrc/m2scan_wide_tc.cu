@@ -580,11 +580,25 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
           float w[kWD];
 #pragma unroll
           for (int d = 0; d < kWD; ++d) w[d] = __ldg(a.W_O + static_cast<size_t>(d) * SH2 + j);
-          for (int s = 0; s < S_t; ++s) {
-            float o = 0.f;
+          // four samples per step: s is a multiple of 4, their sX values in
+          // one 16-byte read per state (entries past S_t read, not stored)
+          for (int s = 0; s < S_t; s += 4) {
+            const int ns = min(4, S_t - s);
+            float hs[4];
 #pragma unroll
-            for (int d = 0; d < kWD; ++d) o = fmaf(sX[d * kWSmax + s], w[d], o);
-            a.out0[(b0 + s) * SH2 + j] = fmaf(a.tw, o, __ldg(a.h_s2 + (b0 + s) * SH2 + j));
+            for (int u = 0; u < 4; ++u) hs[u] = u < ns ? __ldg(a.h_s2 + (b0 + s + u) * SH2 + j) : 0.f;
+            float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int d = 0; d < kWD; ++d) {
+              const float4 x = *reinterpret_cast<const float4*>(sX + d * kWSmax + s);
+              o[0] = fmaf(x.x, w[d], o[0]);
+              o[1] = fmaf(x.y, w[d], o[1]);
+              o[2] = fmaf(x.z, w[d], o[2]);
+              o[3] = fmaf(x.w, w[d], o[3]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (u < ns) a.out0[(b0 + s + u) * SH2 + j] = fmaf(a.tw, o[u], hs[u]);
           }
         }
       } else {
