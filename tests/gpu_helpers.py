@@ -62,8 +62,8 @@ def shape_of(x):
 
 
 def runs_wide(x, force_generic=False):
-    """Whether the backward of these shapes runs the wide-state family (38
-    sample ranges for the weight gradients instead of 152 slots)."""
+    """Whether the backward of these shapes runs the wide-state family (its
+    own sample ranges for the weight gradients, as many as the slots)."""
     ensure_built()
     B, K, SH2, D = shape_of(x)
     return not force_generic and g.m2scan_path_for(K, SH2, D) == 3

@@ -57,12 +57,15 @@ def test_tensor_core_multi_tile_shapes(B, K, SH2):
     check(custom(B, K, SH2, 16, seed=B + K + SH2, wa_scale=2.0))
 
 
+# samples per tile 16, 8, 6, 4 and 1 cover the three dot layouts of the
+# wide-state tile kernels (8, 4 and 2 chunk columns per thread)
 @pytest.mark.parametrize("B,K,SH2", [
-    (1, 1, 128), (5, 16, 512), (37, 3, 128), (1000, 7, 384), (300, 128, 256), (2047, 16, 512)])
+    (1, 1, 128), (5, 16, 512), (37, 3, 128), (1000, 7, 384), (300, 128, 256), (2047, 16, 512),
+    (700, 20, 128), (333, 32, 256)])
 def test_wide_state_shapes(B, K, SH2):
-    # D = 64 runs the wide-state FP32 kernels: 128-row tiles of up to 16
-    # samples, a partial last tile, and up to 38 sample ranges for the dW
-    # products (fewer when B < 38)
+    # D = 64 runs the wide-state tensor-core kernels: 128-row tiles of up to
+    # 16 samples, a partial last tile, and up to 152 sample ranges for the dW
+    # products (fewer when B < 152)
     import gated_ssm_temporal_gb300 as g
     ensure_built()
     assert g.m2scan_path_for(K, SH2, 64) == 3

@@ -71,8 +71,8 @@ def term_budget(K, SH2):
 
 def chain_length(name, B, K, SH2, D, wide=False):
     """L: the longest chain of fp32 roundings from a term of output ``name`` to
-    its result, for any kernel family (``wide``: the wide-state family's 38
-    sample ranges in place of 152 slots)."""
+    its result, for any kernel family (``wide``: the wide-state family's
+    sample ranges in place of the slots; both number 152)."""
     if name in ("h_enriched", "d_h_s2"):
         return D + 2
     if name == "d_h_history":
