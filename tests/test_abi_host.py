@@ -76,7 +76,7 @@ def test_workspace_query(probe):
     assert probe["ws_bytes_small_B"] == 3 * 4 * 256 * 16 * 4
     assert probe["ws_bytes_B0"] == 0
     assert probe["ws_bytes_bad"] == 0
-dB [B*K][128] and [dC | ctx] [B][128]|dB [B*K][128] and [dC | ctx] [B][128]
+    # wide states: 152 sample-range slots plus dA|dB [B*K][128] and [dC | ctx] [B][128]
     assert probe["ws_bytes_wide"] == (152 * 4 * 512 * 64 + 16384 * 16 * 128 + 16384 * 128) * 4
 
 
