@@ -15,7 +15,7 @@
 //
 //   wide_tc_kernel<false, KPP>  forward, per 128-row tile (S = 128 / K samples,
 //       S <= 16): A|B = h_history . [W_A|W_B] on the tensor cores (32-column
-//       chunks of SH2 through a ring of two stages); C = h_s2 . W_C on the FMA
+//       chunks of SH2 through a ring of four stages); C = h_s2 . W_C on the FMA
 //       pipe during the chunks; the scan x_t = sigmoid(A_t) x_{t-1} + B_t,
 //       ctx = C x_{K-1} and h_enriched = h_s2 + tw ctx . W_O.
 //   wide_tc_kernel<true, KPP>   backward, per tile: the same projections and
