@@ -40,7 +40,9 @@ constexpr int kBfN = 64;       // MMA N: [W1_A | W1_B | W2_A | W2_B], 16 columns
 constexpr uint32_t kBfSetCols = 64;
 
 struct BfBars {
-  uint64_t full[kBfStages];     // producer -> all: stage loaded
+  uint64_t full[kBfStages];     // producer -> MMA, compute: chunk loaded into stage s
+  uint64_t fullo[kBfStages];    // producer -> compute: h_s2 rows loaded into stage s (the MMA
+                                // thread skips these items, so they have a barrier of their own)
   uint64_t empty[kBfStages];    // chunk stage free: MMA commit + one arrival per compute warp
   uint64_t outdone[kBfStages];  // compute -> producer: h_s2 item read (one arrival per warp)
   uint64_t mdone[2];            // MMA -> compute: tile t's products (set t & 1) done
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(kBfThreads, 1) fwd_bf16_kernel(const __grid_co
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_hs)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
+      mbar_init(&bb->fullo[s], 1);
       mbar_init(&bb->empty[s], 1 + kBfComputeWarps);
       mbar_init(&bb->outdone[s], kBfComputeWarps);
     }
@@ -152,8 +155,9 @@ __global__ void __launch_bounds__(kBfThreads, 1) fwd_bf16_kernel(const __grid_co
   auto produce_one = [&]() {
     if (pn >= NST) release_one();
     unsigned char* sp = stage_ptr(lp.i);
-    uint64_t* bar = &bb->full[lp.i];
-    if (pit < (pround < T ? NC : 0)) {
+    const bool chunk = pit < (pround < T ? NC : 0);
+    uint64_t* bar = chunk ? &bb->full[lp.i] : &bb->fullo[lp.i];
+    if (chunk) {
       const long long tb0 = tile_start(pround);
       mbar_arrive_expect_tx(bar, a.hc_bytes + a.sc_bytes);
       tma_load_3d(sp, &a.tm_h, pit * kBfChunk, 0, static_cast<int>(tb0), bar);
@@ -242,12 +246,14 @@ __global__ void __launch_bounds__(kBfThreads, 1) fwd_bf16_kernel(const __grid_co
       const uint32_t ring = smem_addr(base);
       const uint32_t w0 = smem_addr(sW);
       BfPos tp;
+      uint32_t fph = 0;  // bit s: parity of the next full[s] phase (chunks only)
       for (int t = 0; t < T; ++t) {
         if (t >= 2) bounded_wait(&bb->accempty[t & 1], ((t - 2) >> 1) & 1, a.err);
         const uint32_t acc = tmem + kBfSetCols * static_cast<uint32_t>(t & 1);
         BfPos pm = tp;
         for (int q = 0; q < NC; ++q) {
-          bounded_wait(&bb->full[pm.i], pm.ph, a.err);
+          bounded_wait(&bb->full[pm.i], (fph >> pm.i) & 1u, a.err);
+          fph ^= 1u << pm.i;
           tc_fence_after();
           const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
           const uint64_t bd = umma_desc_sw128(w0 + static_cast<uint32_t>(q * kBfN * 128));
@@ -272,10 +278,12 @@ __global__ void __launch_bounds__(kBfThreads, 1) fwd_bf16_kernel(const __grid_co
     // 8 columns of each chunk
     const int sd_jo = tid & 7, sd_sp = (tid >> 3) & 7, sd_dq = tid >> 6;
     BfPos ip;
+    uint32_t cph = 0, oph = 0;  // bit s: parity of the next full[s] / fullo[s] phase
     auto output_tile = [&](int tt) {
       const long long tb0 = tile_start(tt);
       const int S_t = static_cast<int>(tile_start(tt + 1) - tb0);
-      bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+      bounded_wait(&bb->fullo[ip.i], (oph >> ip.i) & 1u, a.err);
+      oph ^= 1u << ip.i;
       const unsigned char* hs = stage_ptr(ip.i);
       const int st = ip.i;
       ip.next(NST);
@@ -341,7 +349,8 @@ __global__ void __launch_bounds__(kBfThreads, 1) fwd_bf16_kernel(const __grid_co
           w[e][0] = lds4(wp);
           w[e][1] = lds4(wp + 4);
         }
-        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        bounded_wait(&bb->full[ip.i], (cph >> ip.i) & 1u, a.err);
+        cph ^= 1u << ip.i;
         const unsigned char* sp = stage_ptr(ip.i);
         // all 16 rows of the box even past S_max: the reads stay inside shared
         // memory and the sums of missing samples are never stored

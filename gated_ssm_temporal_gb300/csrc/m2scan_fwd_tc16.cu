@@ -39,7 +39,9 @@ constexpr int kLoBufs = 3;
 // commit stalls only the stream of the thread that issues it, so the main
 // and the remainder products of a chunk overlap each other's stalls.
 struct FwdBars {
-  uint64_t full[kMaxStages];     // producer -> all: stage loaded
+  uint64_t full[kMaxStages];     // producer -> MMA, compute: chunk loaded into stage s
+  uint64_t fullo[kMaxStages];    // producer -> compute: h_s2 rows loaded into stage s (the MMA
+                                 // threads skip these items, so they have a barrier of their own)
   uint64_t empty[kMaxStages];    // chunk stage s free: main products done (commit) + compute read (arrive)
   uint64_t outdone[kMaxStages];  // compute -> producer: h_s2 item in stage s read (one arrival per warp)
   uint64_t loready[kChunkRing];  // compute -> remainder MMA thread: chunk c read, h - trunc(h) in TMEM
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm_hs)) : "memory");
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bb->full[s], 1);
+      mbar_init(&bb->fullo[s], 1);
       mbar_init(&bb->empty[s], 2);
       mbar_init(&bb->outdone[s], kComputeWarps);
     }
@@ -152,8 +155,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
   auto produce_one = [&]() {
     if (pn >= NST) release_one();
     unsigned char* sp = stage_ptr(lp.i);
-    uint64_t* bar = &bb->full[lp.i];
-    if (pit < (pround < T ? NC : 0)) {
+    const bool chunk = pit < (pround < T ? NC : 0);
+    uint64_t* bar = chunk ? &bb->full[lp.i] : &bb->fullo[lp.i];
+    if (chunk) {
       const long long tb0 = tile_start(pround);
       mbar_arrive_expect_tx(bar, a.hc_bytes + a.sc_bytes);
       tma_load_3d(sp, &a.tm_h, pit * kChunk, 0, static_cast<int>(tb0), bar);
@@ -239,13 +243,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       const uint32_t ring = smem_addr(base);
       const uint32_t w0 = smem_addr(sW);
       RingPos tp;
+      uint32_t fph = 0;  // bit s: parity of the next full[s] phase (chunks only)
       for (int t = 0; t < T; ++t) {
         // the set's previous tile (t - 2) has been read back
         if (t >= 2) bounded_wait(&bb->accempty[t & 1], ((t - 2) >> 1) & 1, a.err);
         const uint32_t acc = tmem + kSetCols * static_cast<uint32_t>(t & 1);
         RingPos pm = tp;
         for (int qm = 0; qm < NC; ++qm) {
-          bounded_wait(&bb->full[pm.i], pm.ph, a.err);
+          bounded_wait(&bb->full[pm.i], (fph >> pm.i) & 1u, a.err);
+          fph ^= 1u << pm.i;
           tc_fence_after();
           TRACE_AT(2, 600 + qm);
           const uint64_t ad = umma_desc_sw128(ring + static_cast<uint32_t>(pm.i) * stage_bytes);
@@ -310,6 +316,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
 #pragma unroll
     for (int v = 0; v < 4; ++v) lo_off[v] = row * 32 + (((4 * sub + v) ^ (row & 7)) << 2);
     RingPos ip, lr, lf;
+    uint32_t cph = 0, oph = 0;  // bit s: parity of the next full[s] / fullo[s] phase
     int c = 0;
     PROF_DECL;
     // ====== output of tile tt: h_enriched = h_s2 + tw ctx . W_O from its h_s2
@@ -319,7 +326,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       const int S_t = static_cast<int>(tile_start(tt + 1) - tile_start(tt));
       {
         PROF_BEGIN();
-        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        bounded_wait(&bb->fullo[ip.i], (oph >> ip.i) & 1u, a.err);
+        oph ^= 1u << ip.i;
         PROF_END(9);
         PROF_BEGIN();
         float* hs = reinterpret_cast<float*>(stage_ptr(ip.i));
@@ -387,7 +395,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
         for (int e = 0; e < 4; ++e) w[e] = lds4(sd_w + e * SH2 + q * kChunk);
         PROF_BEGIN();
         if (tid == 0) TRACE_AT(0, 10);
-        bounded_wait(&bb->full[ip.i], ip.ph, a.err);
+        bounded_wait(&bb->full[ip.i], (cph >> ip.i) & 1u, a.err);
+        cph ^= 1u << ip.i;
         if (tid == 0) TRACE_AT(0, 11);
         PROF_END(0);
         PROF_BEGIN();

@@ -7,8 +7,9 @@ interleavings with asynchronous completions: TMA loads complete in any
 order, the commits of one issuing thread in issue order. The run fails on
 
 * a deadlock (no role can move and nothing is in flight),
-* parity aliasing (a waiter two phases behind its barrier, which a parity
-  wait cannot tell apart from the phase it wants),
+* parity aliasing: a waiter two phases behind its barrier, or one that
+  starts waiting for a phase two ahead of it (a parity wait cannot tell
+  either apart from the phase it wants),
 * a hazard: a stage reloaded while a role still reads it, a tensor-memory
   buffer or accumulator set written while another role reads or writes it.
 
@@ -83,6 +84,13 @@ def schedule(actors, bars, events, seed, limit=10 ** 6):
             blocked[k] = next(actors[k])
         except StopIteration:
             done.add(k)
+            continue
+        w = blocked[k]
+        if w[0] == "wait":
+            # a parity wait for phase n also passes while the barrier has
+            # completed only n - 1 phases: a waiter may start at most one
+            # phase ahead of the barrier
+            assert bars[w[1]].completed >= w[2], ("parity aliasing ahead", k, w, bars[w[1]].completed)
     else:
         raise RuntimeError("no progress within the step limit")
     assert not any(events.values()), "completions left over"
@@ -123,12 +131,16 @@ def post_item(p, NSI, NRI):
 
 def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
     """fwd_tc16_kernel: producer rounds (tile u's chunks, then tile u-1's h_s2
-    rows), a main and a remainder MMA thread, the compute warps."""
+    rows), a main and a remainder MMA thread, the compute warps. A chunk
+    signals full[s], a row item fullo[s]: the main MMA thread skips the row
+    items, and with one barrier for both its parity waits could start two
+    phases ahead."""
     S = tiles(B, P, cta, K)
     T, NC = len(S), SH2 // 32
     bars = {}
     for s in range(NST):
         bars["full%d" % s] = Bar("full", 1)
+        bars["fullo%d" % s] = Bar("fullo", 1)
         bars["empty%d" % s] = Bar("empty", 2)
         bars["outdone%d" % s] = Bar("outdone", 1)
     for s in range(kChunkRing):
@@ -158,10 +170,12 @@ def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
                 use[b][st] += 1
             st = pn % NST
             assert not st_read[st], ("stage reloaded while read", st)
-            events["tma"].append(("full%d" % st, None))
+            one = mutation == "one_full_barrier"
+            events["tma"].append((("full%d" if items[pn] == "chunk" or one else "fullo%d") % st, None))
 
     def main():
         tp = 0
+        fuse = [0] * NST
         for t in range(T):
             if t >= 2 and mutation != "no_accempty_wait":
                 yield W("accempty%d" % (t & 1), (t - 2) >> 1)
@@ -169,7 +183,8 @@ def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
             for q in range(NC):
                 it = tp + q
                 st = it % NST
-                yield W("full%d" % st, it // NST)
+                yield W("full%d" % st, it // NST if mutation == "one_full_barrier" else fuse[st])
+                fuse[st] += 1
                 st_read[st].add(("m", it))
                 acc_w[t & 1] += 1
 
@@ -202,10 +217,19 @@ def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
 
     def compute():
         seq = c = 0
+        one = mutation == "one_full_barrier"
+        cuse, ouse = [0] * NST, [0] * NST
+
+        def wait_item(kind, st):
+            if one:
+                return W("full%d" % st, seq // NST)
+            u = cuse if kind == "chunk" else ouse
+            u[st] += 1
+            return W(("full%d" if kind == "chunk" else "fullo%d") % st, u[st] - 1)
         for t in range(T):
             for q in range(NC):
                 st = seq % NST
-                yield W("full%d" % st, seq // NST)
+                yield wait_item("chunk", st)
                 st_read[st].add(("c", seq))
                 if q > 0:
                     bars["loready%d" % ((c - 1) % kChunkRing)].arrive()
@@ -219,7 +243,7 @@ def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
             st_read[(seq - 1) % NST].discard(("c", seq - 1))
             if t >= 1:
                 st = seq % NST
-                yield W("full%d" % st, seq // NST)
+                yield wait_item("out", st)
                 st_read[st].add(("o", seq))
                 yield ("yield",)
                 st_read[st].discard(("o", seq))
@@ -235,7 +259,7 @@ def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
             bars["accempty%d" % (t & 1)].arrive()
         if T:
             st = seq % NST
-            yield W("full%d" % st, seq // NST)
+            yield wait_item("out", st)
             bars["outdone%d" % st].arrive()
 
     schedule({"p": producer(), "m": main(), "r": corr(), "c": compute()}, bars, events, seed)
@@ -243,12 +267,14 @@ def fwd_tc16(B, P, cta, K, SH2, NST, seed, mutation=None):
 
 def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
     """fwd_bf16_kernel: the same rounds with 64-column chunks and one MMA
-    thread; a chunk stage is freed by the MMA commit and the compute warps."""
+    thread; a chunk stage is freed by the MMA commit and the compute warps.
+    As in fwd_tc16, chunks signal full[s] and row items fullo[s]."""
     S = tiles(B, P, cta, K)
     T, NC = len(S), SH2 // 64
     bars = {}
     for s in range(NST):
         bars["full%d" % s] = Bar("full", 1)
+        bars["fullo%d" % s] = Bar("fullo", 1)
         bars["empty%d" % s] = Bar("empty", 2)
         bars["outdone%d" % s] = Bar("outdone", 1)
     for s in range(2):
@@ -273,10 +299,12 @@ def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
                 use[b][st] += 1
             st = pn % NST
             assert not st_read[st], ("stage reloaded while read", st)
-            events["tma"].append(("full%d" % st, None))
+            one = mutation == "one_full_barrier"
+            events["tma"].append((("full%d" if items[pn] == "chunk" or one else "fullo%d") % st, None))
 
     def mma():
         tp = 0
+        fuse = [0] * NST
         for t in range(T):
             if t >= 2 and mutation != "no_accempty_wait":
                 yield W("accempty%d" % (t & 1), (t - 2) >> 1)
@@ -284,7 +312,8 @@ def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
             for q in range(NC):
                 it = tp + q
                 st = it % NST
-                yield W("full%d" % st, it // NST)
+                yield W("full%d" % st, it // NST if mutation == "one_full_barrier" else fuse[st])
+                fuse[st] += 1
                 st_read[st].add(("m", it))
                 acc_w[t & 1] += 1
 
@@ -297,10 +326,19 @@ def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
 
     def compute():
         seq = 0
+        one = mutation == "one_full_barrier"
+        cuse, ouse = [0] * NST, [0] * NST
+
+        def wait_item(kind, st):
+            if one:
+                return W("full%d" % st, seq // NST)
+            u = cuse if kind == "chunk" else ouse
+            u[st] += 1
+            return W(("full%d" if kind == "chunk" else "fullo%d") % st, u[st] - 1)
         for t in range(T):
             for q in range(NC):
                 st = seq % NST
-                yield W("full%d" % st, seq // NST)
+                yield wait_item("chunk", st)
                 if mutation == "early_empty":
                     bars["empty%d" % st].arrive()
                 st_read[st].add(("c", seq))
@@ -311,7 +349,7 @@ def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
                 seq += 1
             if t >= 1:
                 st = seq % NST
-                yield W("full%d" % st, seq // NST)
+                yield wait_item("out", st)
                 st_read[st].add(("o", seq))
                 yield ("yield",)
                 st_read[st].discard(("o", seq))
@@ -326,7 +364,7 @@ def fwd_bf16(B, P, cta, K, SH2, NST, seed, mutation=None):
             bars["accempty%d" % (t & 1)].arrive()
         if T:
             st = seq % NST
-            yield W("full%d" % st, seq // NST)
+            yield wait_item("out", st)
             bars["outdone%d" % st].arrive()
 
     schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)

@@ -50,9 +50,11 @@ MUTATIONS = [
     ("fwd_tc16", "no_lofree_wait"),
     ("fwd_tc16", "no_last_lofree_wait"),
     ("fwd_tc16", "no_accempty_wait"),
+    ("fwd_tc16", "one_full_barrier"),
     ("fwd_bf16", "no_accempty_wait"),
     ("fwd_bf16", "no_mdone_wait"),
     ("fwd_bf16", "early_empty"),
+    ("fwd_bf16", "one_full_barrier"),
     ("bwd_tc", "no_htfree_wait"),
     ("bwd_tc", "no_dhfree1_wait"),
     ("bwd_tc", "early_row_empty"),
