@@ -85,6 +85,7 @@ constexpr uint32_t kDwSmem = kDwOffBar + 128 + 1024;
 // [B][SH2] (box 32 x S_max, 128-byte swizzle) for the C / d_ctx dots.
 struct alignas(128) WideTcArgs {
   CUtensorMap tm_h, tm_wa, tm_wb, tm_wak, tm_wbk, tm_hs, tm_g;
+  CUtensorMap tm_wal, tm_wbl;  // backward: remainders of the split weights
   const float* h_s2;
   const float* W_C;
   const float* W_O;
@@ -121,6 +122,8 @@ struct TileBars {
   uint64_t dab_ready;     // compute -> MMA: dA|dB in TMEM (backward)
   uint64_t dh_full[2];    // MMA -> compute: a d_h block done
   uint64_t dh_free[2];    // compute -> MMA: that block read back
+  uint64_t wlo_full[2];   // W remainder loader -> MMA: a chunk's W_lo in remainder buffer p (backward)
+  uint64_t tile_done;     // MMA -> W remainder loader: every product of a tile done (backward)
   uint32_t tslot;
 };
 
@@ -188,6 +191,40 @@ __device__ __forceinline__ void split_two_boxes(float* hi0, float* lo0, float* h
   }
 }
 
+// The same for one [128 x 128 B] box.
+template <int kThr>
+__device__ __forceinline__ void split_one_box(float* hi0, float* lo0, int t) {
+  constexpr int kPer = static_cast<int>(kBox / 16) / kThr;
+  static_assert(kPer * kThr == static_cast<int>(kBox / 16), "box not divisible by the thread count");
+  float4 v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) v[u] = reinterpret_cast<const float4*>(hi0)[t + u * kThr];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const float4 x = v[u];
+    const float4 h = make_float4(tf32_rn(x.x), tf32_rn(x.y), tf32_rn(x.z), tf32_rn(x.w));
+    reinterpret_cast<float4*>(hi0)[t + u * kThr] = h;
+    reinterpret_cast<float4*>(lo0)[t + u * kThr] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+  }
+}
+
+// The weights' split for the backward, written once per call: out holds
+// [W_A hi | W_A lo | W_B hi | W_B lo], n = SH2 x D floats each, hi = tf32_rn(w)
+// and lo = w - hi as the tile kernels' own split forms them.
+__global__ void __launch_bounds__(256) wide_wsplit_kernel(const float* __restrict__ W_A,
+                                                          const float* __restrict__ W_B,
+                                                          float* __restrict__ out, int n) {
+  const int n4 = n / 4;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n4; i += gridDim.x * blockDim.x) {
+    const int m = i < n4 ? 0 : 1, k = i - m * n4;
+    const float4 x = __ldg(reinterpret_cast<const float4*>(m == 0 ? W_A : W_B) + k);
+    const float4 h = make_float4(tf32_rn(x.x), tf32_rn(x.y), tf32_rn(x.z), tf32_rn(x.w));
+    float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(2 * m) * n);
+    o[k] = h;
+    o[n4 + k] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+  }
+}
+
 // Position in a ring of n barriers: index and the parity of its current use.
 struct Ring {
   int i = 0;
@@ -230,7 +267,9 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bb->dh_full[s], 1);
       mbar_init(&bb->dh_free[s], kCW);
+      mbar_init(&bb->wlo_full[s], 1);
     }
+    mbar_init(&bb->tile_done, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&bb->tslot, kCols);
@@ -281,6 +320,32 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
             }
         }
       }
+    } else if (BWD && lane == 1) {
+      // W remainder loader: the backward's weights come split (tf32 part and
+      // remainder) from the workspace; the tf32 parts travel in the stages,
+      // the remainders go straight into remainder buffer cq & 1 once the
+      // products of stage use cq - 2, which read it, are done. The first two
+      // chunks of a tile follow the previous tile's d_h stages, whose end the
+      // MMA thread signals once (tile_done); the others wait for chunk cq - 2
+      // of the same tile. So every wait starts at most one phase ahead of its
+      // barrier, and the MMA thread, which needs these copies, cannot get two
+      // phases ahead of the loader.
+      int cq = 0, lt = 0;
+      const int n_dh = 2 * (SH2 / kWN);
+      for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
+        if (lt > 0) bounded_wait(&bb->tile_done, (lt - 1) & 1, a.err);
+        for (int q = 0; q < NQ; ++q, ++cq) {
+          if (q >= 2) bounded_wait(&bb->empty[(cq - 2) % kNst], ((cq - 2) / kNst) & 1, a.err);
+          unsigned char* lo = base + kOffAB + 2 * kBox * (cq & 1) + kBox;
+          uint64_t* bar = &bb->wlo_full[cq & 1];
+          mbar_arrive_expect_tx(bar, kBox);
+          tma_load_2d(lo, &a.tm_wal, 0, 32 * q, bar);
+          tma_load_2d(lo + 4096, &a.tm_wal, 32, 32 * q, bar);
+          tma_load_2d(lo + 8192, &a.tm_wbl, 0, 32 * q, bar);
+          tma_load_2d(lo + 12288, &a.tm_wbl, 32, 32 * q, bar);
+        }
+        cq += n_dh;  // the d_h stages: their remainders come from the compute warps
+      }
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------------- MMA
@@ -290,6 +355,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
       Ring r;
       int lt = 0, cq = 0;    // cq: stages consumed (the remainder buffer is cq & 1)
       int uses[2] = {0, 0};  // d_h blocks issued into each accumulator so far
+      int wlo[2] = {0, 0};   // backward: W remainders taken from each buffer so far
       for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
         // TMEM is free again: the previous tile's projections (forward) or
         // its last d_h blocks (backward, which also means that its products
@@ -303,6 +369,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
         for (int q = 0; q < NQ; ++q) {
           bounded_wait(&bb->full[r.i], r.ph, a.err);
           bounded_wait(&bb->split[r.i], r.ph, a.err);
+          if (BWD) bounded_wait(&bb->wlo_full[cq & 1], wlo[cq & 1]++ & 1, a.err);
           tc_fence_after();
           const uint32_t st = smem_addr(base + r.i * kStage);
           const uint32_t lo = smem_addr(base + kOffAB + 2 * kBox * (cq & 1));
@@ -354,6 +421,10 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
             }
             umma_commit(&bb->dh_full[buf]);
           }
+          // lands once every product of the tile is done: the remainder
+          // loader may then fill both remainder buffers for the next tile
+          // (none after the last tile, where nobody would wait for it)
+          if (t + gridDim.x < n_tiles) umma_commit(&bb->tile_done);
         }
       }
     }
@@ -426,7 +497,10 @@ __global__ void __launch_bounds__(kTileThreads, 1) wide_tc_kernel(const __grid_c
         bounded_wait(&bb->full[r.i], r.ph, a.err);
         float* sp = reinterpret_cast<float*>(base + r.i * kStage);
         float* lo = lo_buffer();
-        split_two_boxes<kCT>(sp, lo, sp + kBox / 4, lo + kBox / 4, tid);  // h, W_A|W_B
+        if (BWD)
+          split_one_box<kCT>(sp, lo, tid);  // h (the weights arrive split)
+        else
+          split_two_boxes<kCT>(sp, lo, sp + kBox / 4, lo + kBox / 4, tid);  // h, W_A|W_B
         {
           const float* hs = sp + 2 * kBox / 4;
           const float* gv = hs + 512;
@@ -953,7 +1027,8 @@ size_t wide_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2) {
   const size_t slots = static_cast<size_t>(wide_ranges(B)) * 4 * static_cast<size_t>(SH2) * kWD;
   const size_t dab = static_cast<size_t>(B) * K * kWN;
   const size_t cc = static_cast<size_t>(B) * kWN;
-  return (slots + dab + cc) * sizeof(float);
+  const size_t wsplit = 4 * static_cast<size_t>(SH2) * kWD;  // the weights' tf32 parts and remainders
+  return (slots + dab + cc + wsplit) * sizeof(float);
 }
 
 static int wide_s_max(int K) {
@@ -1019,8 +1094,8 @@ cudaError_t launch_wide_fwd(const float* h_history, const float* h_s2, const flo
   return cudaGetLastError();
 }
 
-// The tile kernel, d_h_s2, the weight-gradient products and the slot
-// reduction: the number of launches goes to *n.
+// The weights' split, the tile kernel, d_h_s2, the weight-gradient products
+// and the slot reduction: the number of launches goes to *n.
 cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const float* W_A,
                             const float* W_B, const float* W_C, const float* W_O, float tw,
                             const float* g, int64_t B, int K, int SH2, float* d_h_history,
@@ -1036,12 +1111,29 @@ cudaError_t launch_wide_bwd(const float* h_history, const float* h_s2, const flo
   float* slots = ws;
   float* dab = ws + static_cast<size_t>(P) * 4 * static_cast<size_t>(SH2) * kWD;
   float* cc = dab + static_cast<size_t>(B) * K * kWN;
+  // the weights split once for every CTA: [W_A hi | W_A lo | W_B hi | W_B lo];
+  // the projections' B operands (MN-major) then come from these arrays
+  float* wsplit = cc + static_cast<size_t>(B) * kWN;
+  const int nw = SH2 * kWD;
+  {
+    const CUtensorMapSwizzle sw32 = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+    const cuuint64_t d[2] = {static_cast<cuuint64_t>(kWD), static_cast<cuuint64_t>(SH2)}, s[1] = {kWD * 4};
+    const cuuint32_t bm[2] = {32, 32};
+    if (encode_tensor_map(&w.tm_wa, wsplit, 2, d, s, bm, sw32) != CUDA_SUCCESS ||
+        encode_tensor_map(&w.tm_wal, wsplit + nw, 2, d, s, bm, sw32) != CUDA_SUCCESS ||
+        encode_tensor_map(&w.tm_wb, wsplit + 2 * nw, 2, d, s, bm, sw32) != CUDA_SUCCESS ||
+        encode_tensor_map(&w.tm_wbl, wsplit + 3 * nw, 2, d, s, bm, sw32) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   w.h_s2 = h_s2; w.W_C = W_C; w.W_O = W_O; w.out0 = d_h_history;
   w.dab = dab; w.cc = cc; w.gate_scale = gate_scale; w.err = err;
   w.B = B; w.K = K; w.SH2 = SH2; w.tw = tw;
-  launch_wide_tile<true>(w, wide_grid(B, w.S_max), stream);
+  wide_wsplit_kernel<<<(2 * (nw / 4) + 255) / 256, 256, 0, stream>>>(W_A, W_B, wsplit, nw);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  ++*n;
+  launch_wide_tile<true>(w, wide_grid(B, w.S_max), stream);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n;
   const dim3 hs_grid(static_cast<unsigned>((B + kHsS - 1) / kHsS), static_cast<unsigned>(SH2 / kHsJ));
   wide_dhs2_kernel<<<hs_grid, kHsThreads, kHsSmem, stream>>>(g, cc, W_C, d_h_s2, B, SH2);

@@ -108,9 +108,10 @@ size_t m2scan_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D);
  * input or output. The projections and the scan are recomputed from the
  * inputs (nothing is saved by the forward). Two kernel launches: the fused
  * backward and the fixed-order reduction of the weight-gradient slots; the
- * wide-state shapes (D = 64, SH2 % 128 == 0) take four: the tile kernel,
- * d_h_s2, the weight-gradient products and the slot reduction
- * (m2scan_last_launch_count reports the number). When B == 0 the weight
+ * wide-state shapes (D = 64, SH2 % 128 == 0) take five: the weights' split
+ * into tf32 parts and remainders, the tile kernel, d_h_s2, the
+ * weight-gradient products and the slot reduction (m2scan_last_launch_count
+ * reports the number). When B == 0 the weight
  * gradients are zero-filled with cudaMemsetAsync.
  */
 m2scan_status m2scan_bwd(const float* h_history, const float* h_s2, const float* W_A,

@@ -697,8 +697,8 @@ def wide_tiles(B, P, cta, K):
 
 def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
     """wide_tc_kernel: per tile NQ = SH2/32 chunk stages (backward: then 2 NB
-    stages of d_h weight tiles), a producer, one MMA thread and the compute
-    warps. Remainder buffer cq & 1 (shared with the A|B buffer); projections
+    stages of d_h weight tiles), a producer, one MMA thread, the compute warps
+    and (backward) the loader of the split weights' remainders. Remainder buffer cq & 1 (shared with the A|B buffer); projections
     into TMEM regions 0-3 (chunk q into q mod 4); backward: d_h blocks into
     regions 0 and 1 in turn, dA|dB in regions 2 and 3."""
     S = wide_tiles(B, P, cta, K)
@@ -712,9 +712,12 @@ def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
     for b in range(2):
         bars["dh_full%d" % b] = Bar("dh_full", 1)
         bars["dh_free%d" % b] = Bar("dh_free", 1)
+        bars["wlo_full%d" % b] = Bar("wlo_full", 1)
+    bars["tile_done"] = Bar("tile_done", 1)
     events = {"tma": [], "mma": []}
     st_read = [set() for _ in range(NST)]
     lo_read, lo_write, ab_use = [0, 0], [0, 0], [0]
+    wlo_pending = [0, 0]  # backward: W remainder copies in flight into buffer p
     tm = Tmem(4)
     per_tile = NQ + (2 * NB if bwd else 0)
 
@@ -726,9 +729,37 @@ def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
             assert not st_read[st], ("stage reloaded while read", st)
             events["tma"].append(("full%d" % st, None))
 
+    def wlo_loader():
+        # backward: the weights come split from the workspace; a chunk's W
+        # remainders are copied into remainder buffer cq & 1 once the products
+        # of stage use cq - 2 are done: for the first two chunks of a tile the
+        # previous tile's products (tile_done), for the others chunk cq - 2.
+        # "skip_dh_waits" is the form that waits on stage cq - 2 even across
+        # the d_h stages it skips.
+        cq = 0
+        for t in range(T):
+            if t > 0 and mutation not in ("no_wlo_free_wait", "skip_dh_waits"):
+                yield W("tile_done", t - 1)
+            for q in range(NQ):
+                if mutation == "skip_dh_waits":
+                    if cq >= 2:
+                        yield W("empty%d" % ((cq - 2) % NST), (cq - 2) // NST)
+                elif q >= 2 and mutation != "no_wlo_free_wait":
+                    yield W("empty%d" % ((cq - 2) % NST), (cq - 2) // NST)
+                p = cq & 1
+                assert lo_read[p] == 0 and ab_use[0] == 0, "W remainder copied while the buffer is read"
+                wlo_pending[p] += 1
+
+                def landed(p=p):
+                    wlo_pending[p] -= 1
+                events["tma"].append(("wlo_full%d" % p, landed))
+                cq += 1
+            cq += 2 * NB
+
     def mma():
         cq = 0
         uses = [0, 0]
+        wlo = [0, 0]
         for t in range(T):
             if bwd:
                 if mutation != "no_dh_free_wait":
@@ -741,6 +772,11 @@ def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
                 st = cq % NST
                 yield W("full%d" % st, cq // NST)
                 yield W("split%d" % st, cq // NST)
+                if bwd:
+                    if mutation != "no_wlo_wait":
+                        yield W("wlo_full%d" % (cq & 1), wlo[cq & 1])
+                    wlo[cq & 1] += 1
+                    assert wlo_pending[cq & 1] == 0, "W remainder read before it landed"
                 assert lo_write[cq & 1] == 0 and ab_use[0] == 0, "remainder buffer read while written"
                 st_read[st].add(("m", cq))
                 lo_read[cq & 1] += 1
@@ -778,6 +814,8 @@ def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
                     events["mma"].append(("empty%d" % st, done))
                     cq += 1
                 events["mma"].append(("dh_full%d" % b, None))
+            if t + 1 < T:  # nobody waits for the last tile's: none is issued
+                events["mma"].append(("tile_done", None))
 
     def compute():
         cq = 0
@@ -818,6 +856,7 @@ def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
                 yield W("acc_full", t)
             # partial sums of C / d_ctx, then A|B, in the buffer the remainders share
             assert lo_read == [0, 0], "A|B buffer written while remainders are read"
+            assert wlo_pending == [0, 0], "A|B buffer written while a W remainder lands"
             ab_use[0] += 1
             tm.compute([0, 1, 2, 3], False, "projections read back")
             yield ("yield",)
@@ -840,7 +879,10 @@ def wide_tc(B, P, cta, K, SH2, NST, seed, mutation=None, bwd=False):
             else:
                 ab_use[0] -= 1
 
-    schedule({"p": producer(), "m": mma(), "c": compute()}, bars, events, seed)
+    roles = {"p": producer(), "m": mma(), "c": compute()}
+    if bwd:
+        roles["w"] = wlo_loader()
+    schedule(roles, bars, events, seed)
 
 
 def wide_tc_bwd(B, P, cta, K, SH2, NST, seed, mutation=None):

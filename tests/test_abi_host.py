@@ -76,8 +76,9 @@ def test_workspace_query(probe):
     assert probe["ws_bytes_small_B"] == 3 * 4 * 256 * 16 * 4
     assert probe["ws_bytes_B0"] == 0
     assert probe["ws_bytes_bad"] == 0
-    # wide states: 152 sample-range slots plus dA|dB [B*K][128] and [dC | ctx] [B][128]
-    assert probe["ws_bytes_wide"] == (152 * 4 * 512 * 64 + 16384 * 16 * 128 + 16384 * 128) * 4
+    # wide states: 152 sample-range slots, dA|dB [B*K][128], [dC | ctx] [B][128]
+    # and the split weights (tf32 parts and remainders of W_A and W_B)
+    assert probe["ws_bytes_wide"] == (152 * 4 * 512 * 64 + 16384 * 16 * 128 + 16384 * 128 + 4 * 512 * 64) * 4
 
 
 def test_bias_grad_workspace_query(probe):

@@ -215,10 +215,11 @@ def test_launch_counts():
     assert g.m2scan_last_launch_count() == 1
     run_bwd(d)
     assert g.m2scan_last_launch_count() == 2
-    # wide-state family: tile kernel, d_h_s2, weight-gradient products, slot sum
+    # wide-state family: the weights' split, tile kernel, d_h_s2,
+    # weight-gradient products, slot sum
     d = to_dev(custom(70, 4, 256, 64, seed=2))
     run_bwd(d)
-    assert g.m2scan_last_launch_count() == 4
+    assert g.m2scan_last_launch_count() == 5
 
 
 def test_no_device_wait_timeouts():

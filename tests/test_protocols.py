@@ -67,6 +67,9 @@ MUTATIONS = [
     ("wide_tc_bwd", "no_lo_wait"),
     ("wide_tc_bwd", "early_split"),
     ("wide_tc_bwd", "no_dh_full_wait"),
+    ("wide_tc_bwd", "no_wlo_wait"),
+    ("wide_tc_bwd", "no_wlo_free_wait"),
+    ("wide_tc_bwd", "skip_dh_waits"),
     ("wide_tc_dw", "no_split_wait"),
     ("wide_tc_dw", "early_split"),
     ("wide_tc_dw", "no_done_wait"),
