@@ -479,8 +479,7 @@ def run_native(args, rank, world, local):
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
         "data": "synthetic",
-        "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g per rank" % (w.name, B, K, SH2, D,
-                                                                             w.tw),
+        "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g" % (w.name, B, K, SH2, D, w.tw),
                    "B": B, "K": K, "SH2": SH2, "D": D, "parallelism": "replicas x%d" % world,
                    "activations": args.dtype,
                    "arithmetic": ("bf16 tensor-core operands (exact products), fp32 sums"
@@ -671,7 +670,7 @@ def run_bias_native(args, rank, world, local):
         "metric": bias_metric(w), "value": value, "unit": "GB/s", "n_gpus": world, "steps": n,
         "warmup": max(3, args.warmup), "ms_per_step": t_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "%s: N=%d C=%d per rank" % (w.name, N, C), "N": N, "C": C,
+        "config": {"workload": "%s: N=%d C=%d" % (w.name, N, C), "N": N, "C": C,
                    "parallelism": "replicas x%d" % world,
                    "l2": L2_NOTE},
         "roofline": {"kernel": "m2scan_bias_grad (partial sums + ordered final sum)",
