@@ -1,6 +1,6 @@
 // Backward of the gated temporal scan layer with its three large contractions
 // on the tensor cores, warp-specialised (D = 16, SH2 % 32 == 0, SH2 <= 256,
-// K <= 128).
+// K <= 128; D = 4 and 8 run with their states zero-padded to 16).
 //
 // One persistent CTA per weight-gradient slot walks its samples in tiles of at
 // most 128 rows (S samples x K). Per tile:
@@ -136,8 +136,12 @@ __device__ __forceinline__ void post_item(int p, int NSI, int NRI, int& kind, in
   idx = 4 + (p - s1);
 }
 
+// DR: the layer's states (4, 8 or 16; a compile-time constant, so that the
+// D = 16 kernel is exactly the unpadded one).
+template <int DR>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_constant__ FastArgs a) {
-  constexpr int D = 16, TD = 32, FD = 64;
+  constexpr int D = 16, TD = 32, FD = 64;  // states inside the kernel
+  constexpr int Dr = DR;  // the layer's states; the others have zero weights
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   float* sW = reinterpret_cast<float*>(base + a.off_wt);       // NC tiles [FD][32], swizzled
@@ -293,11 +297,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float* src = (q < 4 ? a.W_A : a.W_B) + wj * D + 4 * (q & 3);
-        wr[q] = wok ? __ldg(reinterpret_cast<const float4*>(src)) : z;
+        const float* src = (q < 4 ? a.W_A : a.W_B) + wj * Dr + 4 * (q & 3);
+        wr[q] = wok && 4 * (q & 3) < Dr ? __ldg(reinterpret_cast<const float4*>(src)) : z;
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) wcr[q] = wok ? __ldg(reinterpret_cast<const float4*>(a.W_C + wj * D + 4 * q)) : z;
+      for (int q = 0; q < 4; ++q)
+        wcr[q] = wok && 4 * q < Dr ? __ldg(reinterpret_cast<const float4*>(a.W_C + wj * Dr + 4 * q)) : z;
     }
     // the first stages are requested after the weights, so that the weight
     // loads are not queued behind them
@@ -496,7 +501,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
     // samples of a tile; role 0 sums h_s2 . W_C, role 1 dY . W_O^T
     const int sd_jq = tid & 7, sd_d = (tid >> 3) & 15, sd_role = tid >> 7;
     const int sd_box = sd_role == 0 ? a.off_S : a.off_G;  // bytes from the stage
-    const float* sd_w = sd_role == 0 ? sW_Ct + sd_d * SH2 + 4 * sd_jq : a.W_O + sd_d * SH2 + 4 * sd_jq;
+    // (a padded state's W_O row is zero: it is not read)
+    const bool sd_wok = sd_role == 0 || sd_d < Dr;
+    const float* sd_w = sd_role == 0 ? sW_Ct + sd_d * SH2 + 4 * sd_jq : a.W_O + (sd_wok ? sd_d : 0) * SH2 + 4 * sd_jq;
     // h of this thread in a chunk: its row, columns 16 sub .. 16 sub + 15
     int lo_off[4];
 #pragma unroll
@@ -536,7 +543,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       RingPos lr_prev = lr;
       for (int q = 0; q < NC; ++q, ++c) {
         const float4 w = sd_role == 0 ? lds4(sd_w + q * kChunk)
-                                      : __ldg(reinterpret_cast<const float4*>(sd_w + q * kChunk));
+                         : sd_wok   ? __ldg(reinterpret_cast<const float4*>(sd_w + q * kChunk))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
         if (tid == 0) TRACE_AT(0, 10);
         bounded_wait(&bb->full[ip.i], ip.ph, a.err);
         if (tid == 0) TRACE_AT(0, 11);
@@ -883,8 +891,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       if (tid == 0) TRACE_AT(0, 46);
     }
     // ===================================== partial sums into the CTA's slot
-    float* slot = a.ws + static_cast<size_t>(cta) * 4 * SH2 * D;
-    const int n = SH2 * D;
+    // the slot holds the layer's Dr states: [4][SH2 * Dr]
+    float* slot = a.ws + static_cast<size_t>(cta) * 4 * SH2 * Dr;
+    const int n = SH2 * Dr;
     bounded_wait(&bb->dwdone, 0, a.err);
     tc_fence_after();
     {
@@ -895,11 +904,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
         tmem_ld<16>(lane_base + kColDW + 64u * sub + 16u * cp, m);
         tmem_ld<16>(lane_base + kColDW + 64u * sub + TD + 16u * cp, r);
         if (jok) {
-          float4* dst = reinterpret_cast<float4*>(slot + cp * n + jrow * D);
+          float4* dst = reinterpret_cast<float4*>(slot + cp * n + jrow * Dr);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_float4(m[4 * i] + r[4 * i], m[4 * i + 1] + r[4 * i + 1], m[4 * i + 2] + r[4 * i + 2],
-                                 m[4 * i + 3] + r[4 * i + 3]);
+            if (4 * i < Dr)
+              dst[i] = make_float4(m[4 * i] + r[4 * i], m[4 * i + 1] + r[4 * i + 1], m[4 * i + 2] + r[4 * i + 2],
+                                   m[4 * i + 3] + r[4 * i + 3]);
         }
       }
     }
@@ -908,12 +918,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tc_kernel(const __grid_con
       for (int i = 0; i < 4; ++i) {
         const int j = 4 * cw_jq + i;
         if (cw_role == 0) {
-          float4* dst = reinterpret_cast<float4*>(slot + 2 * n + j * D + 8 * cw_dh);
-          dst[0] = make_float4(cacc[i][0], cacc[i][1], cacc[i][2], cacc[i][3]);
-          dst[1] = make_float4(cacc[i][4], cacc[i][5], cacc[i][6], cacc[i][7]);
+          float4* dst = reinterpret_cast<float4*>(slot + 2 * n + j * Dr + 8 * cw_dh);
+          if (8 * cw_dh < Dr) dst[0] = make_float4(cacc[i][0], cacc[i][1], cacc[i][2], cacc[i][3]);
+          if (8 * cw_dh + 4 < Dr) dst[1] = make_float4(cacc[i][4], cacc[i][5], cacc[i][6], cacc[i][7]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) slot[3 * n + (8 * cw_dh + e) * SH2 + j] = a.tw * cacc[i][e];
+          for (int e = 0; e < 8; ++e)
+            if (8 * cw_dh + e < Dr) slot[3 * n + (8 * cw_dh + e) * SH2 + j] = a.tw * cacc[i][e];
         }
       }
     }
@@ -930,8 +941,12 @@ int round_up_b(int x, int m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
-bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a) {
-  if (!fast_path_ok(K, SH2, D) || D != 16) return false;
+// D = 4 and 8 run the same kernel with 16 states, the others zero-padded
+// (their weights read as zero, their gradients not written): every term they
+// add is an exact zero.
+bool bwd_tc_plan(int K, int SH2, int Dr, FastArgs* a) {
+  if (!fast_path_ok(K, SH2, Dr)) return false;
+  constexpr int D = 16;
   int S_max = kTileRows / K;
   if (S_max > 16) S_max = 16;  // the dots cover two halves of 8 samples, the scan 16 x D threads
   const int hc = S_max * K * 128, sc = S_max * 128;
@@ -973,16 +988,26 @@ bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a) {
   a->n_stages = n_stages;
   a->tc = 1;
   a->tmem_cols = 512;
+  a->Dr = Dr;
   return a->smem_bytes <= 227 * 1024;
 }
 
 cudaError_t launch_bwd_tc(const FastArgs& a, int grid, cudaStream_t stream) {
-  bwd_tc_kernel<<<grid, kBwdThreads, a.smem_bytes, stream>>>(a);
+  switch (a.Dr) {
+    case 4: bwd_tc_kernel<4><<<grid, kBwdThreads, a.smem_bytes, stream>>>(a); break;
+    case 8: bwd_tc_kernel<8><<<grid, kBwdThreads, a.smem_bytes, stream>>>(a); break;
+    default: bwd_tc_kernel<16><<<grid, kBwdThreads, a.smem_bytes, stream>>>(a); break;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t prepare_bwd_tc_kernels(int max_smem) {
-  return cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  return e;
 }
 
 }  // namespace m2scan

@@ -73,8 +73,12 @@ struct RingPos {
   }
 };
 
+// DR: the layer's states (4 or 16; a compile-time constant, so that the
+// D = 16 kernel is exactly the unpadded one).
+template <int DR>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_constant__ FastArgs a) {
-  constexpr int D = 16, TD = 32, FD = 64;
+  constexpr int D = 16, TD = 32, FD = 64;  // states inside the kernel
+  constexpr int Dr = DR;  // the layer's states; the others have zero weights
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   float* sW = reinterpret_cast<float*>(base + a.off_wt);      // NC tiles [FD][32], swizzled
@@ -190,10 +194,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_tc16_kernel(const __grid_c
       const bool ok = i < SH2 * 4;
       const int j = i % SH2, dq = i / SH2;
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      wa[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_A + j * D + 4 * dq)) : z;
-      wb[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_B + j * D + 4 * dq)) : z;
-      wc[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_C + j * D + 4 * dq)) : z;
-      wo[u] = ok ? __ldg(reinterpret_cast<const float4*>(a.W_O) + i) : z;
+      // states Dr .. 15 of a layer with fewer states: zero weights
+      const bool okd = ok && 4 * dq < Dr;
+      wa[u] = okd ? __ldg(reinterpret_cast<const float4*>(a.W_A + j * Dr + 4 * dq)) : z;
+      wb[u] = okd ? __ldg(reinterpret_cast<const float4*>(a.W_B + j * Dr + 4 * dq)) : z;
+      wc[u] = okd ? __ldg(reinterpret_cast<const float4*>(a.W_C + j * Dr + 4 * dq)) : z;
+      wo[u] = ok && i < Dr * SH2 / 4 ? __ldg(reinterpret_cast<const float4*>(a.W_O) + i) : z;
     }
     // the first stages are requested after the weights, so that the weight
     // loads are not queued behind them
@@ -570,8 +576,12 @@ int round_up_f(int x, int m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
-bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a) {
-  if (!fast_path_ok(K, SH2, D) || D != 16) return false;
+// D = 4 runs the same kernel with 16 states, 12 of them zero-padded (their
+// weights read as zero): every term they add is an exact zero. (D = 8 has a
+// kernel of its own.)
+bool fwd_tc16_plan(int K, int SH2, int Dr, FastArgs* a) {
+  if (!fast_path_ok(K, SH2, Dr) || (Dr != 16 && Dr != 4)) return false;
+  constexpr int D = 16;
   int S_max = kTileRows / K;
   if (S_max > 16) S_max = 16;  // the dots cover two halves of 8 samples, the output four groups of 4
   const int hc = S_max * K * 128, sc = S_max * 128;
@@ -608,16 +618,23 @@ bool fwd_tc16_plan(int K, int SH2, int D, FastArgs* a) {
   a->n_stages = n_stages;
   a->tc = 2;
   a->tmem_cols = 512;
+  a->Dr = Dr;
   return a->smem_bytes <= 227 * 1024;
 }
 
 cudaError_t launch_fwd_tc16(const FastArgs& a, int grid, cudaStream_t stream) {
-  fwd_tc16_kernel<<<grid, kFwdThreads, a.smem_bytes, stream>>>(a);
+  if (a.Dr == 4)
+    fwd_tc16_kernel<4><<<grid, kFwdThreads, a.smem_bytes, stream>>>(a);
+  else
+    fwd_tc16_kernel<16><<<grid, kFwdThreads, a.smem_bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t prepare_fwd_tc16_kernels(int max_smem) {
-  return cudaFuncSetAttribute(fwd_tc16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc16_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fwd_tc16_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  return e;
 }
 
 }  // namespace m2scan

@@ -59,6 +59,8 @@ struct alignas(128) FastArgs {
   int tc;         // 0: FP32-FMA kernel, 1: tensor-core kernel, 2: tensor-core forward for D = 16
   int tmem_cols;  // TMEM columns allocated by each CTA (power of two)
   int smem_bytes;
+  int Dr;       // tensor-core kernels for D = 16: the layer's D (4, 8 or 16); states
+                // Dr .. 15 are zero-padded inside the kernel
   float tw;
 };
 
