@@ -12,10 +12,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libm2scan.so")
-SOURCES = ["m2scan_api.cu", "m2scan_fast.cu", "m2scan_fwd_tc.cu", "m2scan_fwd_tc16.cu",
-           "m2scan_bwd_tc.cu", "m2scan_generic.cu", "m2scan_noalloc.cu", "m2scan_wide_tc.cu",
-           "m2scan_colsum.cu", "m2scan_blend.cu", "m2scan_fwd_bf16.cu",
-           "m2scan_selftest.cu", "m2scan_bwd_bf16.cu"]
+SOURCES = ["m2scan_api.cu", "m2scan_fwd_tc.cu", "m2scan_fwd_tc16.cu", "m2scan_bwd_tc.cu",
+           "m2scan_generic.cu", "m2scan_noalloc.cu", "m2scan_wide_tc.cu", "m2scan_colsum.cu",
+           "m2scan_blend.cu", "m2scan_fwd_bf16.cu", "m2scan_selftest.cu", "m2scan_bwd_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -14,7 +14,6 @@
 #include "m2scan_internal.h"
 
 namespace m2scan {
-cudaError_t prepare_fast_kernels(int max_smem);
 cudaError_t prepare_generic_kernels(int max_smem);
 cudaError_t prepare_fwd_tc_kernels(int max_smem);
 cudaError_t prepare_bwd_tc_kernels(int max_smem);
@@ -70,7 +69,6 @@ m2scan_status prepare_device(int* dev_out) {
       (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
     return cuda_fail(e);
   if (major != 10 || minor != 3) return M2SCAN_ERR_DEVICE;  // built for sm_103a only
-  if ((e = prepare_fast_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_generic_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_fwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
   if ((e = prepare_bwd_tc_kernels(smem)) != cudaSuccess) return cuda_fail(e);
@@ -134,15 +132,14 @@ m2scan_status check_shape(int64_t B, int32_t K, int32_t SH2, int32_t D) {
 
 int slots_for(int64_t B) { return B < kMaxSlots ? static_cast<int>(B) : kMaxSlots; }
 
-// 1 = fast path (plan->tc set when the tensor-core kernel is used), 2 = generic,
-// 3 = wide-state FP32 kernels, 0 = unsupported.
+// 1 = fused tensor-core kernels (plan->tc says which forward), 2 = generic,
+// 3 = wide-state tensor-core kernels, 0 = unsupported.
 int choose_path(int64_t B, int32_t K, int32_t SH2, int32_t D, bool bwd, int max_smem,
                 FastArgs* plan) {
   if (!g_force_generic.load() && B <= 0x7fffffffll) {
     if (!bwd && fwd_tc16_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (!bwd && fwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     if (bwd && bwd_tc_plan(K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
-    if (fast_plan(bwd, K, SH2, D, plan) && plan->smem_bytes <= max_smem) return 1;
     // (the wide-state kernels address rows with 32-bit TMA coordinates)
     if (wide_path_ok(K, SH2, D) && B * K < (1ll << 31)) return 3;
   }
@@ -318,9 +315,7 @@ m2scan_status m2scan_fwd_ex(const float* h_history, const float* h_s2, const flo
     fa.out0 = h_enriched; fa.out1 = nullptr; fa.ws = nullptr; fa.gate_scale = gate_scale;
     fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, nullptr, B)) return M2SCAN_ERR_UNSUPPORTED;
-    e = fa.tc == 2 ? launch_fwd_tc16(fa, grid, stream)
-        : fa.tc    ? launch_fwd_tc(D, fa, grid, stream)
-                   : launch_fast(false, D, fa, grid, stream);
+    e = fa.tc == 2 ? launch_fwd_tc16(fa, grid, stream) : launch_fwd_tc(D, fa, grid, stream);
   } else if (path == 3) {
     e = launch_wide_fwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, B, K, SH2, h_enriched,
                         gate_scale, g_err_ptr[dev], stream);
@@ -575,7 +570,7 @@ m2scan_status m2scan_bwd_ex(const float* h_history, const float* h_s2, const flo
     fa.out0 = d_h_history; fa.out1 = d_h_s2; fa.ws = ws; fa.gate_scale = gate_scale;
     fa.err = g_err_ptr[dev]; fa.B = B; fa.tw = tw; fa.trace = trace_buffer();
     if (!encode_fast_maps(&fa, h_history, h_s2, d_h_enriched, B)) return M2SCAN_ERR_UNSUPPORTED;
-    e = fa.tc ? launch_bwd_tc(fa, grid, stream) : launch_fast(true, D, fa, grid, stream);
+    e = launch_bwd_tc(fa, grid, stream);
   } else if (path == 3) {
     int n = 0;
     e = launch_wide_bwd(h_history, h_s2, W_A, W_B, W_C, W_O, tw, d_h_enriched, B, K, SH2, d_h_history,

@@ -9,14 +9,11 @@
 
 namespace m2scan {
 
-constexpr int kThreads = 256;     // threads per CTA, every kernel
-constexpr int kStages = 3;        // depth of the copy ring of the FP32-FMA fast kernels
-constexpr int kMaxStages = 6;     // ring depth, at most (any fast kernel)
+constexpr int kThreads = 256;     // threads per CTA of the generic and small kernels
+constexpr int kMaxStages = 6;     // copy-ring depth of the fused kernels, at most
 constexpr int kMaxSlots = 152;    // CTAs (= weight-gradient slots) per call, at most
 constexpr int kTileRows = 128;    // rows (samples x K) per pass-1 tile, at most
 constexpr int kChunk = 32;        // SH2 columns per pass-1 chunk (128 bytes)
-constexpr int kRowsPerItem = 32;  // h_history rows per pass-2 row item
-constexpr int kMaxSampleItem = 16;
 
 // Arguments of the fused kernels. The three tensor maps describe h_history as
 // a 3-D tensor [SH2, K, B] (box [32, K, S_max]) and h_s2 / d_h_enriched as 2-D
@@ -52,11 +49,8 @@ struct alignas(128) FastArgs {
   int off_wab, off_wct, off_wo, off_p, off_cs, off_ctx, off_dctx, off_dc, off_bar;
   int off_hlo;    // tensor-core path: two [128 x 32] buffers of h - tf32(h)
   int off_wt;     // tensor-core path: W_A|W_B transposed, K-major tiles (tf32 part)
-  int off_wtlo;   // tensor-core path: the remainder W - tf32(W), same layout
-  int off_mbar;   // tensor-core path: two MMA-completion barriers
-  int off_tslot;  // tensor-core path: TMEM base address written by tcgen05.alloc
   int n_stages;   // depth of the copy ring
-  int tc;         // 0: FP32-FMA kernel, 1: tensor-core kernel, 2: tensor-core forward for D = 16
+  int tc;         // 1: tensor-core kernel (fwd_tc / bwd_tc), 2: tensor-core forward for D = 4, 16
   int tmem_cols;  // TMEM columns allocated by each CTA (power of two)
   int smem_bytes;
   int Dr;       // tensor-core kernels for D = 16: the layer's D (4, 8 or 16); states
@@ -84,15 +78,13 @@ struct GenericArgs {
   int staged = 0;           // set by launch_generic: weights, h rows and slot in shared memory
 };
 
-// Fast path shape limits (see m2scan.h).
-bool fast_path_ok(int K, int SH2, int D);
-// Fills the shared-memory plan of a fast kernel. Returns false if it does not fit.
-bool fast_plan(bool bwd, int K, int SH2, int D, FastArgs* a);
-// Whether the tensor-core variant of the fast kernels covers this direction and D.
-bool tc_path_ok(bool bwd, int D);
+// Shapes of the fused tensor-core kernels (the fast path of m2scan.h).
+inline bool fast_path_ok(int K, int SH2, int D) {
+  return (D == 4 || D == 8 || D == 16) && SH2 >= kChunk && SH2 % kChunk == 0 && SH2 <= 256 &&
+         SH2 * D <= 4096 && K >= 1 && K <= kTileRows;
+}
 size_t generic_smem_bytes(bool bwd, int K, int SH2, int D);
 
-cudaError_t launch_fast(bool bwd, int D, const FastArgs& a, int grid, cudaStream_t stream);
 // Tensor-core kernels for wide states (D = 64, SH2 % 128 == 0, K <= 128).
 bool wide_path_ok(int K, int SH2, int D);
 int wide_ranges(int64_t B);
@@ -120,7 +112,7 @@ cudaError_t launch_fwd_tc16(const FastArgs& a, int grid, cudaStream_t stream);
 bool fwd_bf16_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_fwd_bf16(const FastArgs& a, int grid, cudaStream_t stream);
 cudaError_t prepare_fwd_bf16_kernels(int max_smem);
-// Warp-specialised tensor-core backward (D = 16).
+// Warp-specialised tensor-core backward (D = 4, 8, 16; plan->Dr = D).
 bool bwd_tc_plan(int K, int SH2, int D, FastArgs* a);
 cudaError_t launch_bwd_tc(const FastArgs& a, int grid, cudaStream_t stream);
 // bf16: the activations (h_history, h_s2, g, out0, out1) are bfloat16. The
@@ -130,7 +122,6 @@ cudaError_t launch_generic(bool bwd, GenericArgs a, int grid, int max_smem, cuda
                            bool bf16 = false);
 cudaError_t launch_reduce(const float* ws, int slots, int n, float* dW_A, float* dW_B,
                           float* dW_C, float* dW_O, cudaStream_t stream);
-cudaError_t prepare_kernels(int max_smem_optin);
 // Bias-gradient column sum (two launches): partial sums of P = colsum_partials(N)
 // row ranges into part [P][C], then their fixed-order sum into db.
 int colsum_partials(long long N);

@@ -16,8 +16,9 @@ pytestmark = pytest.mark.gpu
 DW = ("dW_A", "dW_B", "dW_C", "dW_O")
 
 # (B, K, SH2, D, bf16, force_generic): the fp32 and bf16 tensor-core
-# backwards on the layer's shape, the wide-state family, the FP32-FMA kernel
-# (D = 8) and the generic per-sample kernel
+# backwards on the layer's shape, the wide-state family, the tensor-core
+# backward with D = 8 zero-padded to 16 states, and the generic per-sample
+# kernel
 CASES = [(8192, 8, 256, 16, False, False), (8192, 8, 256, 16, True, False),
          (1000, 4, 512, 64, False, False), (3000, 8, 128, 8, False, False),
          (500, 8, 256, 16, False, True)]
