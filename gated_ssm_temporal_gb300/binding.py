@@ -78,6 +78,8 @@ def load_library(path: str | None = None):
         lib.m2scan_set_force_generic.restype = ctypes.c_int
         lib.m2scan_path_for.argtypes = [i32, i32, i32]
         lib.m2scan_path_for.restype = ctypes.c_int
+        lib.m2scan_fwd_path_for.argtypes = [i32, i32, i32]
+        lib.m2scan_fwd_path_for.restype = ctypes.c_int
         lib.m2scan_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.m2scan_read_device_flags.restype = ctypes.c_int
         lib.m2scan_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
@@ -174,6 +176,10 @@ def m2scan_set_force_generic(force):
 
 def m2scan_path_for(K, SH2, D):
     return load_library().m2scan_path_for(K, SH2, D)
+
+
+def m2scan_fwd_path_for(K, SH2, D):
+    return load_library().m2scan_fwd_path_for(K, SH2, D)
 
 
 def m2scan_read_device_flags():

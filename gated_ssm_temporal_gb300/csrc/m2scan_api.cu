@@ -189,7 +189,7 @@ bool encode_bf16_maps(FastArgs* a, const void* h_history, const void* h_s2, int6
   return true;
 }
 
-// Tensor maps of the fast kernels: h_history as [SH2, K, B] with box
+// Tensor maps of the fused tensor-core kernels: h_history as [SH2, K, B] with box
 // [32, K, S_max]; h_s2 and (backward) d_h_enriched as [SH2, B] with box [32, S_max].
 bool encode_fast_maps(FastArgs* a, const float* h_history, const float* h_s2, const float* g,
                       int64_t B) {
@@ -241,6 +241,13 @@ int m2scan_path_for(int32_t K, int32_t SH2, int32_t D) {
   FastArgs plan;
   const int max_smem = 227 * 1024;
   return choose_path(1, K, SH2, D, true, max_smem, &plan);
+}
+
+int m2scan_fwd_path_for(int32_t K, int32_t SH2, int32_t D) {
+  if (check_shape(1, K, SH2, D) != M2SCAN_OK) return 0;
+  FastArgs plan;
+  const int max_smem = 227 * 1024;
+  return choose_path(1, K, SH2, D, false, max_smem, &plan);
 }
 
 size_t m2scan_bwd_workspace_bytes(int64_t B, int32_t K, int32_t SH2, int32_t D) {

@@ -1,6 +1,6 @@
-// Generic kernels of the gated temporal scan layer, for shapes outside the
-// fused fast path (e.g. D = 64 with SH2 = 512), and the slot reduction shared
-// by both backward paths.
+// Generic kernels of the gated temporal scan layer, for shapes that neither
+// the fused tensor-core kernels nor the wide-state kernels take (e.g. D = 24,
+// or SH2 = 36), and the slot reduction that every backward family ends with.
 //
 // The generic kernels keep one sample at a time in shared memory: each CTA
 // owns the samples [c*B/P, (c+1)*B/P) and the weight-gradient slot c. Every

@@ -291,10 +291,14 @@ int m2scan_last_cuda_error(void);
  * generic fallback kernels. Process-wide; returns the previous value. */
 int m2scan_set_force_generic(int force);
 
-/* Which kernel family m2scan_fwd/m2scan_bwd would launch for these shapes:
- * 1 = fused fast path, 2 = generic fallback, 3 = wide-state tensor-core
- * kernels (D = 64, SH2 % 128 == 0, K <= 128), 0 = unsupported shape. */
+/* Which kernel family m2scan_bwd would launch for these shapes (any B >= 1
+ * with B * K < 2^31): 1 = fused tensor-core kernels (the fast path), 2 =
+ * generic fallback, 3 = wide-state tensor-core kernels (D = 64,
+ * SH2 % 128 == 0, K <= 128), 0 = unsupported shape. Host-only: needs no GPU. */
 int m2scan_path_for(int32_t K, int32_t SH2, int32_t D);
+
+/* The same for m2scan_fwd. */
+int m2scan_fwd_path_for(int32_t K, int32_t SH2, int32_t D);
 
 /*
  * Device-side error flags of the current device (bit 0: a kernel gave up

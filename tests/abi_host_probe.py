@@ -76,6 +76,14 @@ res["path_tiny"] = g.m2scan_path_for(8, 32, 4)
 res["path_wide"] = g.m2scan_path_for(16, 512, 64)
 res["path_K129"] = g.m2scan_path_for(129, 256, 16)
 res["path_huge"] = g.m2scan_path_for(100000, 256, 64)
+res["fwd_path_pages"] = g.m2scan_fwd_path_for(8, 256, 16)
+res["fwd_path_wide"] = g.m2scan_fwd_path_for(16, 512, 64)
+res["fwd_path_K129"] = g.m2scan_fwd_path_for(129, 256, 16)
+res["fwd_path_huge"] = g.m2scan_fwd_path_for(100000, 256, 64)
+# every shape of the fused kernels' range (D in {4, 8, 16}, SH2 a multiple of
+# 32 up to 256, K up to 128): the family each direction takes
+res["fused_range"] = sorted({(g.m2scan_fwd_path_for(k, s, d), g.m2scan_path_for(k, s, d))
+                             for k in range(1, 129) for s in range(32, 257, 32) for d in (4, 8, 16)})
 
 
 def bias(**kw):

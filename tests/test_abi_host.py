@@ -103,4 +103,15 @@ def test_path_choice(probe):
     assert probe["path_wide"] == 3
     assert probe["path_K129"] == 2
     assert probe["path_huge"] == 0
+    assert probe["fwd_path_pages"] == 1
+    assert probe["fwd_path_wide"] == 3
+    assert probe["fwd_path_K129"] == 2
+    assert probe["fwd_path_huge"] == 0
+
+
+def test_fused_range_has_tensor_core_plans_in_both_directions(probe):
+    # every shape the fused kernels take has a tensor-core plan that fits in
+    # 227 KB of shared memory, forward and backward (the library keeps no
+    # other kernel for these shapes)
+    assert probe["fused_range"] == [[1, 1]]
     assert probe["status_str_ok"] == "ok"
