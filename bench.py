@@ -200,6 +200,23 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+# nominal dense tensor rates (PFLOP/s): tf32 1.1, bf16 2.25
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def fp32_product_peak():
+    """TFLOP/s of fp32-accurate products on the tensor cores: the bf16 burst
+    peak (measured, else the fallback 1.9 PFLOP/s) times the nominal
+    tf32:bf16 ratio, divided by 3 for the three tf32 products of a 3 x TF32
+    split. Returns (peak, source)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16, src = float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        bf16, src = 1900.0, "fallback"
+    return bf16 * TF32_PER_BF16 / 3.0, src
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_ssm_temporal_gb300", "csrc")
@@ -316,7 +333,8 @@ def run_native(args, rank, world, local):
 
     import gated_ssm_temporal_gb300 as g
     from gated_ssm_temporal_gb300 import build as gbuild
-    from gated_ssm_temporal_gb300.workloads import WORKLOADS, algorithmic_bytes, make_inputs
+    from gated_ssm_temporal_gb300.workloads import (WORKLOADS, algorithmic_bytes, algorithmic_flops,
+                                                    make_inputs)
 
     torch.cuda.set_device(local)
     dist = init_dist(world, "nccl")
@@ -468,12 +486,33 @@ def run_native(args, rank, world, local):
         return
     elem = 2 if bf16 else 4
     ab = algorithmic_bytes(B, K, SH2, elem=elem)
+    af = algorithmic_flops(B, K, SH2, D)
     peak, peak_src = measured_peaks()
-    achieved = ab["bwd"] / (bwd_ms / 1e3) / 1e9
-    bwd_kernel = ("m2scan_bwd_bf16" if bf16 else "m2scan_bwd (fused backward + slot reduction)")
+    wide = g.m2scan_path_for(K, SH2, D) == 3
+    bwd_kernel = ("m2scan_bwd_bf16" if bf16 else
+                  "m2scan_bwd (wide-state weight split, tile kernel, d_h_s2, dW products, slot "
+                  "reduction)" if wide else "m2scan_bwd (fused backward + slot reduction)")
     bwd_write = elem * SH2 * (K + 1) * B  # d_h_history and d_h_s2
-    traffic = traffic_fields("m2scan_bwd_bf16" if bf16 else "m2scan_bwd", ab["bwd"] - bwd_write,
-                             bwd_write)
+    # the bound of the backward call: its bytes at the HBM peak against its
+    # method FLOPs as 3 x TF32 tensor-core products (fp32 arithmetic only)
+    tpeak, tpeak_src = fp32_product_peak()
+    tensor_bound = not bf16 and af["bwd"] / (tpeak * 1e12) > ab["bwd"] / (peak * 1e9)
+    if tensor_bound:
+        achieved = af["bwd"] / (bwd_ms / 1e3) / 1e12
+        roof = {"kernel": bwd_kernel, "bound": "tensor", "achieved": achieved, "peak": tpeak,
+                "peak_source": tpeak_src + " bf16_tflops burst x nominal tf32:bf16 (1.1/2.25) / 3 "
+                               "(3 x TF32: three tf32 products per fp32 product)",
+                "unit": "TFLOP/s", "frac": achieved / tpeak, "algorithmic_flops": af["bwd"],
+                "algorithmic_bytes": ab["bwd"],
+                "hbm_frac_of_measured": ab["bwd"] / (bwd_ms / 1e3) / 1e9 / peak,
+                "traffic": None, "traffic_note": "no DRAM-counter record for this call"}
+    else:
+        achieved = ab["bwd"] / (bwd_ms / 1e3) / 1e9
+        traffic = traffic_fields("m2scan_bwd_bf16" if bf16 else "m2scan_bwd", ab["bwd"] - bwd_write,
+                                 bwd_write)
+        roof = dict({"kernel": bwd_kernel, "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src + " hbm_gbs burst", "unit": "GB/s",
+                     "frac": achieved / peak, "algorithmic_bytes": ab["bwd"]}, **traffic)
     line = {
         "metric": metric_for(w) + (" with bf16 activations" if bf16 else ""), "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
@@ -489,11 +528,7 @@ def run_native(args, rank, world, local):
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_ms_mean": fwd_mean, "bwd_ms_mean": bwd_mean,
         "hbm_gbs": ab["total"] / (step_ms / 1e3) / 1e9,
         "hbm_frac_of_measured": ab["total"] / (step_ms / 1e3) / 1e9 / peak,
-        "roofline": dict({"kernel": bwd_kernel, "bound": "hbm",
-                          "achieved": achieved, "peak": peak,
-                          "peak_source": peak_src + " hbm_gbs burst",
-                          "unit": "GB/s", "frac": achieved / peak,
-                          "algorithmic_bytes": ab["bwd"]}, **traffic),
+        "roofline": roof,
         "device_flags": int(flags_any),
         "e2e": {"value": whole_job_throughput(B, world, e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

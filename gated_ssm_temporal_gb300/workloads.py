@@ -96,6 +96,17 @@ def algorithmic_bytes(B: int, K: int, SH2: int, elem: int = 4) -> dict:
     return dict(fwd=fwd, bwd=bwd, total=fwd + bwd)
 
 
+def algorithmic_flops(B: int, K: int, SH2: int, D: int) -> dict:
+    """Floating-point operations of the method per call (a multiply-add
+    counts 2): forward 4*SH2*D*(K+1) per sample (the A|B projections over K
+    steps and C, then context . W_O), backward with the projections
+    recomputed 2*SH2*D*(6K+5) per sample (A|B again, d_h_history, dW_A|dW_B,
+    d_ctx, dW_O, dW_C, d_h_s2). The scan's O(K*D) work is left out."""
+    fwd = 4 * SH2 * D * (K + 1) * B
+    bwd = 2 * SH2 * D * (6 * K + 5) * B
+    return dict(fwd=fwd, bwd=bwd, total=fwd + bwd)
+
+
 # The bias-gradient column sum: the per-output-feature gradient dy [N, C] of
 # a fully connected layer of the pages' network ("Phase 3 Kernel Optimization
 # Implementation Plan": batch 8192, out_dim from 3 to 256 for the main
