@@ -4,12 +4,20 @@ kernels' tile splits, ring depths and item counts must finish without a
 deadlock, a parity alias or a buffer hazard, and each planted protocol
 mistake must be caught."""
 import itertools
+import os
+import re
 
 import pytest
 
 import protocol_models as pm
 
 P = 152
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                    "gated_ssm_temporal_gb300", "csrc")
+# every copy-ring depth a kernel can run with: the fused kernels' plans pick
+# 2 .. kMaxStages stages from the shared memory they need, the wide-state and
+# bf16 kernels have fixed depths
+DEPTHS = (2, 3, 4, 5, 6)
 # (B, K): the layer's workload, ragged splits, a CTA with one or no sample,
 # the narrowest and widest histories
 SHAPES = [(8192, 8), (65536, 8), (1000, 8), (300, 16), (152, 8), (20, 8), (700, 1), (400, 128), (333, 3)]
@@ -21,9 +29,31 @@ WIDTHS = {"fwd_tc16": (256, 64, 32), "fwd_bf16": (256, 128, 64), "bwd_tc": (256,
 @pytest.mark.parametrize("model", sorted(pm.MODELS))
 def test_protocol_runs_clean(model):
     f = pm.MODELS[model]
-    for (B, K), SH2, NST, cta in itertools.product(SHAPES, WIDTHS[model], (2, 3, 5, 6), (0, 77, P - 1)):
+    for (B, K), SH2, NST, cta in itertools.product(SHAPES, WIDTHS[model], DEPTHS, (0, 77, P - 1)):
         for seed in range(6):
             f(B, P, cta, K, SH2, NST, seed)
+
+
+def _kernel_constant(fname, name):
+    src = open(os.path.join(CSRC, fname)).read()
+    found = re.findall(r"constexpr int %s = (\d+);" % name, src)
+    assert len(found) == 1, (fname, name)
+    return int(found[0])
+
+
+def test_models_use_the_kernels_constants():
+    # item sizes, hand-off rings and remainder buffers as the kernels define them
+    assert pm.kRowItem == _kernel_constant("m2scan_bwd_tc.cu", "kRowItem")
+    assert pm.kBwdSampleItem == _kernel_constant("m2scan_bwd_tc.cu", "kBwdSampleItem")
+    for f in ("m2scan_bwd_tc.cu", "m2scan_fwd_tc16.cu"):
+        assert pm.kChunkRing == _kernel_constant(f, "kChunkRing")
+        assert pm.kLoBufs == _kernel_constant(f, "kLoBufs")
+    # every copy-ring depth a kernel can run with is one the models run
+    assert max(DEPTHS) == _kernel_constant("m2scan_internal.h", "kMaxStages")
+    assert pm.kChunkRing >= max(DEPTHS)
+    for f, name in (("m2scan_wide_tc.cu", "kNst"), ("m2scan_wide_tc.cu", "kDwNst"),
+                    ("m2scan_bwd_bf16.cu", "kNst"), ("m2scan_fwd_bf16.cu", "kBfStages")):
+        assert _kernel_constant(f, name) in DEPTHS, (f, name)
 
 
 def test_tile_split_covers_the_slice():
