@@ -58,10 +58,11 @@ def test_tensor_core_multi_tile_shapes(B, K, SH2):
 
 
 # samples per tile 16, 8, 6, 4 and 1 cover the three dot layouts of the
-# wide-state tile kernels (8, 4 and 2 chunk columns per thread)
+# wide-state tile kernels (8, 4 and 2 chunk columns per thread); SH2 from 128
+# to 1024 (4 to 32 chunks and 1 to 8 column blocks per tile)
 @pytest.mark.parametrize("B,K,SH2", [
     (1, 1, 128), (5, 16, 512), (37, 3, 128), (1000, 7, 384), (300, 128, 256), (2047, 16, 512),
-    (700, 20, 128), (333, 32, 256)])
+    (700, 20, 128), (333, 32, 256), (300, 4, 1024), (155, 2, 640)])
 def test_wide_state_shapes(B, K, SH2):
     # D = 64 runs the wide-state tensor-core kernels: 128-row tiles of up to
     # 16 samples, a partial last tile, and up to 152 sample ranges for the dW
