@@ -32,7 +32,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-METRIC = "fwd+bwd samples/s (B=8192, K=8, SH2=256, D=16)"
 UNIT = "samples/s"
 FLUSH_BYTES = 512 << 20
 L2_NOTE = ("flushed before every timed call: a 512 MiB write, then a 512 MiB read of another "
@@ -189,6 +188,15 @@ class ClockSampler:
 def metric_for(w) -> str:
     """The headline metric's name, with the workload's own dimensions."""
     return "fwd+bwd samples/s (B=%d, K=%d, SH2=%d, D=%d)" % (w.B, w.K, w.SH2, w.D)
+
+
+def layer_config(w, world: int, activations: str) -> dict:
+    """The workload's config, the same dict on both arms (the native line and
+    the oracle's reference line); ``l2`` states how the native arm's timed
+    calls treat L2."""
+    return {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g" % (w.name, w.B, w.K, w.SH2, w.D, w.tw),
+            "B": w.B, "K": w.K, "SH2": w.SH2, "D": w.D, "parallelism": "replicas x%d" % world,
+            "activations": activations, "l2": L2_NOTE}
 
 
 def measured_peaks():
@@ -518,12 +526,9 @@ def run_native(args, rank, world, local):
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
         "data": "synthetic",
-        "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g" % (w.name, B, K, SH2, D, w.tw),
-                   "B": B, "K": K, "SH2": SH2, "D": D, "parallelism": "replicas x%d" % world,
-                   "activations": args.dtype,
-                   "arithmetic": ("bf16 tensor-core operands (exact products), fp32 sums"
-                                  if bf16 else "fp32 (3 x TF32 tensor-core products)"),
-                   "l2": L2_NOTE},
+        "config": layer_config(w, world, args.dtype),
+        "arithmetic": ("bf16 tensor-core operands (exact products), fp32 sums"
+                       if bf16 else "fp32 (3 x TF32 tensor-core products)"),
         "timing": "median of the per-step CUDA-event times (fwd, bwd and their sum)",
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_ms_mean": fwd_mean, "bwd_ms_mean": bwd_mean,
         "hbm_gbs": ab["total"] / (step_ms / 1e3) / 1e9,
@@ -589,13 +594,14 @@ def run_reference(args, rank, world):
     el = time.perf_counter() - t0
     value = ns * args.steps / el
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "impl": "reference", "metric": metric_for(base), "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "%s: B=%d K=%d SH2=%d D=%d tw=%g" % (base.name, base.B, base.K,
-                                                                    base.SH2, base.D, base.tw),
-                   "B": base.B, "K": base.K, "SH2": base.SH2, "D": base.D},
+        "config": layer_config(base, world, "f32"),
+        "arithmetic": "fp64 loops on the host cores (the oracle); each step a bounded sample of "
+                      "the batch; the config's l2 entry describes the native arm's timed calls",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": "first %d of the %d samples per step" % (ns, base.B)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
