@@ -155,20 +155,27 @@ def test_bwd_bitwise_reproducible_and_stream_independent():
     assert torch.equal(y1, y2)
 
 
-def test_guard_bands_untouched():
-    """Outputs sit inside larger buffers filled with a sentinel; nothing outside is written."""
+# one shape per kernel family: the D = 16, 4 and 8 tensor-core kernels, the
+# wide-state kernels and the generic kernels, each with a ragged last tile
+GUARD_SHAPES = [(153, 8, 256, 16), (153, 8, 256, 4), (153, 8, 256, 8), (155, 4, 512, 64),
+                (23, 8, 36, 16)]
+
+
+@pytest.mark.parametrize("B,K,SH2,D", GUARD_SHAPES)
+def test_guard_bands_untouched(B, K, SH2, D):
+    """Outputs and the workspace sit inside larger buffers filled with a
+    sentinel (16 KB on each side); nothing outside them is written."""
     import torch
     import gated_ssm_temporal_gb300 as g
     ensure_built()
-    x = custom(153, 8, 256, 16, seed=3, tw=0.1)
+    x = custom(B, K, SH2, D, seed=3, tw=0.1)
     d = to_dev(x)
-    B, K, SH2, D = 153, 8, 256, 16
-    pad = 64
+    pad = 4096
     sentinel = 12345.5
 
-    def guarded(shape):
+    def guarded(shape, dtype=torch.float32):
         n = int(np.prod(shape))
-        buf = torch.full((n + 2 * pad,), sentinel, device="cuda", dtype=torch.float32)
+        buf = torch.full((n + 2 * pad,), sentinel, device="cuda", dtype=dtype)
         return buf, buf[pad:pad + n].view(*shape)
 
     bufs = {}
@@ -188,7 +195,45 @@ def test_guard_bands_untouched():
     ref = oracle_all(x)
     got = {k: v.cpu().numpy() for k, v in outs.items()}
     got["h_enriched"] = y.cpu().numpy()
-    assert_outputs(got, ref, shape_of(x), NAMES)
+    assert_outputs(got, ref, shape_of(x), NAMES, wide=runs_wide(x, False))
+    assert g.m2scan_read_device_flags() == 0
+
+
+def test_guard_bands_untouched_bf16():
+    """The same for the bf16 kernels: bf16 activation outputs, fp32 weight
+    gradients and workspace, each inside sentinel-filled buffers."""
+    import torch
+    import gated_ssm_temporal_gb300 as g
+    ensure_built()
+    B, K, SH2, D = 153, 8, 256, 16
+    d = to_dev(custom(B, K, SH2, D, seed=4, tw=0.1))
+    for k in ("h_history", "h_s2", "d_h_enriched"):
+        d[k] = d[k].to(torch.bfloat16)
+    pad = 4096
+    sentinel = 1234.0  # exact in bf16
+
+    def guarded(shape, dtype):
+        n = int(np.prod(shape))
+        buf = torch.full((n + 2 * pad,), sentinel, device="cuda", dtype=dtype)
+        return buf, buf[pad:pad + n].view(*shape)
+
+    bf, f32 = torch.bfloat16, torch.float32
+    shapes = {"d_h_history": ((B, K, SH2), bf), "d_h_s2": ((B, SH2), bf), "dW_A": ((SH2, D), f32),
+              "dW_B": ((SH2, D), f32), "dW_C": ((SH2, D), f32), "dW_O": ((D, SH2), f32)}
+    bufs, outs = {}, {}
+    for k, (sh, dt) in shapes.items():
+        bufs[k], outs[k] = guarded(sh, dt)
+    ybuf, y = guarded((B, SH2), bf)
+    wsbuf, ws = guarded((g.m2scan_bwd_workspace_bytes(B, K, SH2, D) // 4,), f32)
+    args = (d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"])
+    g.fwd_bf16(*args, out=y)
+    g.bwd_bf16(*args, d["d_h_enriched"], outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    for buf in list(bufs.values()) + [ybuf, wsbuf]:
+        assert torch.all(buf[:pad] == sentinel) and torch.all(buf[-pad:] == sentinel)
+    for k, v in list(outs.items()) + [("h_enriched", y)]:
+        assert torch.isfinite(v.float()).all(), k
+    assert g.m2scan_read_device_flags() == 0
 
 
 def test_empty_batch():
