@@ -155,6 +155,39 @@ def test_bwd_bitwise_reproducible_and_stream_independent():
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("B,K,SH2,D", [(8192, 8, 256, 16), (4096, 16, 512, 64)])
+def test_concurrent_calls_on_two_streams(B, K, SH2, D):
+    """Forward and backward calls on two streams at once, each with its own
+    inputs, outputs and workspace, give the results of the same calls made
+    one after another: the calls share no state."""
+    import torch
+    import gated_ssm_temporal_gb300 as g
+    ensure_built()
+    ds = [to_dev(custom(B, K, SH2, D, seed=s, tw=0.1)) for s in (31, 32)]
+    wss = [g.alloc_workspace(B, K, SH2, D, "cuda") for _ in ds]
+
+    def call(d, ws, stream=None):
+        y = g.fwd(d["h_history"], d["h_s2"], d["W_A"], d["W_B"], d["W_C"], d["W_O"], d["tw"],
+                  stream=stream)
+        r = run_bwd(d, workspace=ws, stream=stream)
+        r["h_enriched"] = y
+        return r
+
+    serial = [call(d, ws) for d, ws in zip(ds, wss)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for rep in range(5):
+        outs = [None, None]
+        for i in (0, 1):
+            with torch.cuda.stream(streams[i]):
+                outs[i] = call(ds[i], wss[i], stream=streams[i])
+        torch.cuda.synchronize()
+        for i in (0, 1):
+            for k, v in outs[i].items():
+                assert torch.equal(v, serial[i][k]), (rep, i, k)
+    assert g.m2scan_read_device_flags() == 0
+
+
 # one shape per kernel family: the D = 16, 4 and 8 tensor-core kernels, the
 # wide-state kernels and the generic kernels, each with a ragged last tile
 GUARD_SHAPES = [(153, 8, 256, 16), (153, 8, 256, 4), (153, 8, 256, 8), (155, 4, 512, 64),
