@@ -50,8 +50,13 @@
  *     from the destroyed context.
  *   - Supported shapes: B >= 0, K >= 1, SH2 >= 4 with SH2 % 4 == 0, D >= 1,
  *     and per-sample scratch of 4*K*2*D bytes within shared memory (the
- *     fallback path): K * D <= 16384. A fused fast path is used when D is 4,
- *     8 or 16, SH2 % 32 == 0, SH2 * D <= 4096 and K <= 128.
+ *     generic fallback kernels): K * D <= 16384. Kernel families by shape
+ *     (m2scan_path_for / m2scan_fwd_path_for answer for a shape):
+ *       fused tensor-core kernels: D = 4, 8 or 16, SH2 % 32 == 0,
+ *         32 <= SH2 <= 256, K <= 128;
+ *       wide-state tensor-core kernels: D = 64, SH2 % 128 == 0, K <= 128,
+ *         B * K < 2^31;
+ *       the generic kernels: every other supported shape.
  */
 #ifndef M2SCAN_H
 #define M2SCAN_H
